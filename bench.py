@@ -1,0 +1,416 @@
+#!/usr/bin/env python
+"""Benchmark of the MXFP4 MoE layer hot path on GB300.
+
+One step = one pass of the whole layer over one batch of synthetic input:
+moe_route -> moe_permute -> moe_mxfp4_forward (gather, W13 GEMM + SiLU*up,
+W2 GEMM, combine). Default workload: one decode step with 7 draft tokens
+(T=8, H=4096, E=256, top-6, I=2048).
+
+Timing: W untimed warm-up steps, then exactly K steps between a barrier and
+a device synchronise on both sides. The L2 cache is flushed (a write of twice
+its size) before every step, outside the per-step CUDA events; `value` is
+tokens over the summed per-step device time. `e2e` repeats the step through
+the public API with pinned host buffers: host->device copy of x and logits,
+the three calls, device->host copy of y, all inside the timed region.
+
+Under torchrun each rank runs an independent replica (weak scaling, no
+collective on the data path); rank 0 prints the JSON line with the maximum
+per-rank time.
+
+--impl reference times the float64 CPU oracle on a bounded token sample of
+the same workload (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer tokens/s and % of HBM / MXFP4-tensor roofline; route µs/layer"
+UNIT = "tokens/s"
+DEFAULT_WORKLOAD = "decode_t8_h4096_e256"
+
+
+def per_expert_bytes(H, I):
+    """Prepacked MXFP4 bytes (nibbles + E8M0 scales) of one expert's W13 and W2."""
+    w13 = 2 * I * H // 2 + 2 * I * H // 32
+    w2 = H * I // 2 + H * I // 32
+    return w13, w2
+
+
+def algorithmic(L, ids):
+    """Algorithmic bytes and flops of one step (roofline section)."""
+    T, H, I, E, k = L["T"], L["H"], L["I"], L["E"], L["k"]
+    touched = int(len(np.unique(ids)))
+    P = T * k
+    w13, w2 = per_expert_bytes(H, I)
+    w13_kernel = touched * w13 + P * H * 2 + P * I * 2 * 2        # weights + gathered x rows + h (hi, lo)
+    layer = touched * (w13 + w2) + T * H * 2 + T * E * 4 + T * H * 4   # weights + x + logits + y
+    flops = 6.0 * P * H * I
+    return dict(touched=touched, w13_kernel_bytes=w13_kernel, layer_bytes=layer, flops=flops)
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d.get("hbm_gbs"), d.get("bf16_tflops"), d.get("bf16_tflops_sustained"), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 100 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-i", str(self.index), "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def dist_setup():
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def allreduce_max(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def oracle_sample(L, n_tokens: int, min_seconds: float, max_reps: int = 50):
+    """Time route + forward of the float64 oracle on the first n_tokens tokens."""
+    import oracle
+    tok = np.arange(min(n_tokens, L["T"]), dtype=np.int32)
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        ids, w, _ = oracle.route(L["logits"], L["k"])
+        oracle.forward(L, ids, w, tokens=tok)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= min_seconds or reps >= max_reps:
+            break
+    return len(tok) * reps / el, el, reps, len(tok)
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    import oracle
+    from mxfp4_mixture_experts_top_gb300 import synth
+    L = synth.make_config(args.workload)
+    n_tok = args.ref_tokens
+    for _ in range(args.warmup):
+        oracle_sample(L, n_tok, 0.0, 1)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle_sample(L, n_tok, 0.0, 1)
+        times.append(time.perf_counter() - t0)
+    ms = 1e3 * sum(times) / len(times)
+    value = n_tok / (ms / 1e3)
+    cores = oracle.max_threads()
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "impl": "reference", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic (seeded splitmix64; sizes of the workload)",
+        "config": {"workload": args.workload, "T": L["T"], "H": L["H"], "I": L["I"], "E": L["E"], "k": L["k"],
+                   "l2": "n/a (CPU)"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"route of all {L['T']} tokens + float64 forward of {n_tok} tokens per step"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def time_workload(moe, L, steps, warmup, flush_buf, events_per_step=True):
+    """Time K device steps of one workload; returns per-kernel and per-step times (ms)."""
+    import torch
+    dev = torch.device("cuda")
+    T, H, I, E, k = L["T"], L["H"], L["I"], L["E"], L["k"]
+    x = torch.from_numpy(L["x_bits"].view(np.int16)).to(dev).view(torch.bfloat16)
+    logits = torch.from_numpy(L["logits"]).to(dev)
+    w = tuple(torch.from_numpy(np.ascontiguousarray(L[n])).to(dev) for n in ("w13_q", "w13_s", "w2_q", "w2_s"))
+    layer = moe.MoELayer.create(T, H, I, E, k, *w, block_m=16, device=dev)
+    del w
+    b = layer.bufs
+
+    def step(evs):
+        evs[0].record()
+        moe.route(logits, k, out=(b["ids"], b["w"], b["bm"]))
+        evs[1].record()
+        moe.permute(b["ids"], E, 16, out=b["perm"], error=b["perm_err"])
+        moe.forward_timed(layer.desc, x, layer.packed, b["w"], b["perm"], layer.workspace, b["y"], evs[2:7])
+
+    mk = lambda: [torch.cuda.Event(enable_timing=True) for _ in range(7)]
+    for _ in range(warmup):
+        flush_buf.zero_()
+        step(mk())
+    torch.cuda.synchronize()
+    assert layer.forward_error() == 0, "device error during warm-up"
+    return layer, x, logits, step, mk
+
+
+def summarize(evsets):
+    # events: 0 start, 1 after route, 2 before gather (after permute), 3 after gather, 4 after W13, 5 after W2, 6 after combine
+    keys = ["route", "permute", "gather", "w13", "w2", "combine"]
+    out = {k: [] for k in keys}
+    total = []
+    for ev in evsets:
+        t = [ev[0].elapsed_time(e) for e in ev]
+        out["route"].append(t[1] - t[0])
+        out["permute"].append(t[2] - t[1])
+        out["gather"].append(t[3] - t[2])
+        out["w13"].append(t[4] - t[3])
+        out["w2"].append(t[5] - t[4])
+        out["combine"].append(t[6] - t[5])
+        total.append(t[6])
+    return {k: float(np.mean(v)) for k, v in out.items()}, float(np.sum(total)), [float(v) for v in total]
+
+
+def run_ours(args, world, rank, local):
+    import torch
+    from mxfp4_mixture_experts_top_gb300 import moe, synth
+    moe.load()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    props = torch.cuda.get_device_properties(dev)
+    l2 = int(getattr(props, "L2_cache_size", 0) or 128 * 1024 * 1024)
+    flush_buf = torch.empty(2 * l2 // 4, dtype=torch.float32, device=dev)
+    hbm_peak, bf16_peak, bf16_sus, peak_kind = measured_peaks()
+
+    L = synth.make_config(args.workload)
+    layer, x, logits, step, mk = time_workload(moe, L, args.steps, args.warmup, flush_buf)
+    T, H, I, E, k = L["T"], L["H"], L["I"], L["E"], L["k"]
+
+    visible = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    smi_index = visible.split(",")[local] if visible else str(local)
+    sampler = ClockSampler(smi_index)
+    sampler.start()
+    time.sleep(0.3)
+    for _ in range(max(args.warmup, 20)):       # keep the GPU busy while the sampler starts
+        flush_buf.zero_()
+        step(mk())
+    torch.cuda.synchronize()
+
+    n0 = moe.launch_count()
+    evsets = [mk() for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush_buf.zero_()
+        step(evsets[i])
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    barrier(world)
+    launches = moe.launch_count() - n0
+    clocks = sampler.stop()
+    assert layer.forward_error() == 0, "device error in the timed region"
+
+    per_kernel, total_ms, step_ms = summarize(evsets)
+    total_ms = allreduce_max(total_ms, world)
+    ms_per_step = total_ms / args.steps
+    value = world * T / (ms_per_step / 1e3)
+
+    ids = layer.bufs["ids"].cpu().numpy()
+    alg = algorithmic(L, ids)
+    w13_ms = per_kernel["w13"]
+    achieved = alg["w13_kernel_bytes"] / (w13_ms / 1e3) / 1e9
+    roofline = {"kernel": "moe_gemm_kernel<W13> (grouped W13 GEMM + SiLU*up)", "bound": "hbm",
+                "achieved": achieved, "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
+                "peak_source": f"{peak_kind} hbm_gbs", "traffic": args.w13_traffic,
+                "bytes_per_launch": alg["w13_kernel_bytes"], "avg_launch_ms": w13_ms}
+    layer_gbs = alg["layer_bytes"] / (ms_per_step / 1e3) / 1e9
+    layer_tflops = alg["flops"] / (ms_per_step / 1e3) / 1e12
+
+    # ---- end to end through the public API with pinned host buffers
+    x_host = torch.from_numpy(L["x_bits"].view(np.int16)).view(torch.bfloat16).pin_memory()
+    lg_host = torch.from_numpy(L["logits"]).pin_memory()
+    y_host = torch.empty((T, H), dtype=torch.float32).pin_memory()
+    x_dev = torch.empty_like(x)
+    lg_dev = torch.empty_like(logits)
+    for _ in range(args.warmup):
+        x_dev.copy_(x_host, non_blocking=True)
+        lg_dev.copy_(lg_host, non_blocking=True)
+        y = layer(x_dev, lg_dev)
+        y_host.copy_(y, non_blocking=True)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_ms = 0.0
+    for _ in range(args.steps):
+        flush_buf.zero_()
+        e0.record()
+        x_dev.copy_(x_host, non_blocking=True)
+        lg_dev.copy_(lg_host, non_blocking=True)
+        y = layer(x_dev, lg_dev)
+        y_host.copy_(y, non_blocking=True)
+        e1.record()
+        e1.synchronize()
+        e2e_ms += e0.elapsed_time(e1)
+    e2e_ms = allreduce_max(e2e_ms, world) / args.steps
+    e2e = {"value": world * T / (e2e_ms / 1e3), "unit": UNIT, "ms_per_step": e2e_ms,
+           "h2d_bytes_per_step": T * H * 2 + T * E * 4, "d2h_bytes_per_step": T * H * 4}
+
+    # ---- other workloads (parity-test shapes), short runs for the per-regime picture
+    per_config = {}
+    if args.all_configs and rank == 0:
+        for name in synth.CONFIG_ORDER:
+            if name == args.workload or name.startswith("tiny"):
+                continue
+            Lc = synth.make_config(name)
+            lay_c, _, _, step_c, mk_c = time_workload(moe, Lc, 10, 3, flush_buf)
+            evs = [mk_c() for _ in range(10)]
+            for i in range(10):
+                flush_buf.zero_()
+                step_c(evs[i])
+            torch.cuda.synchronize()
+            pk, tot, _ = summarize(evs)
+            ms = tot / 10
+            a = algorithmic(Lc, lay_c.bufs["ids"].cpu().numpy())
+            per_config[name] = {
+                "tokens_per_s": Lc["T"] / (ms / 1e3), "ms_per_step": ms, "touched_experts": a["touched"],
+                "layer_hbm_frac": a["layer_bytes"] / (ms / 1e3) / 1e9 / hbm_peak,
+                "layer_bf16_tensor_frac": a["flops"] / (ms / 1e3) / 1e12 / bf16_sus,
+                "w13_hbm_frac": a["w13_kernel_bytes"] / (pk["w13"] / 1e3) / 1e9 / hbm_peak,
+                "route_us": 1e3 * (pk["route"] + pk["permute"]), "kernel_ms": pk}
+            del lay_c
+            torch.cuda.empty_cache()
+
+    # ---- CPU baseline: the oracle on the host cores, bounded sample
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        import oracle
+        v, el, reps, ntok = oracle_sample(L, args.ref_tokens, args.cpu_seconds)
+        cpu = {"value": v, "unit": UNIT, "cores": oracle.max_threads(), "kind": "oracle",
+               "sample": f"{reps} x (route of all {T} tokens + float64 forward of {ntok} tokens), {el:.1f} s"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16 (MXFP4 weights decoded exactly to bf16; fp32 accumulate)",
+            "data": "synthetic (seeded splitmix64 inputs of the workload's shapes and distributions)",
+            "config": {"workload": args.workload, "T": T, "H": H, "I": I, "E": E, "k": k, "block_m": 16,
+                       "touched_experts": alg["touched"], "l2": f"flushed before every step ({2 * l2 >> 20} MiB write)"},
+            "route_us_per_layer": 1e3 * (per_kernel["route"] + per_kernel["permute"]),
+            "kernel_ms": per_kernel,
+            "layer_roofline": {"bytes": alg["layer_bytes"], "achieved_gbs": layer_gbs, "hbm_frac": layer_gbs / hbm_peak,
+                               "flops": alg["flops"], "achieved_tflops": layer_tflops,
+                               "bf16_frac_sustained": layer_tflops / bf16_sus},
+            "roofline": roofline,
+            "e2e": e2e,
+            "gpu_launches": launches,
+            "wall_s_timed": wall,
+            "clocks": clocks,
+            "cpu_baseline": cpu,
+        }
+        if per_config:
+            line["per_config"] = per_config
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--all-configs", action="store_true", help="also time the other 4096-wide workloads")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--ref-tokens", type=int, default=4)
+    ap.add_argument("--w13-traffic", type=float, default=None,
+                    help="DRAM bytes per W13 launch from an ncu capture of this workload (reported as-is)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_ours(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,220 @@
+/*
+ * moe_mxfp4.h — C ABI of the GB300 (sm_103a) MXFP4 mixture-of-experts layer.
+ *
+ * The layer (one call of each, in order, on one stream):
+ *   moe_route          top-k expert routing over fp32 router logits
+ *   moe_permute        per-expert histogram, prefix offsets, block-padded
+ *                      offsets and the stable token permutation
+ *   moe_mxfp4_forward  gather -> grouped W13 GEMM with SiLU(gate)*up ->
+ *                      grouped W2 GEMM -> routing-weighted combine
+ * plus the one-time weight reorder moe_mxfp4_prepack.
+ *
+ * The method follows "DeepSeek V4 Flash 单卡 MI300X: 10 个 overlay 起家..."
+ * (txtmix.com): §一 (top-6 of 256 experts; routing, then the expert GEMMs),
+ * §三 (MXFP4 expert weights with a shared E8M0 scale; the routing bitmatrix
+ * whose padding lanes are masked by the logical block size; SiLU fused with a
+ * gate/up pair), §九 (the optional SwiGLU clamp). Element formats are the OCP
+ * Microscaling (MX) v1.0 E2M1 and E8M0 encodings.
+ *
+ * Conventions for every entry point:
+ *   - Pointers named d_* are DEVICE pointers (cudaMalloc'd or equivalent) on
+ *     the current device; the caller allocates and owns all of them. The
+ *     library never allocates, frees or keeps device memory between calls.
+ *     Every device pointer must be 16-byte aligned.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream). All work is enqueued on that stream only; no call
+ *     synchronises the device or copies between host and device (except
+ *     moe_read_device_error), so route/permute/forward can be captured in a
+ *     CUDA graph.
+ *   - Argument errors are detected on the host before any launch and return
+ *     MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED / MOE_ERR_MISALIGNED /
+ *     MOE_ERR_WORKSPACE. A failed launch returns MOE_ERR_CUDA. Faults found on
+ *     the device (an expert id outside [0,E), a pipeline wait that ran out of
+ *     time) never trap: the kernel records a moe_status_t code in a device
+ *     error word and skips the faulty access; moe_read_device_error reads it.
+ *   - T == 0 is a valid no-op. Logits must be finite and scale bytes must not
+ *     be 0xFF (E8M0 NaN); outside these preconditions results are unspecified
+ *     but no out-of-bounds access happens.
+ */
+#ifndef MOE_MXFP4_H
+#define MOE_MXFP4_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MOE_ABI_VERSION 1
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,   /* bad size, null pointer, k > E, ...          */
+    MOE_ERR_UNSUPPORTED = 2,   /* valid but outside the shapes this build runs */
+    MOE_ERR_MISALIGNED = 3,    /* a pointer is not 16-byte aligned             */
+    MOE_ERR_WORKSPACE = 4,     /* workspace or packed buffer too small         */
+    MOE_ERR_CUDA = 5,          /* a CUDA runtime/driver call or launch failed  */
+    MOE_ERR_DEVICE = 6,        /* device-detected bad input (expert id range)  */
+    MOE_ERR_TIMEOUT = 7        /* a bounded device-side wait gave up           */
+} moe_status_t;
+
+/* Shapes of one MoE layer.
+ *   T tokens, H hidden width, I expert intermediate width, E experts, k
+ *   experts per token, block_m the row alignment of each expert segment in
+ *   the permutation (16, 32, 64 or 128).
+ *   swiglu_limit > 0 enables the clamp gate = min(gate, L),
+ *   up = clamp(up, -L, L) before SiLU(gate) * up; <= 0 disables it.
+ *   flags: reserved, must be 0.
+ * Supported: 1 <= k <= min(E, 32), E <= 1024, H and I multiples of 128. */
+typedef struct moe_layer_desc {
+    int T, H, I, E, k, block_m;
+    float swiglu_limit;
+    unsigned flags;
+} moe_layer_desc;
+
+/* ABI version of the loaded library (MOE_ABI_VERSION at build time). */
+int moe_abi_version(void);
+
+/* Static description of a status code. */
+const char *moe_status_string(moe_status_t status);
+
+/*
+ * Routing (txtmix.com §一: every token picks k of E experts from its router
+ * scores; §三: the routing bitmatrix).
+ *   d_logits    fp32 [T, E] row-major, finite.
+ *   d_topk_ids  int32 [T, k] out: the k largest logits of each row in
+ *               descending order; equal logits go to the lower expert index
+ *               and -0.0 equals +0.0. Bit-exact with the oracle.
+ *   d_topk_w    fp32 [T, k] out: softmax over the row restricted to the chosen
+ *               k and renormalised (sums to 1).
+ *   d_bitmatrix uint32 [T, ceil(E/32)] out, may be NULL: bit (e % 32) of word
+ *               e / 32 set iff expert e was chosen; bits >= E are 0.
+ * Supported: E <= 1024, 1 <= k <= min(E, 32).
+ */
+moe_status_t moe_route(const float *d_logits, int T, int E, int k,
+                       int32_t *d_topk_ids, float *d_topk_w, uint32_t *d_bitmatrix,
+                       void *stream);
+
+/* Rows of the padded permutation: T*k + min(E, T*k) * (block_m - 1). */
+int64_t moe_permute_rows_capacity(int T, int E, int k, int block_m);
+
+/*
+ * Permutation (txtmix.com §三: the per-expert histogram whose padding lanes
+ * are masked by the logical block size, so lanes past the T*k real (token,
+ * slot) pairs never count). Pair p = t*k + j is token t's j-th choice.
+ *   d_topk_ids       int32 [T, k] in (from moe_route).
+ *   d_counts         int32 [E] out: pairs routed to each expert.
+ *   d_offsets        int32 [E+1] out: exclusive prefix sum of counts.
+ *   d_padded_offsets int32 [E+1] out: exclusive prefix sum of counts rounded
+ *                    up to block_m.
+ *   d_row_to_pair    int32 [moe_permute_rows_capacity(...)] out: the rows of
+ *                    expert e are padded[e] .. padded[e]+counts[e]-1 holding
+ *                    its pairs in ascending pair (= token) order; all other
+ *                    rows, padding and tail, hold -1.
+ *   d_pair_to_row    int32 [T*k] out: inverse map.
+ *   d_error          int32 [1] device error word, may be NULL: set to
+ *                    MOE_ERR_DEVICE if an id is outside [0, E) (that pair is
+ *                    skipped and its pair_to_row entry is -1).
+ * All integer outputs are bit-exact with the oracle. Runs as one thread block.
+ */
+moe_status_t moe_permute(const int32_t *d_topk_ids, int T, int E, int k, int block_m,
+                         int32_t *d_counts, int32_t *d_offsets, int32_t *d_padded_offsets,
+                         int32_t *d_row_to_pair, int32_t *d_pair_to_row, int32_t *d_error,
+                         void *stream);
+
+/* Bytes of the prepacked weight buffer for desc (T is ignored). */
+size_t moe_mxfp4_packed_bytes(const moe_layer_desc *desc);
+
+/*
+ * One-time reorder of canonical MXFP4 weights into the kernels' tile order
+ * (same byte count). Canonical inputs (element 2j of a row in the low nibble
+ * of byte j; one E8M0 byte per 32 consecutive K elements):
+ *   d_w13_q uint8 [E, 2I, H/2], d_w13_s uint8 [E, 2I, H/32]
+ *           rows [0, I) are the gate projection (W1), rows [I, 2I) the up
+ *           projection (W3);
+ *   d_w2_q  uint8 [E, H, I/2],  d_w2_s  uint8 [E, H, I/32].
+ * d_packed must hold moe_mxfp4_packed_bytes(desc) bytes. Each 128-row tile
+ * of W13 pairs 64 gate rows with their 64 up rows (the gate/up interleave of
+ * txtmix.com §三).
+ */
+moe_status_t moe_mxfp4_prepack(const moe_layer_desc *desc,
+                               const uint8_t *d_w13_q, const uint8_t *d_w13_s,
+                               const uint8_t *d_w2_q, const uint8_t *d_w2_s,
+                               void *d_packed, size_t packed_bytes, void *stream);
+
+/*
+ * Decode prepacked weights of one expert back to dense bfloat16 in canonical
+ * row order (exact: every E2M1 x E8M0 product is a bfloat16 value). Uses the
+ * same on-chip decoder as the GEMMs.
+ *   which 0: W13, d_out uint16 (bf16 bits) [2I, H]; which 1: W2, [H, I].
+ */
+moe_status_t moe_mxfp4_dequant_bf16(const moe_layer_desc *desc, const void *d_packed,
+                                    int which, int expert, uint16_t *d_out, void *stream);
+
+/* Workspace bytes moe_mxfp4_forward needs for desc (all of T, H, I, E, k,
+ * block_m matter). The first 256 bytes hold the forward's device error word. */
+size_t moe_mxfp4_workspace_bytes(const moe_layer_desc *desc);
+
+/*
+ * Layer output (txtmix.com §三: grouped MXFP4 expert GEMMs with fused SiLU;
+ * §九: optional clamp). For token t and slot j, e = topk_ids[t, j]:
+ *   gate = W1_e x_t, up = W3_e x_t           (K = H, MXFP4 weights)
+ *   a = SiLU(gate) * up                      (clamped first if enabled)
+ *   o = W2_e a                               (K = I)
+ *   y[t] = sum_j topk_w[t, j] * o_j          (slots in ascending order)
+ * Inputs:
+ *   d_x              bf16 bits [T, H] row-major.
+ *   d_packed         from moe_mxfp4_prepack.
+ *   d_topk_w         fp32 [T, k] (from moe_route).
+ *   d_offsets, d_padded_offsets, d_row_to_pair   from moe_permute.
+ * Output:
+ *   d_y              fp32 [T, H], fully overwritten.
+ * d_workspace: moe_mxfp4_workspace_bytes(desc) bytes, contents need not be
+ * initialised; the call resets its device error word.
+ * Numerics: weights decoded exactly to bf16 on chip; bf16 x bf16 tensor-core
+ * products accumulated in fp32; the SiLU product kept as a two-term bf16 sum
+ * for the second GEMM; output fp32. Result within 2e-2 * rms of the float64
+ * oracle (measured errors are far smaller).
+ * Launches 4 kernels on `stream`; deterministic (bit-identical reruns).
+ */
+moe_status_t moe_mxfp4_forward(const moe_layer_desc *desc, const uint16_t *d_x,
+                               const void *d_packed, const float *d_topk_w,
+                               const int32_t *d_offsets, const int32_t *d_padded_offsets,
+                               const int32_t *d_row_to_pair, float *d_y,
+                               void *d_workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * moe_mxfp4_forward with timing: identical work, plus cudaEventRecord of
+ * events[0..4] (cudaEvent_t passed as void*, created by the caller on this
+ * device) on `stream` before the gather, after the gather, after the W13 GEMM,
+ * after the W2 GEMM and after the combine. NULL entries are skipped.
+ */
+moe_status_t moe_mxfp4_forward_timed(const moe_layer_desc *desc, const uint16_t *d_x,
+                                     const void *d_packed, const float *d_topk_w,
+                                     const int32_t *d_offsets, const int32_t *d_padded_offsets,
+                                     const int32_t *d_row_to_pair, float *d_y,
+                                     void *d_workspace, size_t workspace_bytes,
+                                     void *const *events, void *stream);
+
+/* Byte offsets of the forward's intermediates inside the workspace, for
+ * inspection: out[0] error word, out[1] gathered activations (bf16 [R, H]),
+ * out[2] SiLU product high part (bf16 [R, I]), out[3] low part (bf16 [R, I]),
+ * out[4] per-pair W2 outputs (fp32 [T*k, H]), out[5] total bytes;
+ * R = moe_permute_rows_capacity(T, E, k, block_m). */
+moe_status_t moe_mxfp4_workspace_layout(const moe_layer_desc *desc, size_t out[6]);
+
+/*
+ * Read and clear a device error word (the d_error of moe_permute or the
+ * first word of a forward workspace). Synchronises `stream`. Writes the
+ * recorded moe_status_t value (MOE_OK if none) to *code.
+ */
+moe_status_t moe_read_device_error(void *d_error_word, int *code, void *stream);
+
+/* Number of kernels launched by this library since load (all entry points). */
+uint64_t moe_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_MXFP4_H */

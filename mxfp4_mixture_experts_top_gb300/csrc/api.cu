@@ -1,0 +1,322 @@
+// Host side of the C ABI: argument validation, tensor-map encoding and
+// caching, workspace layout, launches. Every entry point enqueues on the
+// caller's stream only and returns before the device work finishes.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <tuple>
+
+#include "../../include/moe_mxfp4.h"
+#include "moe_internal.h"
+#include "mxfp4_tile.cuh"
+
+namespace moe {
+
+static std::atomic<unsigned long long> g_launches{0};
+void note_launch(int n) { g_launches.fetch_add((unsigned long long)n, std::memory_order_relaxed); }
+
+namespace {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn()
+{
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+struct MapKey {
+    int dev;
+    const void *ptr;
+    uint64_t inner, rows;
+    bool operator<(const MapKey &o) const
+    {
+        return std::tie(dev, ptr, inner, rows) < std::tie(o.dev, o.ptr, o.inner, o.rows);
+    }
+};
+
+struct MapEntry {
+    CUtensorMap map;
+};
+
+std::mutex g_map_mu;
+std::map<MapKey, MapEntry> g_maps;
+
+// 2-D bf16 tensor [rows, inner] (inner contiguous), box 64 x 16, 128-byte swizzle.
+const CUtensorMap *bf16_rows_map(const void *ptr, uint64_t inner, uint64_t rows, moe_status_t *st)
+{
+    int dev = 0;
+    cudaGetDevice(&dev);
+    MapKey key{dev, ptr, inner, rows};
+    std::lock_guard<std::mutex> lk(g_map_mu);
+    auto it = g_maps.find(key);
+    if (it != g_maps.end()) return &it->second.map;
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) { *st = MOE_ERR_CUDA; return nullptr; }
+    if (g_maps.size() > 4096) g_maps.clear();
+    MapEntry ent;
+    cuuint64_t dims[2] = {inner, rows};
+    cuuint64_t strides[1] = {inner * 2};
+    cuuint32_t box[2] = {64, 16};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(&ent.map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) { *st = MOE_ERR_CUDA; return nullptr; }
+    auto res = g_maps.emplace(key, ent);
+    return &res.first->second.map;
+}
+
+int sm_count()
+{
+    int dev = 0, n = 0;
+    cudaGetDevice(&dev);
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 1;
+    return n;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+moe_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+moe_status_t check_desc(const moe_layer_desc *d)
+{
+    if (!d) return MOE_ERR_INVALID_ARG;
+    if (d->T < 0 || d->H <= 0 || d->I <= 0 || d->E <= 0 || d->k <= 0 || d->k > d->E) return MOE_ERR_INVALID_ARG;
+    if (d->flags != 0) return MOE_ERR_INVALID_ARG;
+    if (d->E > 1024 || d->k > 32) return MOE_ERR_UNSUPPORTED;
+    if (d->H % 128 || d->I % 128) return MOE_ERR_UNSUPPORTED;
+    if (d->block_m != 16 && d->block_m != 32 && d->block_m != 64 && d->block_m != 128) return MOE_ERR_UNSUPPORTED;
+    if ((int64_t)d->T * d->k > (int64_t)INT32_MAX / 2) return MOE_ERR_UNSUPPORTED;
+    return MOE_OK;
+}
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+struct Layout {
+    size_t err, xp, hhi, hlo, staging, total;
+};
+
+Layout workspace_layout(const moe_layer_desc *d)
+{
+    const int64_t P = (int64_t)d->T * d->k;
+    const int64_t R = moe_permute_rows_capacity(d->T, d->E, d->k, d->block_m);
+    Layout L;
+    L.err = 0;
+    L.xp = 1024;
+    L.hhi = align_up(L.xp + (size_t)R * d->H * 2, 1024);
+    L.hlo = align_up(L.hhi + (size_t)R * d->I * 2, 1024);
+    L.staging = align_up(L.hlo + (size_t)R * d->I * 2, 1024);
+    L.total = align_up(L.staging + (size_t)P * d->H * 4, 1024);
+    return L;
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+int moe_abi_version(void) { return MOE_ABI_VERSION; }
+
+const char *moe_status_string(moe_status_t s)
+{
+    switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported shape";
+    case MOE_ERR_MISALIGNED: return "pointer not 16-byte aligned";
+    case MOE_ERR_WORKSPACE: return "workspace or packed buffer too small";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_DEVICE: return "device-detected invalid input (expert id out of range)";
+    case MOE_ERR_TIMEOUT: return "device-side wait timed out";
+    }
+    return "unknown status";
+}
+
+uint64_t moe_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+moe_status_t moe_route(const float *d_logits, int T, int E, int k, int32_t *d_topk_ids, float *d_topk_w,
+                       uint32_t *d_bitmatrix, void *stream)
+{
+    if (T < 0 || E <= 0 || k <= 0 || k > E) return MOE_ERR_INVALID_ARG;
+    if (E > 1024 || k > 32) return MOE_ERR_UNSUPPORTED;
+    if (T == 0) return MOE_OK;
+    if (!d_logits || !d_topk_ids || !d_topk_w) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(d_logits) || !aligned16(d_topk_ids) || !aligned16(d_topk_w) ||
+        (d_bitmatrix && !aligned16(d_bitmatrix)))
+        return MOE_ERR_MISALIGNED;
+    return from_cuda(launch_route(d_logits, T, E, k, d_topk_ids, d_topk_w, d_bitmatrix, (cudaStream_t)stream));
+}
+
+int64_t moe_permute_rows_capacity(int T, int E, int k, int block_m)
+{
+    if (T < 0 || E <= 0 || k <= 0 || block_m <= 0) return 0;
+    const int64_t P = (int64_t)T * k;
+    const int64_t used = P < E ? P : E;
+    return P + used * (block_m - 1);
+}
+
+moe_status_t moe_permute(const int32_t *d_topk_ids, int T, int E, int k, int block_m, int32_t *d_counts,
+                         int32_t *d_offsets, int32_t *d_padded_offsets, int32_t *d_row_to_pair,
+                         int32_t *d_pair_to_row, int32_t *d_error, void *stream)
+{
+    if (T < 0 || E <= 0 || k <= 0 || k > E) return MOE_ERR_INVALID_ARG;
+    if (E > 1024 || k > 32) return MOE_ERR_UNSUPPORTED;
+    if (block_m != 16 && block_m != 32 && block_m != 64 && block_m != 128) return MOE_ERR_UNSUPPORTED;
+    if ((int64_t)T * k > (int64_t)INT32_MAX / 2) return MOE_ERR_UNSUPPORTED;
+    if (!d_counts || !d_offsets || !d_padded_offsets) return MOE_ERR_INVALID_ARG;
+    if (T > 0 && (!d_topk_ids || !d_row_to_pair || !d_pair_to_row)) return MOE_ERR_INVALID_ARG;
+    const void *ptrs[] = {d_topk_ids, d_counts, d_offsets, d_padded_offsets, d_row_to_pair, d_pair_to_row, d_error};
+    for (const void *p : ptrs)
+        if (p && !aligned16(p)) return MOE_ERR_MISALIGNED;
+    const int64_t cap = moe_permute_rows_capacity(T, E, k, block_m);
+    return from_cuda(launch_permute(d_topk_ids, T, E, k, block_m, d_counts, d_offsets, d_padded_offsets,
+                                    d_row_to_pair, cap, d_pair_to_row, d_error, (cudaStream_t)stream));
+}
+
+size_t moe_mxfp4_packed_bytes(const moe_layer_desc *d)
+{
+    if (!d || d->E <= 0 || d->H <= 0 || d->I <= 0 || d->H % 128 || d->I % 128) return 0;
+    return packed_w13_bytes(d->E, d->H, d->I) + packed_w2_bytes(d->E, d->H, d->I);
+}
+
+moe_status_t moe_mxfp4_prepack(const moe_layer_desc *d, const uint8_t *d_w13_q, const uint8_t *d_w13_s,
+                               const uint8_t *d_w2_q, const uint8_t *d_w2_s, void *d_packed, size_t packed_bytes,
+                               void *stream)
+{
+    moe_status_t st = check_desc(d);
+    if (st != MOE_OK) return st;
+    if (!d_w13_q || !d_w13_s || !d_w2_q || !d_w2_s || !d_packed) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(d_w13_q) || !aligned16(d_w13_s) || !aligned16(d_w2_q) || !aligned16(d_w2_s) ||
+        !aligned16(d_packed))
+        return MOE_ERR_MISALIGNED;
+    if (packed_bytes < moe_mxfp4_packed_bytes(d)) return MOE_ERR_WORKSPACE;
+    return from_cuda(launch_prepack(d_w13_q, d_w13_s, d_w2_q, d_w2_s, d->E, d->H, d->I,
+                                    static_cast<uint8_t *>(d_packed), (cudaStream_t)stream));
+}
+
+moe_status_t moe_mxfp4_dequant_bf16(const moe_layer_desc *d, const void *d_packed, int which, int expert,
+                                    uint16_t *d_out, void *stream)
+{
+    moe_status_t st = check_desc(d);
+    if (st != MOE_OK) return st;
+    if (!d_packed || !d_out || (which != 0 && which != 1) || expert < 0 || expert >= d->E)
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned16(d_packed) || !aligned16(d_out)) return MOE_ERR_MISALIGNED;
+    return from_cuda(launch_dequant(static_cast<const uint8_t *>(d_packed), which, expert, d->E, d->H, d->I, d_out,
+                                    (cudaStream_t)stream));
+}
+
+size_t moe_mxfp4_workspace_bytes(const moe_layer_desc *d)
+{
+    if (check_desc(d) != MOE_OK) return 0;
+    return workspace_layout(d).total;
+}
+
+moe_status_t moe_mxfp4_workspace_layout(const moe_layer_desc *d, size_t out[6])
+{
+    moe_status_t st = check_desc(d);
+    if (st != MOE_OK) return st;
+    if (!out) return MOE_ERR_INVALID_ARG;
+    Layout L = workspace_layout(d);
+    out[0] = L.err;
+    out[1] = L.xp;
+    out[2] = L.hhi;
+    out[3] = L.hlo;
+    out[4] = L.staging;
+    out[5] = L.total;
+    return MOE_OK;
+}
+
+moe_status_t moe_mxfp4_forward_timed(const moe_layer_desc *d, const uint16_t *d_x, const void *d_packed,
+                                     const float *d_topk_w, const int32_t *d_offsets,
+                                     const int32_t *d_padded_offsets, const int32_t *d_row_to_pair, float *d_y,
+                                     void *d_workspace, size_t workspace_bytes, void *const *events, void *stream)
+{
+    moe_status_t st = check_desc(d);
+    if (st != MOE_OK) return st;
+    if (d->T == 0) return MOE_OK;
+    const void *ptrs[] = {d_x, d_packed, d_topk_w, d_offsets, d_padded_offsets, d_row_to_pair, d_y, d_workspace};
+    for (const void *p : ptrs)
+        if (!p) return MOE_ERR_INVALID_ARG;
+    for (const void *p : ptrs)
+        if (!aligned16(p)) return MOE_ERR_MISALIGNED;
+    Layout L = workspace_layout(d);
+    if (workspace_bytes < L.total) return MOE_ERR_WORKSPACE;
+    cudaStream_t s = (cudaStream_t)stream;
+    uint8_t *ws = static_cast<uint8_t *>(d_workspace);
+    const int64_t R = moe_permute_rows_capacity(d->T, d->E, d->k, d->block_m);
+
+    ForwardArgs a{};
+    a.T = d->T;
+    a.H = d->H;
+    a.I = d->I;
+    a.E = d->E;
+    a.k = d->k;
+    a.block_m = d->block_m;
+    a.swiglu_limit = d->swiglu_limit;
+    a.rows_cap = R;
+    a.x = d_x;
+    a.packed = static_cast<const uint8_t *>(d_packed);
+    a.topk_w = d_topk_w;
+    a.offsets = d_offsets;
+    a.padded = d_padded_offsets;
+    a.row_to_pair = d_row_to_pair;
+    a.y = d_y;
+    a.dev_error = reinterpret_cast<int32_t *>(ws + L.err);
+    a.xp = reinterpret_cast<uint16_t *>(ws + L.xp);
+    a.h_hi = reinterpret_cast<uint16_t *>(ws + L.hhi);
+    a.h_lo = reinterpret_cast<uint16_t *>(ws + L.hlo);
+    a.staging = reinterpret_cast<float *>(ws + L.staging);
+    a.num_sms = sm_count();
+    a.events = events;
+    a.tmap_xp = bf16_rows_map(a.xp, (uint64_t)d->H, (uint64_t)R, &st);
+    if (!a.tmap_xp) return st;
+    a.tmap_hhi = bf16_rows_map(a.h_hi, (uint64_t)d->I, (uint64_t)R, &st);
+    if (!a.tmap_hhi) return st;
+    a.tmap_hlo = bf16_rows_map(a.h_lo, (uint64_t)d->I, (uint64_t)R, &st);
+    if (!a.tmap_hlo) return st;
+    if (cudaMemsetAsync(a.dev_error, 0, sizeof(int32_t), s) != cudaSuccess) return MOE_ERR_CUDA;
+    return from_cuda(launch_forward(a, s));
+}
+
+moe_status_t moe_mxfp4_forward(const moe_layer_desc *d, const uint16_t *d_x, const void *d_packed,
+                               const float *d_topk_w, const int32_t *d_offsets, const int32_t *d_padded_offsets,
+                               const int32_t *d_row_to_pair, float *d_y, void *d_workspace, size_t workspace_bytes,
+                               void *stream)
+{
+    return moe_mxfp4_forward_timed(d, d_x, d_packed, d_topk_w, d_offsets, d_padded_offsets, d_row_to_pair, d_y,
+                                   d_workspace, workspace_bytes, nullptr, stream);
+}
+
+moe_status_t moe_read_device_error(void *d_error_word, int *code, void *stream)
+{
+    if (!d_error_word || !code) return MOE_ERR_INVALID_ARG;
+    cudaStream_t s = (cudaStream_t)stream;
+    int v = 0;
+    if (cudaMemcpyAsync(&v, d_error_word, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaMemsetAsync(d_error_word, 0, sizeof(int), s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+    *code = v;
+    return MOE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,56 @@
+// Internal declarations shared by the library's translation units.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+namespace moe {
+
+// Device error codes (same values as moe_status_t in the public header).
+constexpr int DEV_ERR_ID_RANGE = 6;   // MOE_ERR_DEVICE
+constexpr int DEV_ERR_TIMEOUT = 7;    // MOE_ERR_TIMEOUT
+
+// Bounded pipeline waits give up after this much wall time.
+constexpr unsigned long long WAIT_LIMIT_NS = 2000000000ull;   // 2 s
+
+void note_launch(int n);
+
+cudaError_t launch_route(const float *logits, int T, int E, int k, int32_t *ids, float *w,
+                         uint32_t *bitmatrix, cudaStream_t s);
+
+cudaError_t launch_permute(const int32_t *ids, int T, int E, int k, int block_m, int32_t *counts,
+                           int32_t *offsets, int32_t *padded, int32_t *row_to_pair, int64_t rows_cap,
+                           int32_t *pair_to_row, int32_t *dev_error, cudaStream_t s);
+
+cudaError_t launch_prepack(const uint8_t *w13_q, const uint8_t *w13_s, const uint8_t *w2_q,
+                           const uint8_t *w2_s, int E, int H, int I, uint8_t *packed, cudaStream_t s);
+
+cudaError_t launch_dequant(const uint8_t *packed, int which, int expert, int E, int H, int I,
+                           uint16_t *out, cudaStream_t s);
+
+// Offsets (bytes) of the two prepacked matrices inside the packed buffer.
+size_t packed_w13_bytes(int E, int H, int I);
+size_t packed_w2_bytes(int E, int H, int I);
+
+struct ForwardArgs {
+    int T, H, I, E, k, block_m;
+    float swiglu_limit;
+    int64_t rows_cap;
+    const uint16_t *x;
+    const uint8_t *packed;
+    const float *topk_w;
+    const int32_t *offsets, *padded, *row_to_pair;
+    float *y;
+    int32_t *dev_error;
+    uint16_t *xp, *h_hi, *h_lo;
+    float *staging;
+    const CUtensorMap *tmap_xp, *tmap_hhi, *tmap_hlo;
+    int num_sms;
+    void *const *events;   // optional: 5 cudaEvent_t recorded between kernels
+};
+
+cudaError_t launch_forward(const ForwardArgs &a, cudaStream_t s);
+
+}  // namespace moe

@@ -1,0 +1,158 @@
+// Per-expert histogram, prefix offsets, block-padded offsets and the stable
+// token permutation, in one thread block.
+//
+// Method: "DeepSeek V4 Flash 单卡 MI300X" (txtmix.com) §三 — the expert
+// histogram is built over a padded, block-aligned layout, and lanes past the
+// logical block (here: past the warp's own range of real pairs, and past
+// T*k) must be masked, or they inject non-existent expert indices into the
+// routing (the page's fix masks with offs_local < BLOCK_SIZE in addition to
+// the global bound). Every lane below carries that two-sided mask.
+//
+// Pairs p = t*k + j are split into 32 contiguous warp ranges. Phase 1: each
+// warp histograms its range into its own shared-memory row with
+// __match_any_sync (one leader per distinct expert per 32 lanes). Phase 2:
+// per expert, a scan over the warp rows turns counts into warp bases; a block
+// scan over experts gives offsets and padded offsets. Phase 3: each warp walks
+// its range again in order; a pair's row is padded[e] + warp base + (pairs of
+// e earlier in the range), so rows of one expert come out in ascending pair
+// order (stable). Phase 4 writes -1 into padding and tail rows.
+#include <cstdint>
+
+#include "moe_internal.h"
+
+namespace moe {
+
+constexpr int PERM_THREADS = 1024;
+constexpr int PERM_WARPS = PERM_THREADS / 32;
+
+// Inclusive block-wide scan of one int per thread (1024 threads).
+__device__ __forceinline__ int block_inclusive_scan(int v, int *warp_tot)
+{
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        int n = __shfl_up_sync(0xFFFFFFFFu, v, o);
+        if (lane >= o) v += n;
+    }
+    if (lane == 31) warp_tot[wid] = v;
+    __syncthreads();
+    if (wid == 0) {
+        int t = warp_tot[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int n = __shfl_up_sync(0xFFFFFFFFu, t, o);
+            if (lane >= o) t += n;
+        }
+        warp_tot[lane] = t;
+    }
+    __syncthreads();
+    int r = v + (wid > 0 ? warp_tot[wid - 1] : 0);
+    __syncthreads();
+    return r;
+}
+
+__global__ void __launch_bounds__(PERM_THREADS, 1)
+permute_kernel(const int32_t *__restrict__ ids, int T, int E, int k, int block_m,
+               int32_t *__restrict__ counts, int32_t *__restrict__ offsets, int32_t *__restrict__ padded,
+               int32_t *__restrict__ row_to_pair, int64_t rows_cap, int32_t *__restrict__ pair_to_row,
+               int32_t *__restrict__ dev_error)
+{
+    extern __shared__ int smem[];
+    int *hist = smem;                                  // [PERM_WARPS][E]
+    int *cnt = hist + PERM_WARPS * E;                  // [E]
+    int *pad_start = cnt + E;                          // [E + 1]
+    int *warp_tot = pad_start + E + 1;                 // [32]
+    __shared__ int s_err;
+
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    const int64_t P = (int64_t)T * k;
+    const int64_t lo = P * wid / PERM_WARPS, hi = P * (wid + 1) / PERM_WARPS;
+    const unsigned lt_mask = (1u << lane) - 1u;
+
+    if (tid == 0) s_err = 0;
+    for (int i = tid; i < PERM_WARPS * E; i += PERM_THREADS) hist[i] = 0;
+    __syncthreads();
+
+    // Phase 1: per-warp histogram; lanes past this warp's range are masked.
+    int *my = hist + wid * E;
+    for (int64_t base = lo; base < hi; base += 32) {
+        int64_t p = base + lane;
+        bool valid = p < hi;                           // logical-block mask (never past T*k)
+        int e = valid ? ids[p] : -1;
+        if (valid && (e < 0 || e >= E)) { e = -1; s_err = 1; }
+        unsigned m = __match_any_sync(0xFFFFFFFFu, e);
+        if (e >= 0 && (m & lt_mask) == 0u) my[e] += __popc(m);
+    }
+    __syncthreads();
+
+    // Phase 2: warp bases per expert, then offsets / padded offsets.
+    int c = 0, pc = 0;
+    for (int e = tid; e < E; e += PERM_THREADS) {      // E <= 1024: at most one expert per thread
+        int run = 0;
+        for (int w = 0; w < PERM_WARPS; ++w) {
+            int v = hist[w * E + e];
+            hist[w * E + e] = run;
+            run += v;
+        }
+        cnt[e] = run;
+        c = run;
+        pc = (run + block_m - 1) / block_m * block_m;
+    }
+    int inc_c = block_inclusive_scan(tid < E ? c : 0, warp_tot);
+    int inc_p = block_inclusive_scan(tid < E ? pc : 0, warp_tot);
+    if (tid < E) {
+        counts[tid] = c;
+        offsets[tid + 1] = inc_c;
+        padded[tid + 1] = inc_p;
+        pad_start[tid + 1] = inc_p;
+    }
+    if (tid == 0) {
+        offsets[0] = 0;
+        padded[0] = 0;
+        pad_start[0] = 0;
+    }
+    __syncthreads();
+
+    // Phase 3: stable scatter.
+    for (int64_t base = lo; base < hi; base += 32) {
+        int64_t p = base + lane;
+        bool valid = p < hi;
+        int e = valid ? ids[p] : -1;
+        if (valid && (e < 0 || e >= E)) e = -1;
+        unsigned m = __match_any_sync(0xFFFFFFFFu, e);
+        int before = (e >= 0) ? my[e] : 0;
+        __syncwarp();
+        if (e >= 0) {
+            int row = pad_start[e] + before + __popc(m & lt_mask);
+            row_to_pair[row] = (int32_t)p;
+            pair_to_row[p] = row;
+            if ((m & lt_mask) == 0u) my[e] = before + __popc(m);
+        } else if (valid) {
+            pair_to_row[p] = -1;
+        }
+        __syncwarp();
+    }
+
+    // Phase 4: padding rows of each expert, then the tail up to rows_cap.
+    for (int e = tid; e < E; e += PERM_THREADS)
+        for (int r = pad_start[e] + cnt[e]; r < pad_start[e + 1]; ++r) row_to_pair[r] = -1;
+    for (int64_t r = pad_start[E] + tid; r < rows_cap; r += PERM_THREADS) row_to_pair[r] = -1;
+
+    __syncthreads();
+    if (tid == 0 && s_err && dev_error) atomicExch(dev_error, DEV_ERR_ID_RANGE);
+}
+
+cudaError_t launch_permute(const int32_t *ids, int T, int E, int k, int block_m, int32_t *counts,
+                           int32_t *offsets, int32_t *padded, int32_t *row_to_pair, int64_t rows_cap,
+                           int32_t *pair_to_row, int32_t *dev_error, cudaStream_t s)
+{
+    size_t smem = sizeof(int) * ((size_t)PERM_WARPS * E + E + E + 1 + 32);
+    cudaError_t err = cudaFuncSetAttribute(permute_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    permute_kernel<<<1, PERM_THREADS, smem, s>>>(ids, T, E, k, block_m, counts, offsets, padded, row_to_pair,
+                                                 rows_cap, pair_to_row, dev_error);
+    note_launch(1);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,260 @@
+"""Python binding of the C ABI in include/moe_mxfp4.h (ctypes).
+
+Argument marshalling only: every step of the layer runs in the CUDA library
+libmoe_mxfp4.so. PyTorch provides device memory and the current stream. There
+is no fallback: if the library has not been built, ``load()`` raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from dataclasses import dataclass
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libmoe_mxfp4.so")
+
+MOE_OK = 0
+STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_MISALIGNED",
+                4: "MOE_ERR_WORKSPACE", 5: "MOE_ERR_CUDA", 6: "MOE_ERR_DEVICE", 7: "MOE_ERR_TIMEOUT"}
+
+# Every symbol the header declares (checked by the CPU test suite).
+EXPORTS = ["moe_abi_version", "moe_status_string", "moe_route", "moe_permute_rows_capacity", "moe_permute",
+           "moe_mxfp4_packed_bytes", "moe_mxfp4_prepack", "moe_mxfp4_dequant_bf16", "moe_mxfp4_workspace_bytes",
+           "moe_mxfp4_forward", "moe_mxfp4_forward_timed", "moe_mxfp4_workspace_layout", "moe_read_device_error", "moe_launch_count"]
+
+
+class MoeError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {STATUS_NAMES.get(status, status)} ({_lib_status_string(status)})")
+
+
+class LayerDesc(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int), ("H", ctypes.c_int), ("I", ctypes.c_int), ("E", ctypes.c_int),
+                ("k", ctypes.c_int), ("block_m", ctypes.c_int), ("swiglu_limit", ctypes.c_float),
+                ("flags", ctypes.c_uint)]
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def load(path: str = LIB_PATH):
+    """Load libmoe_mxfp4.so; raises if it is missing (build it with __graft_entry__.build())."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(path):
+            raise RuntimeError(f"CUDA library not built: {path} is missing (run __graft_entry__.build())")
+        lib = ctypes.CDLL(path)
+        P, i32, i64, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
+        D = ctypes.POINTER(LayerDesc)
+        sigs = {
+            "moe_abi_version": ([], i32),
+            "moe_status_string": ([i32], ctypes.c_char_p),
+            "moe_route": ([P, i32, i32, i32, P, P, P, P], i32),
+            "moe_permute_rows_capacity": ([i32, i32, i32, i32], i64),
+            "moe_permute": ([P, i32, i32, i32, i32, P, P, P, P, P, P, P], i32),
+            "moe_mxfp4_packed_bytes": ([D], sz),
+            "moe_mxfp4_prepack": ([D, P, P, P, P, P, sz, P], i32),
+            "moe_mxfp4_dequant_bf16": ([D, P, i32, i32, P, P], i32),
+            "moe_mxfp4_workspace_bytes": ([D], sz),
+            "moe_mxfp4_forward": ([D, P, P, P, P, P, P, P, P, sz, P], i32),
+            "moe_mxfp4_forward_timed": ([D, P, P, P, P, P, P, P, P, sz, P, P], i32),
+            "moe_mxfp4_workspace_layout": ([D, ctypes.POINTER(ctypes.c_size_t * 6)], i32),
+            "moe_read_device_error": ([P, ctypes.POINTER(ctypes.c_int), P], i32),
+            "moe_launch_count": ([], ctypes.c_uint64),
+        }
+        for name, (args, res) in sigs.items():
+            fn = getattr(lib, name)
+            fn.argtypes = args
+            fn.restype = res
+        _lib = lib
+        return lib
+
+
+def _lib_status_string(status: int) -> str:
+    try:
+        return load().moe_status_string(status).decode()
+    except Exception:  # pragma: no cover - only while formatting an error
+        return "?"
+
+
+def _check(status: int, what: str):
+    if status != MOE_OK:
+        raise MoeError(status, what)
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _cuda(t: torch.Tensor, dtype, name: str):
+    if not t.is_cuda or t.dtype != dtype or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA {dtype} tensor")
+    return t
+
+
+def abi_version() -> int:
+    return load().moe_abi_version()
+
+
+def launch_count() -> int:
+    return int(load().moe_launch_count())
+
+
+def rows_capacity(T: int, E: int, k: int, block_m: int) -> int:
+    return int(load().moe_permute_rows_capacity(T, E, k, block_m))
+
+
+def route(logits: torch.Tensor, k: int, bitmatrix: bool = True, out=None, stream=None):
+    """moe_route. Returns (topk_ids int32 [T,k], topk_w fp32 [T,k], bitmatrix int32 [T, ceil(E/32)] or None)."""
+    _cuda(logits, torch.float32, "logits")
+    T, E = logits.shape
+    if out is None:
+        ids = torch.empty((T, k), dtype=torch.int32, device=logits.device)
+        w = torch.empty((T, k), dtype=torch.float32, device=logits.device)
+        bm = torch.empty((T, (E + 31) // 32), dtype=torch.int32, device=logits.device) if bitmatrix else None
+    else:
+        ids, w, bm = out
+    _check(load().moe_route(_ptr(logits), T, E, k, _ptr(ids), _ptr(w), _ptr(bm), _stream(stream)), "moe_route")
+    return ids, w, bm
+
+
+def permute(topk_ids: torch.Tensor, E: int, block_m: int, out=None, error=None, stream=None):
+    """moe_permute. Returns dict counts, offsets, padded_offsets, row_to_pair, pair_to_row (int32)."""
+    _cuda(topk_ids, torch.int32, "topk_ids")
+    T, k = topk_ids.shape
+    dev = topk_ids.device
+    if out is None:
+        cap = rows_capacity(T, E, k, block_m)
+        out = dict(counts=torch.empty(E, dtype=torch.int32, device=dev),
+                   offsets=torch.empty(E + 1, dtype=torch.int32, device=dev),
+                   padded_offsets=torch.empty(E + 1, dtype=torch.int32, device=dev),
+                   row_to_pair=torch.empty(max(cap, 1), dtype=torch.int32, device=dev),
+                   pair_to_row=torch.empty(max(T * k, 1), dtype=torch.int32, device=dev))
+    _check(load().moe_permute(_ptr(topk_ids), T, E, k, block_m, _ptr(out["counts"]), _ptr(out["offsets"]),
+                              _ptr(out["padded_offsets"]), _ptr(out["row_to_pair"]), _ptr(out["pair_to_row"]),
+                              _ptr(error), _stream(stream)), "moe_permute")
+    return out
+
+
+def make_desc(T, H, I, E, k, block_m=16, swiglu_limit=0.0) -> LayerDesc:
+    return LayerDesc(T, H, I, E, k, block_m, float(swiglu_limit), 0)
+
+
+def packed_bytes(desc: LayerDesc) -> int:
+    return int(load().moe_mxfp4_packed_bytes(ctypes.byref(desc)))
+
+
+def workspace_bytes(desc: LayerDesc) -> int:
+    return int(load().moe_mxfp4_workspace_bytes(ctypes.byref(desc)))
+
+
+def workspace_layout(desc: LayerDesc):
+    arr = (ctypes.c_size_t * 6)()
+    _check(load().moe_mxfp4_workspace_layout(ctypes.byref(desc), ctypes.byref(arr)), "moe_mxfp4_workspace_layout")
+    return dict(error=arr[0], xp=arr[1], h_hi=arr[2], h_lo=arr[3], staging=arr[4], total=arr[5])
+
+
+def prepack(desc: LayerDesc, w13_q, w13_s, w2_q, w2_s, stream=None) -> torch.Tensor:
+    """moe_mxfp4_prepack into a new uint8 device buffer."""
+    for t, n in ((w13_q, "w13_q"), (w13_s, "w13_s"), (w2_q, "w2_q"), (w2_s, "w2_s")):
+        _cuda(t, torch.uint8, n)
+    nbytes = packed_bytes(desc)
+    packed = torch.empty(nbytes, dtype=torch.uint8, device=w13_q.device)
+    _check(load().moe_mxfp4_prepack(ctypes.byref(desc), _ptr(w13_q), _ptr(w13_s), _ptr(w2_q), _ptr(w2_s),
+                                    _ptr(packed), nbytes, _stream(stream)), "moe_mxfp4_prepack")
+    return packed
+
+
+def dequant_bf16(desc: LayerDesc, packed: torch.Tensor, which: int, expert: int, stream=None) -> torch.Tensor:
+    """moe_mxfp4_dequant_bf16: one expert's W13 ([2I, H]) or W2 ([H, I]) as bf16."""
+    shape = (2 * desc.I, desc.H) if which == 0 else (desc.H, desc.I)
+    out = torch.empty(shape, dtype=torch.bfloat16, device=packed.device)
+    _check(load().moe_mxfp4_dequant_bf16(ctypes.byref(desc), _ptr(packed), which, expert, _ptr(out),
+                                         _stream(stream)), "moe_mxfp4_dequant_bf16")
+    return out
+
+
+def forward(desc: LayerDesc, x: torch.Tensor, packed: torch.Tensor, topk_w: torch.Tensor, perm: dict,
+            workspace: torch.Tensor, y: torch.Tensor = None, stream=None) -> torch.Tensor:
+    """moe_mxfp4_forward: y fp32 [T, H]."""
+    _cuda(x, torch.bfloat16, "x")
+    if y is None:
+        y = torch.empty((desc.T, desc.H), dtype=torch.float32, device=x.device)
+    _check(load().moe_mxfp4_forward(ctypes.byref(desc), _ptr(x), _ptr(packed), _ptr(topk_w), _ptr(perm["offsets"]),
+                                    _ptr(perm["padded_offsets"]), _ptr(perm["row_to_pair"]), _ptr(y),
+                                    _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                    _stream(stream)), "moe_mxfp4_forward")
+    return y
+
+
+def forward_timed(desc: LayerDesc, x: torch.Tensor, packed: torch.Tensor, topk_w: torch.Tensor, perm: dict,
+                  workspace: torch.Tensor, y: torch.Tensor, events, stream=None) -> torch.Tensor:
+    """moe_mxfp4_forward_timed: records 5 torch.cuda.Event objects between the forward's kernels."""
+    arr = (ctypes.c_void_p * 5)(*[ctypes.c_void_p(e.cuda_event) if e is not None else None for e in events])
+    _check(load().moe_mxfp4_forward_timed(ctypes.byref(desc), _ptr(x), _ptr(packed), _ptr(topk_w),
+                                          _ptr(perm["offsets"]), _ptr(perm["padded_offsets"]),
+                                          _ptr(perm["row_to_pair"]), _ptr(y), _ptr(workspace),
+                                          workspace.numel() * workspace.element_size(), arr, _stream(stream)),
+           "moe_mxfp4_forward_timed")
+    return y
+
+
+def read_device_error(word: torch.Tensor, stream=None) -> int:
+    """moe_read_device_error on a device int32 word (permute error word or workspace start)."""
+    code = ctypes.c_int(0)
+    _check(load().moe_read_device_error(_ptr(word), ctypes.byref(code), _stream(stream)), "moe_read_device_error")
+    return code.value
+
+
+@dataclass
+class MoELayer:
+    """One MXFP4 MoE layer on the current CUDA device: prepacked weights plus
+    persistent buffers, so a call is route -> permute -> forward with no
+    allocation (CUDA-graph capturable)."""
+
+    desc: LayerDesc
+    packed: torch.Tensor
+    workspace: torch.Tensor
+    bufs: dict
+
+    @classmethod
+    def create(cls, T, H, I, E, k, w13_q, w13_s, w2_q, w2_s, block_m=16, swiglu_limit=0.0, device="cuda"):
+        desc = make_desc(T, H, I, E, k, block_m, swiglu_limit)
+        packed = prepack(desc, w13_q, w13_s, w2_q, w2_s)
+        ws = torch.empty(max(workspace_bytes(desc), 1024), dtype=torch.uint8, device=device)
+        cap = rows_capacity(T, E, k, block_m)
+        dev = torch.device(device)
+        bufs = dict(ids=torch.empty((T, k), dtype=torch.int32, device=dev),
+                    w=torch.empty((T, k), dtype=torch.float32, device=dev),
+                    bm=torch.empty((T, (E + 31) // 32), dtype=torch.int32, device=dev),
+                    perm=dict(counts=torch.empty(E, dtype=torch.int32, device=dev),
+                              offsets=torch.empty(E + 1, dtype=torch.int32, device=dev),
+                              padded_offsets=torch.empty(E + 1, dtype=torch.int32, device=dev),
+                              row_to_pair=torch.empty(max(cap, 1), dtype=torch.int32, device=dev),
+                              pair_to_row=torch.empty(max(T * k, 1), dtype=torch.int32, device=dev)),
+                    perm_err=torch.zeros(4, dtype=torch.int32, device=dev),
+                    y=torch.empty((T, H), dtype=torch.float32, device=dev))
+        return cls(desc, packed, ws, bufs)
+
+    def __call__(self, x: torch.Tensor, logits: torch.Tensor, stream=None) -> torch.Tensor:
+        b = self.bufs
+        route(logits, self.desc.k, out=(b["ids"], b["w"], b["bm"]), stream=stream)
+        permute(b["ids"], self.desc.E, self.desc.block_m, out=b["perm"], error=b["perm_err"], stream=stream)
+        return forward(self.desc, x, self.packed, b["w"], b["perm"], self.workspace, y=b["y"], stream=stream)
+
+    def forward_error(self) -> int:
+        return read_device_error(self.workspace[:4].view(torch.int32))

@@ -189,7 +189,7 @@ def make_layer(T: int, H: int, E: int, k: int, I: int, zipf_bias: bool = False, 
     x = activations(seed, T, H)
     logits = router_logits(seed, x, E, zipf_bias)
     w13_q, w13_s, w2_q, w2_s = mxfp4_weights(seed, E, H, I)
-    return dict(T=T, H=H, E=E, k=k, I=I, x_bits=x, logits=logits,
+    return dict(T=T, H=H, E=E, k=k, I=I, seed=seed, x_bits=x, logits=logits,
                 w13_q=w13_q, w13_s=w13_s, w2_q=w2_q, w2_s=w2_s)
 
 

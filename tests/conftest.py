@@ -21,3 +21,47 @@ def gpu_lib():
     from mxfp4_mixture_experts_top_gb300 import moe
     moe.load()
     return moe
+
+
+class GpuLayers:
+    """Session cache of uploaded inputs: weights are shared between workloads
+    of the same sizes, so the 3.4 GB expert set is uploaded and prepacked once."""
+
+    def __init__(self, moe):
+        import torch
+        self.moe = moe
+        self.torch = torch
+        self.dev = torch.device("cuda:0")
+        self._weights = {}
+        self._packed = {}
+
+    def up(self, a):
+        import numpy as np
+        return self.torch.from_numpy(np.ascontiguousarray(a)).to(self.dev)
+
+    def weights(self, L):
+        key = (L.get("seed", 0), L["E"], L["H"], L["I"])
+        if key not in self._weights:
+            if len(self._weights) >= 2:
+                self._weights.clear()
+                self._packed.clear()
+                self.torch.cuda.empty_cache()
+            self._weights[key] = tuple(self.up(L[n]) for n in ("w13_q", "w13_s", "w2_q", "w2_s"))
+        return key, self._weights[key]
+
+    def packed(self, L):
+        key, w = self.weights(L)
+        if key not in self._packed:
+            d = self.moe.make_desc(L["T"], L["H"], L["I"], L["E"], L["k"], 16)
+            self._packed[key] = self.moe.prepack(d, *w)
+        return self._packed[key]
+
+    def inputs(self, L):
+        import numpy as np
+        x = self.up(L["x_bits"].view(np.int16)).view(self.torch.bfloat16)
+        return x, self.up(L["logits"])
+
+
+@pytest.fixture(scope="session")
+def gpu_layers(gpu_lib):
+    return GpuLayers(gpu_lib)

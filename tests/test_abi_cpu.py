@@ -1,0 +1,102 @@
+"""The C-ABI library loads on a host without a GPU and exports every declared
+symbol; host-side validation rejects bad arguments before any launch."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from mxfp4_mixture_experts_top_gb300 import moe
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moe_mxfp4.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(moe.LIB_PATH):
+        import __graft_entry__
+        __graft_entry__.build()
+    return moe.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert len(names) >= 13
+    for n in names:
+        assert hasattr(lib, n), n
+    assert sorted(moe.EXPORTS) == names
+
+
+def test_abi_version_and_status_strings(lib):
+    assert moe.abi_version() == 1
+    for s in range(8):
+        assert lib.moe_status_string(s)
+    assert b"unknown" in lib.moe_status_string(99)
+
+
+def test_rows_capacity():
+    assert moe.rows_capacity(37, 32, 6, 16) == 222 + 32 * 15
+    assert moe.rows_capacity(8, 256, 6, 16) == 48 + 48 * 15
+    assert moe.rows_capacity(8191, 256, 6, 128) == 49146 + 256 * 127
+    assert moe.rows_capacity(0, 256, 6, 16) == 0
+
+
+def test_packed_and_workspace_sizes():
+    d = moe.make_desc(8, 4096, 2048, 256, 6, 16)
+    # packed bytes equal the canonical MXFP4 bytes (nibbles + scales), only reordered
+    assert moe.packed_bytes(d) == 256 * (2 * 2048 * 4096 // 2 + 2 * 2048 * 4096 // 32
+                                         + 4096 * 2048 // 2 + 4096 * 2048 // 32)
+    lay = moe.workspace_layout(d)
+    R = moe.rows_capacity(8, 256, 6, 16)
+    assert lay["xp"] >= 256 and lay["h_hi"] >= lay["xp"] + R * 4096 * 2
+    assert lay["staging"] >= lay["h_lo"] + R * 2048 * 2
+    assert lay["total"] >= lay["staging"] + 48 * 4096 * 4
+    assert moe.workspace_bytes(d) == lay["total"]
+    assert all(v % 256 == 0 for v in lay.values())
+
+
+@pytest.mark.parametrize("T,H,I,E,k,bm,code", [
+    (8, 4096, 2048, 256, 7, 16, 0),     # valid
+    (8, 4096, 2048, 256, 0, 16, 1),     # k < 1
+    (8, 4096, 2048, 4, 6, 16, 1),       # k > E
+    (-1, 4096, 2048, 256, 6, 16, 1),    # T < 0
+    (8, 4000, 2048, 256, 6, 16, 2),     # H not a multiple of 128
+    (8, 4096, 2000, 256, 6, 16, 2),     # I not a multiple of 128
+    (8, 4096, 2048, 2048, 6, 16, 2),    # E > 1024
+    (8, 4096, 2048, 256, 6, 24, 2),     # block_m not supported
+])
+def test_desc_validation(lib, T, H, I, E, k, bm, code):
+    d = moe.make_desc(T, H, I, E, k, bm)
+    arr = (ctypes.c_size_t * 6)()
+    assert lib.moe_mxfp4_workspace_layout(ctypes.byref(d), ctypes.byref(arr)) == code
+
+
+def test_entry_points_reject_bad_arguments_without_launching(lib):
+    n0 = moe.launch_count()
+    null = None
+    fake = ctypes.c_void_p(0x10000)        # never dereferenced: validation fails first
+    odd = ctypes.c_void_p(0x10008)
+    assert lib.moe_route(fake, 4, 8, 9, fake, fake, null, null) == 1           # k > E
+    assert lib.moe_route(fake, 4, 2048, 6, fake, fake, null, null) == 2        # E > 1024
+    assert lib.moe_route(null, 4, 8, 2, fake, fake, null, null) == 1           # null logits
+    assert lib.moe_route(odd, 4, 8, 2, fake, fake, null, null) == 3            # misaligned
+    assert lib.moe_route(fake, 0, 8, 2, fake, fake, null, null) == 0           # T == 0: no-op
+    assert lib.moe_permute(fake, 4, 8, 2, 24, fake, fake, fake, fake, fake, null, null) == 2
+    assert lib.moe_permute(fake, 4, 8, 2, 16, null, fake, fake, fake, fake, null, null) == 1
+    d = moe.make_desc(4, 512, 256, 8, 2, 16)
+    assert lib.moe_mxfp4_forward(ctypes.byref(d), fake, fake, fake, fake, fake, fake, fake, fake, 16, null) == 4
+    assert lib.moe_mxfp4_forward(ctypes.byref(d), odd, fake, fake, fake, fake, fake, fake, fake, 1 << 40, null) == 3
+    assert lib.moe_mxfp4_forward(ctypes.byref(d), null, fake, fake, fake, fake, fake, fake, fake, 1 << 40, null) == 1
+    assert lib.moe_mxfp4_prepack(ctypes.byref(d), fake, fake, fake, fake, fake, 16, null) == 4
+    assert lib.moe_mxfp4_dequant_bf16(ctypes.byref(d), fake, 2, 0, fake, null) == 1
+    assert lib.moe_mxfp4_dequant_bf16(ctypes.byref(d), fake, 0, 8, fake, null) == 1
+    d0 = moe.make_desc(0, 512, 256, 8, 2, 16)
+    assert lib.moe_mxfp4_forward(ctypes.byref(d0), null, null, null, null, null, null, null, null, 0, null) == 0
+    assert moe.launch_count() == n0

@@ -1,0 +1,185 @@
+"""GPU parity of the MXFP4 layer: decoder bit-exact, layer output within
+2e-2 * rms of the float64 oracle on every workload.
+
+Small workloads compare every output; the 4096-wide workloads compare every
+output of sampled tokens (the first and last token, random tokens, and tokens
+routed to the most and to the least loaded experts), run in the same launch
+configuration as the benchmark (block_m 16, persistent grid of one CTA per
+SM). Measured error ratios are printed.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from mxfp4_mixture_experts_top_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+TOL = 2e-2   # max |gpu - oracle| <= TOL * rms(oracle)
+
+
+def _oracle_decode_bf16_bits(q, s):
+    """Expected bf16 bits of every weight: the oracle's E2M1 x E8M0 product (exact in bf16)."""
+    e2m1 = np.array([oracle.e2m1_value(c) for c in range(16)])
+    e8m0 = np.array([oracle.e8m0_value(v) for v in range(256)])
+    vals = np.stack([e2m1[q & 0xF], e2m1[q >> 4]], -1).reshape(*q.shape[:-1], q.shape[-1] * 2)
+    vals = vals * np.repeat(e8m0[s], 32, axis=-1)
+    return (vals.astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+
+
+def test_decoder_bit_exact_on_workload_weights(gpu_lib, gpu_layers):
+    moe = gpu_lib
+    L = synth.make_config("tiny_t37_h512_e32")
+    packed = gpu_layers.packed(L)
+    d = moe.make_desc(L["T"], L["H"], L["I"], L["E"], L["k"], 16)
+    for e in (0, 7, L["E"] - 1):
+        w13 = moe.dequant_bf16(d, packed, 0, e).view(torch.int16).cpu().numpy().view(np.uint16)
+        np.testing.assert_array_equal(w13, _oracle_decode_bf16_bits(L["w13_q"][e], L["w13_s"][e]))
+        w2 = moe.dequant_bf16(d, packed, 1, e).view(torch.int16).cpu().numpy().view(np.uint16)
+        np.testing.assert_array_equal(w2, _oracle_decode_bf16_bits(L["w2_q"][e], L["w2_s"][e]))
+
+
+def test_decoder_bit_exact_all_codes_all_scales(gpu_lib):
+    """Every E2M1 code under every finite E8M0 scale (0..254), incl. subnormal results."""
+    moe = gpu_lib
+    H, I, E = 256, 128, 1
+    rng = np.random.default_rng(11)
+    w13_q = rng.integers(0, 256, size=(E, 2 * I, H // 2), dtype=np.uint8)
+    w13_q[0, :16, :8] = (np.arange(16, dtype=np.uint8)[:, None] * 17)          # both nibbles = code c
+    w13_s = (np.arange(E * 2 * I * H // 32) % 255).astype(np.uint8).reshape(E, 2 * I, H // 32)
+    w2_q = rng.integers(0, 256, size=(E, H, I // 2), dtype=np.uint8)
+    w2_s = ((np.arange(E * H * I // 32) * 7) % 255).astype(np.uint8).reshape(E, H, I // 32)
+    dv = lambda a: torch.from_numpy(a).cuda()
+    d = moe.make_desc(1, H, I, E, 1, 16)
+    packed = moe.prepack(d, dv(w13_q), dv(w13_s), dv(w2_q), dv(w2_s))
+    got13 = moe.dequant_bf16(d, packed, 0, 0).view(torch.int16).cpu().numpy().view(np.uint16)
+    got2 = moe.dequant_bf16(d, packed, 1, 0).view(torch.int16).cpu().numpy().view(np.uint16)
+    np.testing.assert_array_equal(got13, _oracle_decode_bf16_bits(w13_q[0], w13_s[0]))
+    np.testing.assert_array_equal(got2, _oracle_decode_bf16_bits(w2_q[0], w2_s[0]))
+    assert set(np.unique(w13_s).tolist()) == set(range(255))
+
+
+def _run_layer(moe, gpu_layers, L, block_m=16, swiglu_limit=0.0):
+    x, logits = gpu_layers.inputs(L)
+    packed = gpu_layers.packed(L)
+    T, H, I, E, k = L["T"], L["H"], L["I"], L["E"], L["k"]
+    d = moe.make_desc(T, H, I, E, k, block_m, swiglu_limit)
+    ids, w, _ = moe.route(logits, k)
+    err = torch.zeros(4, dtype=torch.int32, device="cuda")
+    perm = moe.permute(ids, E, block_m, error=err)
+    ws = torch.empty(moe.workspace_bytes(d), dtype=torch.uint8, device="cuda")
+    y = moe.forward(d, x, packed, w, perm, ws)
+    torch.cuda.synchronize()
+    assert moe.read_device_error(err) == 0
+    assert moe.read_device_error(ws[:4].view(torch.int32)) == 0
+    return dict(y=y, ids=ids, w=w, perm=perm, ws=ws, desc=d, x=x)
+
+
+def _sample_tokens(L, ids, n_random=3, seed=0):
+    T, E = L["T"], L["E"]
+    counts = np.bincount(ids.ravel(), minlength=E)
+    hot = int(np.argmax(counts))
+    rare = int(np.argmin(np.where(counts > 0, counts, 1 << 30)))
+    tok = {0, T - 1, int(np.nonzero((ids == hot).any(1))[0][0]), int(np.nonzero((ids == rare).any(1))[0][-1])}
+    rng = np.random.default_rng(seed)
+    tok.update(int(t) for t in rng.integers(0, T, size=n_random))
+    return np.array(sorted(tok), dtype=np.int32)
+
+
+def _compare(name, y_gpu, y_ref):
+    y_gpu = y_gpu.astype(np.float64)
+    rms = np.sqrt(np.mean(y_ref ** 2))
+    err = np.abs(y_gpu - y_ref)
+    ratio = err.max() / rms
+    print(f"[{name}] max|gpu-oracle|/rms = {ratio:.3e}, rms err/rms = {np.sqrt(np.mean(err ** 2)) / rms:.3e}")
+    assert np.isfinite(y_gpu).all()
+    assert ratio <= TOL, f"{name}: max err {err.max():.4g} > {TOL} * rms {rms:.4g}"
+    return ratio
+
+
+@pytest.mark.parametrize("block_m", [16, 128])
+def test_forward_tiny_all_outputs(gpu_lib, gpu_layers, block_m):
+    L = synth.make_config("tiny_t37_h512_e32")
+    r = _run_layer(gpu_lib, gpu_layers, L, block_m)
+    ids_r, w_r, _ = oracle.route(L["logits"], L["k"])
+    assert np.array_equal(r["ids"].cpu().numpy(), ids_r)
+    _compare(f"tiny bm{block_m}", r["y"].cpu().numpy(), oracle.forward(L, ids_r, w_r))
+
+
+def test_forward_tiny_intermediates(gpu_lib, gpu_layers):
+    """Diagnostic: the W13 epilogue's SiLU product (hi + lo) against float64."""
+    moe = gpu_lib
+    L = synth.make_config("tiny_t37_h512_e32")
+    r = _run_layer(moe, gpu_layers, L, 16)
+    lay = moe.workspace_layout(r["desc"])
+    R = int(r["perm"]["padded_offsets"][-1].item())
+    I, H, k = L["I"], L["H"], L["k"]
+    ws = r["ws"]
+    hh = ws[lay["h_hi"]:lay["h_hi"] + R * I * 2].view(torch.bfloat16).float().view(R, I)
+    hl = ws[lay["h_lo"]:lay["h_lo"] + R * I * 2].view(torch.bfloat16).float().view(R, I)
+    h_gpu = (hh.double() + hl.double()).cpu().numpy()
+    r2p = r["perm"]["row_to_pair"].cpu().numpy()[:R]
+    ids = r["ids"].cpu().numpy()
+    e2m1 = np.array([oracle.e2m1_value(c) for c in range(16)])
+    x = synth.bf16_bits_to_f64(L["x_bits"])
+    worst = 0.0
+    for row in range(R):
+        p = r2p[row]
+        if p < 0:
+            assert np.all(h_gpu[row] == 0), f"padding row {row} not zero"
+            continue
+        t, e = p // k, ids[p // k, p % k]
+        q, s = L["w13_q"][e], L["w13_s"][e]
+        W = np.stack([e2m1[q & 0xF], e2m1[q >> 4]], -1).reshape(2 * I, H) * np.repeat(np.ldexp(1.0, s.astype(int) - 127), 32, 1)
+        gu = W @ x[t]
+        h = gu[:I] / (1 + np.exp(-gu[:I])) * gu[I:]
+        worst = max(worst, np.abs(h_gpu[row] - h).max() / np.sqrt(np.mean(h ** 2)))
+    print(f"[tiny h] max|h_gpu-h|/rms(h) = {worst:.3e}")
+    assert worst < 1e-4
+
+
+def test_forward_decode_t8_all_outputs(gpu_lib, gpu_layers):
+    L = synth.make_config("decode_t8_h4096_e256")
+    r = _run_layer(gpu_lib, gpu_layers, L)
+    ids_r, w_r, _ = oracle.route(L["logits"], L["k"])
+    assert np.array_equal(r["ids"].cpu().numpy(), ids_r)
+    _compare("decode t8", r["y"].cpu().numpy(), oracle.forward(L, ids_r, w_r))
+
+
+@pytest.mark.parametrize("name", ["decode_t512_h4096_e256", "prefill_t2048_h4096_e256",
+                                  "prefill_t8191_zipf_h4096_e256"])
+def test_forward_large_sampled_tokens(gpu_lib, gpu_layers, name):
+    L = synth.make_config(name)
+    r = _run_layer(gpu_lib, gpu_layers, L)
+    ids_r, w_r, _ = oracle.route(L["logits"], L["k"])
+    assert np.array_equal(r["ids"].cpu().numpy(), ids_r)
+    tok = _sample_tokens(L, ids_r)
+    y = r["y"].cpu().numpy()
+    assert np.isfinite(y).all()
+    _compare(f"{name} tokens {tok.tolist()}", y[tok], oracle.forward(L, ids_r, w_r, tokens=tok))
+
+
+@pytest.mark.parametrize("name", ["tiny_t37_h512_e32", "decode_t8_h4096_e256"])
+def test_forward_swiglu_clamp_variant(gpu_lib, gpu_layers, name):
+    L = synth.make_config(name)
+    r = _run_layer(gpu_lib, gpu_layers, L, swiglu_limit=10.0)
+    ids_r, w_r, _ = oracle.route(L["logits"], L["k"])
+    tok = np.arange(min(L["T"], 8), dtype=np.int32)
+    _compare(f"{name} clamp10", r["y"].cpu().numpy()[tok], oracle.forward(L, ids_r, w_r, tokens=tok, swiglu_limit=10.0))
+
+
+@pytest.mark.parametrize("T,H,I,E,k", [(1, 256, 128, 8, 2), (17, 128, 256, 16, 4), (200, 256, 128, 5, 3),
+                                       (300, 128, 128, 64, 6)])
+def test_forward_fuzz_shapes(gpu_lib, gpu_layers, T, H, I, E, k):
+    L = synth.make_layer(T=T, H=H, E=E, k=k, I=I, seed=T + E)
+    r = _run_layer(gpu_lib, gpu_layers, L)
+    ids_r, w_r, _ = oracle.route(L["logits"], k)
+    _compare(f"fuzz {T}x{H}x{I} E{E} k{k}", r["y"].cpu().numpy(), oracle.forward(L, ids_r, w_r))
+
+
+def test_forward_deterministic(gpu_lib, gpu_layers):
+    L = synth.make_config("decode_t512_h4096_e256")
+    a = _run_layer(gpu_lib, gpu_layers, L)["y"].clone()
+    b = _run_layer(gpu_lib, gpu_layers, L)["y"]
+    assert torch.equal(a, b)
