@@ -83,15 +83,23 @@ __device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b)
 // Decode one prepacked 32-bit word into 4 bf16x2 words (elements 8w..8w+7 in
 // order). `m1` = scale_mult_lo(s); `m2` = scale_mult_hi(s) is applied only
 // when `big_scale` (s > 128 somewhere in the warp).
+// Word j takes nibbles j and j+4. For j = 0, 1 they sit at bits 4j and 16+4j
+// of q; for j = 2, 3 the same positions of q >> 8. Masking one pair and
+// multiplying by 2^(6-4j') + 2^(12-4j') (j' = j mod 2) places each magnitude
+// at bits 8..6 / 24..22 and each sign at bit 15 / 31 without carries; the
+// final mask drops the other copies.
 __device__ __forceinline__ void decode_word(uint32_t q, uint32_t m1, uint32_t m2, bool big_scale,
                                             uint32_t *out)
 {
+    const uint32_t q2 = q >> 8;
+    uint32_t raw[4];
+    raw[0] = ((q & 0x000F000Fu) * 0x1040u) & 0x81C081C0u;
+    raw[1] = ((q & 0x00F000F0u) * 0x0104u) & 0x81C081C0u;
+    raw[2] = ((q2 & 0x000F000Fu) * 0x1040u) & 0x81C081C0u;
+    raw[3] = ((q2 & 0x00F000F0u) * 0x0104u) & 0x81C081C0u;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-        uint32_t t = (q >> (4 * j)) & 0x000F000Fu;   // element pair: nibble j, nibble j+4
-        uint32_t v = t * 0x1040u;                      // t << 6 | t << 12 (disjoint bits)
-        uint32_t raw = v & 0x81C081C0u;                // sign -> bit 15, magnitude -> bits 8..6
-        uint32_t r = bf16x2_mul(raw, m1);
+        uint32_t r = bf16x2_mul(raw[j], m1);
         if (big_scale) r = bf16x2_mul(r, m2);
         out[j] = r;
     }

@@ -256,5 +256,19 @@ class MoELayer:
         permute(b["ids"], self.desc.E, self.desc.block_m, out=b["perm"], error=b["perm_err"], stream=stream)
         return forward(self.desc, x, self.packed, b["w"], b["perm"], self.workspace, y=b["y"], stream=stream)
 
+    def capture_graph(self, x: torch.Tensor, logits: torch.Tensor):
+        """Capture route -> permute -> forward on x/logits (fixed addresses) into
+        one CUDA graph; returns (graph, y). Replaying the graph re-runs the whole
+        layer on whatever x and logits then hold, with one launch."""
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            self(x, logits)                       # warm-up outside capture (sets kernel attributes)
+        torch.cuda.current_stream().wait_stream(side)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            y = self(x, logits)
+        return graph, y
+
     def forward_error(self) -> int:
         return read_device_error(self.workspace[:4].view(torch.int32))
