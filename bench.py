@@ -60,6 +60,24 @@ def algorithmic(L, ids):
     return dict(touched=touched, w13_kernel_bytes=w13_kernel, layer_bytes=layer, flops=flops)
 
 
+def w13_traffic_per_launch(alg_bytes: float):
+    """DRAM bytes per W13 launch, scaled from the committed ncu capture of a smaller case by the
+    ratio traffic / algorithmic bytes; None when the kernel sources changed since that capture."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "w13_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    h = hashlib.sha256()
+    for rel in d["kernel_sources"]:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    if h.hexdigest() != d["kernel_sources_sha256"]:
+        return None
+    return d["traffic_over_algorithmic"] * alg_bytes
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -169,12 +187,20 @@ def oracle_sample(L, n_tokens: int, min_seconds: float, max_reps: int = 50):
     return len(tok) * reps / el, el, reps, len(tok)
 
 
+def load_workload(name: str):
+    from mxfp4_mixture_experts_top_gb300 import synth
+    if name.startswith("custom:"):
+        T, H, I, E, k = (int(v) for v in name[len("custom:"):].split(","))
+        return synth.make_layer(T=T, H=H, E=E, k=k, I=I, seed=0)
+    return synth.make_config(name)
+
+
 def run_reference(args, world, rank):
     if rank != 0:
         return
     import oracle
     from mxfp4_mixture_experts_top_gb300 import synth
-    L = synth.make_config(args.workload)
+    L = load_workload(args.workload)
     n_tok = args.ref_tokens
     for _ in range(args.warmup):
         oracle_sample(L, n_tok, 0.0, 1)
@@ -218,7 +244,12 @@ def time_workload(moe, L, steps, warmup, flush_buf, events_per_step=True):
         moe.permute(b["ids"], E, 16, out=b["perm"], error=b["perm_err"])
         moe.forward_timed(layer.desc, x, layer.packed, b["w"], b["perm"], layer.workspace, b["y"], evs[2:7])
 
-    mk = lambda: [torch.cuda.Event(enable_timing=True) for _ in range(7)]
+    def mk():
+        # events are created (first record) here so the library can re-record their handles
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(7)]
+        for e in evs:
+            e.record()
+        return evs
     for _ in range(warmup):
         flush_buf.zero_()
         step(mk())
@@ -255,7 +286,7 @@ def run_ours(args, world, rank, local):
     flush_buf = torch.empty(2 * l2 // 4, dtype=torch.float32, device=dev)
     hbm_peak, bf16_peak, bf16_sus, peak_kind = measured_peaks()
 
-    L = synth.make_config(args.workload)
+    L = load_workload(args.workload)
     layer, x, logits, step, mk = time_workload(moe, L, args.steps, args.warmup, flush_buf)
     T, H, I, E, k = L["T"], L["H"], L["I"], L["E"], L["k"]
 
@@ -295,7 +326,11 @@ def run_ours(args, world, rank, local):
     achieved = alg["w13_kernel_bytes"] / (w13_ms / 1e3) / 1e9
     roofline = {"kernel": "moe_gemm_kernel<W13> (grouped W13 GEMM + SiLU*up)", "bound": "hbm",
                 "achieved": achieved, "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
-                "peak_source": f"{peak_kind} hbm_gbs", "traffic": args.w13_traffic,
+                "peak_source": f"{peak_kind} hbm_gbs",
+                "traffic": args.w13_traffic if args.w13_traffic is not None
+                else w13_traffic_per_launch(alg["w13_kernel_bytes"]),
+                "traffic_source": "ncu capture of a 32-expert decode case scaled by algorithmic bytes "
+                                  "(profiles/w13_traffic.json); null if the kernel changed since",
                 "bytes_per_launch": alg["w13_kernel_bytes"], "avg_launch_ms": w13_ms}
     layer_gbs = alg["layer_bytes"] / (ms_per_step / 1e3) / 1e9
     layer_tflops = alg["flops"] / (ms_per_step / 1e3) / 1e12
@@ -392,7 +427,8 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
+                    help="a named workload, or custom:T,H,I,E,k (seed 0) for small profiling cases")
     ap.add_argument("--all-configs", action="store_true", help="also time the other 4096-wide workloads")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)

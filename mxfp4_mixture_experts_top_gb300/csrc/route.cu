@@ -76,15 +76,14 @@ __global__ void __launch_bounds__(256) route_kernel(const float *__restrict__ lo
         w[(int64_t)t * k + lane] = ex / z;
     }
     if (bitmatrix) {
+        // every lane takes part in the shuffles; lane q builds word q (E <= 1024: at most 32 words)
         const int words = (E + 31) >> 5;
-        for (int q = (int)lane; q < words; q += 32) {
-            uint32_t bits = 0u;
-            for (int j = 0; j < k; ++j) {
-                int e = __shfl_sync(0xFFFFFFFFu, my_id, j);
-                if ((e >> 5) == q) bits |= 1u << (e & 31);
-            }
-            bitmatrix[(int64_t)t * words + q] = bits;
+        uint32_t bits = 0u;
+        for (int j = 0; j < k; ++j) {
+            const int e = __shfl_sync(0xFFFFFFFFu, my_id, j);
+            if ((e >> 5) == (int)lane) bits |= 1u << (e & 31);
         }
+        if ((int)lane < words) bitmatrix[(int64_t)t * words + lane] = bits;
     }
 }
 
