@@ -48,6 +48,9 @@ extern "C" {
 
 #define MOE_ABI_VERSION 1
 
+/* Size of the static scratch array behind moe_mxfp4_forward_noalloc. */
+#define MOE_NOALLOC_SCRATCH_BYTES (32u << 20)
+
 typedef enum {
     MOE_OK = 0,
     MOE_ERR_INVALID_ARG = 1,   /* bad size, null pointer, k > E, ...          */
@@ -203,6 +206,32 @@ moe_status_t moe_mxfp4_forward_timed(const moe_layer_desc *desc, const uint16_t 
  * out[4] per-pair W2 outputs (fp32 [T*k, H]), out[5] total bytes;
  * R = moe_permute_rows_capacity(T, E, k, block_m). */
 moe_status_t moe_mxfp4_workspace_layout(const moe_layer_desc *desc, size_t out[6]);
+
+/*
+ * Forward without a caller workspace, for callers that cannot allocate device
+ * memory where they run the layer (a runtime that forbids allocation after
+ * start-up, a plugin whose host framework owns all device memory, code that
+ * must not call cudaMalloc because it can synchronise the device). There is no
+ * counterpart in the source pages; it is a convenience of this library.
+ *   Same arguments and results as moe_mxfp4_forward, minus the workspace: the
+ *   intermediates live in a static device array of MOE_NOALLOC_SCRATCH_BYTES
+ *   (32 MiB) that every GPU loading this library holds until the process exits.
+ *   The call allocates nothing (no cudaMalloc/cudaFree, no allocating library
+ *   routine).
+ *   Returns MOE_ERR_WORKSPACE when moe_mxfp4_workspace_bytes(desc) exceeds
+ *   MOE_NOALLOC_SCRATCH_BYTES (e.g. H = 4096, I = 2048, E = 256, k = 6,
+ *   block_m = 16 fits up to T = 20 tokens); use moe_mxfp4_forward for larger layers.
+ *   The first call on a device looks up the array's device address (once per
+ *   device, with that device current); make that first call before any stream
+ *   capture. All calls share the array, which keeps the previous call's
+ *   contents (the call clears what it needs cleared): calls whose work overlaps
+ *   on the GPU, e.g. on two streams, race on it. The device error word is the
+ *   array's first word and is not readable through moe_read_device_error.
+ */
+moe_status_t moe_mxfp4_forward_noalloc(const moe_layer_desc *desc, const uint16_t *d_x,
+                                       const void *d_packed, const float *d_topk_w,
+                                       const int32_t *d_offsets, const int32_t *d_padded_offsets,
+                                       const int32_t *d_row_to_pair, float *d_y, void *stream);
 
 /*
  * Read and clear a device error word (the d_error of moe_permute or the

@@ -23,7 +23,8 @@ STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
 # Every symbol the header declares (checked by the CPU test suite).
 EXPORTS = ["moe_abi_version", "moe_status_string", "moe_route", "moe_permute_rows_capacity", "moe_permute",
            "moe_mxfp4_packed_bytes", "moe_mxfp4_prepack", "moe_mxfp4_dequant_bf16", "moe_mxfp4_workspace_bytes",
-           "moe_mxfp4_forward", "moe_mxfp4_forward_timed", "moe_mxfp4_workspace_layout", "moe_read_device_error", "moe_launch_count"]
+           "moe_mxfp4_forward", "moe_mxfp4_forward_timed", "moe_mxfp4_workspace_layout", "moe_read_device_error", "moe_launch_count",
+           "moe_mxfp4_forward_noalloc"]
 
 
 class MoeError(RuntimeError):
@@ -68,6 +69,7 @@ def load(path: str = LIB_PATH):
             "moe_mxfp4_workspace_layout": ([D, ctypes.POINTER(ctypes.c_size_t * 6)], i32),
             "moe_read_device_error": ([P, ctypes.POINTER(ctypes.c_int), P], i32),
             "moe_launch_count": ([], ctypes.c_uint64),
+            "moe_mxfp4_forward_noalloc": ([D, P, P, P, P, P, P, P, P], i32),
         }
         for name, (args, res) in sigs.items():
             fn = getattr(lib, name)
@@ -198,6 +200,23 @@ def forward(desc: LayerDesc, x: torch.Tensor, packed: torch.Tensor, topk_w: torc
                                     _ptr(perm["padded_offsets"]), _ptr(perm["row_to_pair"]), _ptr(y),
                                     _ptr(workspace), workspace.numel() * workspace.element_size(),
                                     _stream(stream)), "moe_mxfp4_forward")
+    return y
+
+
+NOALLOC_SCRATCH_BYTES = 32 << 20   # MOE_NOALLOC_SCRATCH_BYTES
+
+
+def forward_noalloc(desc: LayerDesc, x: torch.Tensor, packed: torch.Tensor, topk_w: torch.Tensor, perm: dict,
+                    y: torch.Tensor = None, stream=None) -> torch.Tensor:
+    """moe_mxfp4_forward_noalloc: the forward with the library's static scratch array as its
+    workspace, for callers that cannot allocate device memory (y must be passed in then)."""
+    _cuda(x, torch.bfloat16, "x")
+    if y is None:
+        y = torch.empty((desc.T, desc.H), dtype=torch.float32, device=x.device)
+    _check(load().moe_mxfp4_forward_noalloc(ctypes.byref(desc), _ptr(x), _ptr(packed), _ptr(topk_w),
+                                            _ptr(perm["offsets"]), _ptr(perm["padded_offsets"]),
+                                            _ptr(perm["row_to_pair"]), _ptr(y), _stream(stream)),
+           "moe_mxfp4_forward_noalloc")
     return y
 
 
