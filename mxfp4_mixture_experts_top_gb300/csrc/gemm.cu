@@ -47,13 +47,33 @@ constexpr int TMEM_COLS = 512;
 constexpr int B_BOX_ROWS = 16;         // TMA box: 64 K elements (128 B) x 16 rows
 constexpr int A_COLS = KSLAB / 2;      // TMEM columns per A buffer (bf16 pairs)
 
-template <int MODE> struct Cfg;
-template <> struct Cfg<0> {           // W13: x rows -> SiLU(gate)*up
-    static constexpr int NMAX = 192, NB = 4, NW = 8, NOPS = 1;
+// Kernel configuration. MODE 0: W13 (activation rows -> SiLU(gate)*up),
+// MODE 1: W2 ((h_hi, h_lo) rows -> per-pair outputs). NMAX: most token rows
+// per tile (experts with more rows get several tiles). NB: activation ring
+// slots (one 64-K slice each), NW: weight ring slots (one 128 x 128 slab
+// each), NA: TMEM A buffers, NACC: accumulators per tile (slab ka adds into
+// accumulator ka % NACC, summed by the epilogue; independent chains keep the
+// tensor pipe busy when N is small). TMEM columns: 2 * NACC * NMAX for the
+// double-buffered accumulators, then NA * 64 for the A buffers (<= 512).
+template <int MODE_, int NMAX_, int NB_, int NW_, int NA_, int NACC_>
+struct Cfg {
+    static constexpr int MODE = MODE_, NMAX = NMAX_, NB = NB_, NW = NW_, NA = NA_, NACC = NACC_;
+    static constexpr int NOPS = MODE == 0 ? 1 : 2;
+    static constexpr int D_COLS = NACC * NMAX;            // one accumulator set
+    static constexpr int A_BASE = 2 * D_COLS;
+    static_assert(A_BASE + NA * A_COLS <= TMEM_COLS, "TMEM budget");
+    static_assert(NMAX % 16 == 0 && NMAX <= 256, "MMA N");
 };
-template <> struct Cfg<1> {           // W2: (h_hi, h_lo) rows -> per-pair outputs
-    static constexpr int NMAX = 128, NB = 4, NW = 8, NOPS = 2;
-};
+
+// decode: <= 32 rows per tile, deep rings, 6 A buffers, 2 accumulator chains
+using W13Small = Cfg<0, 32, 24, 12, 6, 2>;
+using W2Small = Cfg<1, 32, 12, 12, 6, 2>;
+// mid: <= 64 rows per tile
+using W13Mid = Cfg<0, 64, 12, 12, 4, 2>;
+using W2Mid = Cfg<1, 64, 6, 12, 4, 2>;
+// prefill: large tiles
+using W13Large = Cfg<0, 192, 4, 8, 2, 1>;
+using W2Large = Cfg<1, 128, 4, 8, 4, 1>;
 
 struct GemmParams {
     CUtensorMap tm_b0;        // W13: gathered x; W2: h_hi
@@ -71,16 +91,17 @@ struct GemmParams {
     int32_t *dev_error;
 };
 
-template <int MODE>
+template <class C>
 struct Smem {
-    static constexpr int BSTAGE = Cfg<MODE>::NOPS * Cfg<MODE>::NMAX * 128;
+    static constexpr int BSTAGE = C::NOPS * C::NMAX * 128;
     static constexpr int B_OFF = 0;
-    static constexpr int W_OFF = B_OFF + Cfg<MODE>::NB * BSTAGE;
-    static constexpr int BAR_OFF = W_OFF + Cfg<MODE>::NW * TILE_BYTES;
-    static constexpr int NBARS = 2 * Cfg<MODE>::NW + 2 * Cfg<MODE>::NB + 2 * 2 + 2 * 2 + 1;
+    static constexpr int W_OFF = B_OFF + C::NB * BSTAGE;
+    static constexpr int BAR_OFF = W_OFF + C::NW * TILE_BYTES;
+    static constexpr int NBARS = 2 * C::NW + 2 * C::NB + 2 * C::NA + 2 * 2 + 1;
     static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;
     static constexpr int PREFIX_OFF = MISC_OFF + 16;
     static size_t bytes(int E) { return 1024 + PREFIX_OFF + sizeof(int) * (size_t)(E + 1 + 32); }
+    static_assert(BSTAGE % 1024 == 0, "B stages must keep the 1024-byte swizzle alignment");
 };
 
 __device__ __forceinline__ void record_error(int32_t *dev_error, int code)
@@ -94,11 +115,11 @@ struct Tile {
     int e, mb, row0, n;
 };
 
-template <int MODE>
+template <class C>
 __device__ __forceinline__ Tile decode_tile(int t, const int *tile_start, int E, int MB,
                                             const int32_t *offsets, const int32_t *padded)
 {
-    constexpr int NMAX = Cfg<MODE>::NMAX;
+    constexpr int NMAX = C::NMAX;
     int lo = 0, hi = E - 1;                 // largest e with tile_start[e] <= t
     while (lo < hi) {
         int mid = (lo + hi + 1) >> 1;
@@ -119,11 +140,11 @@ __device__ __forceinline__ Tile decode_tile(int t, const int *tile_start, int E,
 
 __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }
 
-template <int MODE>
+template <class C>
 __global__ void __launch_bounds__(GEMM_THREADS, 1) moe_gemm_kernel(const __grid_constant__ GemmParams p)
 {
-    using C = Cfg<MODE>;
-    using S = Smem<MODE>;
+    constexpr int MODE = C::MODE;
+    using S = Smem<C>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *bring = smem + S::B_OFF;
@@ -131,8 +152,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) moe_gemm_kernel(const __grid_
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + S::BAR_OFF);
     uint64_t *w_full = bars, *w_empty = w_full + C::NW;
     uint64_t *b_full = w_empty + C::NW, *b_empty = b_full + C::NB;
-    uint64_t *a_full = b_empty + C::NB, *a_empty = a_full + 2;
-    uint64_t *d_full = a_empty + 2, *d_empty = d_full + 2;
+    uint64_t *a_full = b_empty + C::NB, *a_empty = a_full + C::NA;
+    uint64_t *d_full = a_empty + C::NA, *d_empty = d_full + 2;
     uint64_t *mma_done = d_empty + 2;
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(smem + S::MISC_OFF);
     volatile int *s_abort = reinterpret_cast<volatile int *>(smem + S::MISC_OFF + 4);
@@ -185,9 +206,11 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) moe_gemm_kernel(const __grid_
     if (tid == 0) {
         for (int i = 0; i < C::NW; ++i) { ptx::mbar_init(&w_full[i], 1); ptx::mbar_init(&w_empty[i], 8); }
         for (int i = 0; i < C::NB; ++i) { ptx::mbar_init(&b_full[i], 1); ptx::mbar_init(&b_empty[i], 1); }
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < C::NA; ++i) {
             ptx::mbar_init(&a_full[i], 8);
             ptx::mbar_init(&a_empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
             ptx::mbar_init(&d_full[i], 1);
             ptx::mbar_init(&d_empty[i], 4);
         }
@@ -204,6 +227,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) moe_gemm_kernel(const __grid_
     ptx::tc_fence_after();
     const uint32_t tmem = *s_tmem;
     const int slabs = p.K / KSLAB;
+    const int nacc = slabs < C::NACC ? slabs : C::NACC;   // accumulators actually written
     const uint64_t LIM = WAIT_LIMIT_NS;
 
     auto fail = [&]() {
@@ -219,7 +243,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) moe_gemm_kernel(const __grid_
             long long issued = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-                Tile tl = decode_tile<MODE>(t, tile_start, E, MB, p.offsets, p.padded);
+                Tile tl = decode_tile<C>(t, tile_start, E, MB, p.offsets, p.padded);
                 const uint8_t *wsrc = p.wpack + ((size_t)tl.e * MB + tl.mb) * (size_t)slabs * TILE_BYTES;
                 for (int ka = 0; ka < slabs; ++ka) {
                     if (!ptx::mbar_wait(&w_empty[wi], wph ^ 1u, s_abort, LIM)) { ok = false; break; }
@@ -247,7 +271,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) moe_gemm_kernel(const __grid_
             long long issued = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-                Tile tl = decode_tile<MODE>(t, tile_start, E, MB, p.offsets, p.padded);
+                Tile tl = decode_tile<C>(t, tile_start, E, MB, p.offsets, p.padded);
                 const uint32_t bbytes = (uint32_t)(C::NOPS * tl.n * 128);
                 for (int kb = 0; kb < 2 * slabs; ++kb) {
                     if (!ptx::mbar_wait(&b_empty[bi], bph ^ 1u, s_abort, LIM)) { ok = false; break; }
@@ -277,15 +301,18 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) moe_gemm_kernel(const __grid_
             uint32_t aph = 0, bph = 0, dph = 0;
             bool ok = true, issued = false;
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-                Tile tl = decode_tile<MODE>(t, tile_start, E, MB, p.offsets, p.padded);
+                Tile tl = decode_tile<C>(t, tile_start, E, MB, p.offsets, p.padded);
                 const uint32_t idesc = ptx::idesc_bf16_f32(128, (uint32_t)tl.n);
                 if (!ptx::mbar_wait(&d_empty[di], dph ^ 1u, s_abort, LIM)) { ok = false; break; }
                 ptx::tc_fence_after();
-                const uint32_t dt = tmem + (uint32_t)(di * C::NMAX);
+                const uint32_t dt0 = tmem + (uint32_t)(di * C::D_COLS);
                 for (int ka = 0; ka < slabs && ok; ++ka) {
                     if (!ptx::mbar_wait(&a_full[ai], aph, s_abort, LIM)) { ok = false; break; }
                     ptx::tc_fence_after();
-                    const uint32_t at0 = tmem + (uint32_t)(2 * C::NMAX + ai * A_COLS);
+                    const uint32_t at0 = tmem + (uint32_t)(C::A_BASE + ai * A_COLS);
+                    const int acc = C::NACC > 1 ? ka % C::NACC : 0;
+                    const uint32_t dt = dt0 + (uint32_t)(acc * C::NMAX);
+                    const bool first = ka < C::NACC;      // first slab of this accumulator
                     for (int half = 0; half < 2; ++half) {
                         if (!ptx::mbar_wait(&b_full[bi], bph, s_abort, LIM)) { ok = false; break; }
                         ptx::tc_fence_after();
@@ -296,7 +323,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) moe_gemm_kernel(const __grid_
 #pragma unroll
                             for (int op = 0; op < C::NOPS; ++op) {
                                 const uint64_t bd = ptx::smem_desc_sw128(bb + op * C::NMAX * 128 + kk * 32);
-                                ptx::mma_bf16_ts(dt, at, bd, idesc, (ka | half | kk | op) != 0);
+                                ptx::mma_bf16_ts(dt, at, bd, idesc, !(first && half == 0 && kk == 0 && op == 0));
                             }
                         }
                         issued = true;
@@ -305,7 +332,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) moe_gemm_kernel(const __grid_
                     }
                     if (!ok) break;
                     ptx::mma_commit(&a_empty[ai]);
-                    if (++ai == 2) { ai = 0; aph ^= 1u; }
+                    if (++ai == C::NA) { ai = 0; aph ^= 1u; }
                 }
                 if (!ok) break;
                 ptx::mma_commit(&d_full[di]);
@@ -356,12 +383,12 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) moe_gemm_kernel(const __grid_
                 }
                 if (!__all_sync(0xFFFFFFFFu, ptx::mbar_wait(&a_empty[ai], aph ^ 1u, s_abort, LIM))) { ok = false; break; }
                 ptx::tc_fence_after();
-                ptx::tmem_st_32x32b_x32(tmem + t_lane + (uint32_t)(2 * C::NMAX + ai * A_COLS + part * 32), v);
+                ptx::tmem_st_32x32b_x32(tmem + t_lane + (uint32_t)(C::A_BASE + ai * A_COLS + part * 32), v);
                 ptx::tmem_wait_st();
                 ptx::tc_fence_before();
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(&a_full[ai]);
-                if (++ai == 2) { ai = 0; aph ^= 1u; }
+                if (++ai == C::NA) { ai = 0; aph ^= 1u; }
             }
         }
         if (!ok && lane == 0) fail();
@@ -372,14 +399,22 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) moe_gemm_kernel(const __grid_
         uint32_t dph = 0;
         bool ok = true;
         for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-            Tile tl = decode_tile<MODE>(t, tile_start, E, MB, p.offsets, p.padded);
+            Tile tl = decode_tile<C>(t, tile_start, E, MB, p.offsets, p.padded);
             if (!__all_sync(0xFFFFFFFFu, ptx::mbar_wait(&d_full[di], dph, s_abort, LIM))) { ok = false; break; }
             ptx::tc_fence_after();
-            const uint32_t dt = tmem + t_lane + (uint32_t)(di * C::NMAX);
+            const uint32_t dt = tmem + t_lane + (uint32_t)(di * C::D_COLS);
             for (int c0 = 0; c0 < tl.n; c0 += 16) {
                 uint32_t raw[16];
                 ptx::tmem_ld_32x32b_x16(dt + (uint32_t)c0, raw);
                 ptx::tmem_wait_ld();
+                for (int acc = 1; acc < nacc; ++acc) {          // sum the split accumulators
+                    uint32_t part[16];
+                    ptx::tmem_ld_32x32b_x16(dt + (uint32_t)(acc * C::NMAX + c0), part);
+                    ptx::tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        raw[j] = __float_as_uint(__uint_as_float(raw[j]) + __uint_as_float(part[j]));
+                }
                 if (MODE == 0) {
                     // lane i < 16: gate of feature f; lane i + 16: up of the same f.
                     const bool is_gate = lane < 16;
@@ -472,21 +507,33 @@ __global__ void combine_kernel(const float *__restrict__ staging, const float *_
     }
 }
 
-template <int MODE>
+template <class C>
 cudaError_t launch_gemm(const GemmParams &p, int grid, cudaStream_t s)
 {
     static unsigned long long attr_set = 0;   // bit d: attribute set on device d
-    const size_t smem = Smem<MODE>::bytes(p.E);
+    const size_t smem = Smem<C>::bytes(p.E);
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 64 || !((attr_set >> dev) & 1ull)) {
-        cudaError_t e = cudaFuncSetAttribute(moe_gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)Smem<MODE>::bytes(1024));
+        cudaError_t e = cudaFuncSetAttribute(moe_gemm_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)Smem<C>::bytes(1024));
         if (e != cudaSuccess) return e;
         if (dev < 64) __atomic_fetch_or(&attr_set, 1ull << dev, __ATOMIC_RELAXED);
     }
-    moe_gemm_kernel<MODE><<<grid, GEMM_THREADS, smem, s>>>(p);
+    moe_gemm_kernel<C><<<grid, GEMM_THREADS, smem, s>>>(p);
     return cudaGetLastError();
+}
+
+// Tile shape by the average rows per expert (T*k/E): decode batches get
+// small tiles with deep pipelines, prefill batches large tiles.
+enum class Regime { Small, Mid, Large };
+
+Regime pick_regime(int T, int k, int E)
+{
+    const double avg = (double)T * k / E;
+    if (avg <= 12.0) return Regime::Small;
+    if (avg <= 64.0) return Regime::Mid;
+    return Regime::Large;
 }
 
 }  // namespace
@@ -528,7 +575,11 @@ cudaError_t launch_forward(const ForwardArgs &a, cudaStream_t s)
     g.wpack = a.packed;
     g.K = a.H;
     g.MB = a.I / 64;
-    if ((err = launch_gemm<0>(g, a.num_sms, s)) != cudaSuccess) return err;
+    const Regime rg = pick_regime(a.T, a.k, a.E);
+    err = rg == Regime::Small ? launch_gemm<W13Small>(g, a.num_sms, s)
+        : rg == Regime::Mid   ? launch_gemm<W13Mid>(g, a.num_sms, s)
+                              : launch_gemm<W13Large>(g, a.num_sms, s);
+    if (err != cudaSuccess) return err;
     mark(a, 2, s);
 
     // W2: K = I, 128 output features per weight tile
@@ -537,7 +588,10 @@ cudaError_t launch_forward(const ForwardArgs &a, cudaStream_t s)
     g.wpack = a.packed + packed_w13_bytes(a.E, a.H, a.I);
     g.K = a.I;
     g.MB = a.H / TILE_ROWS;
-    if ((err = launch_gemm<1>(g, a.num_sms, s)) != cudaSuccess) return err;
+    err = rg == Regime::Small ? launch_gemm<W2Small>(g, a.num_sms, s)
+        : rg == Regime::Mid   ? launch_gemm<W2Mid>(g, a.num_sms, s)
+                              : launch_gemm<W2Large>(g, a.num_sms, s);
+    if (err != cudaSuccess) return err;
     mark(a, 3, s);
 
     {

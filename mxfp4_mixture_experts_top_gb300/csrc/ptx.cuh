@@ -63,14 +63,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
 
 // Bounded wait on one mbarrier phase. Gives up after `limit_ns` of wall time
 // (or as soon as *abort becomes non-zero) and returns false; never spins
-// forever.
+// forever. The timer and the abort flag are read once per 32 polls.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort,
                                           uint64_t limit_ns)
 {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
+#pragma unroll 1
+        for (int i = 0; i < 32; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
         if (*abort) return false;
         if (globaltimer_ns() - t0 > limit_ns) return false;
     }
