@@ -25,7 +25,7 @@
 //     L2.
 //   * W2 consumes the SiLU product as hi + lo bf16 terms (two MMAs into the
 //     same accumulator), keeping ~16 bits of its precision.
-// Warp roles (512 threads): 0-3 epilogue, 4 weight producer (bulk copies),
+// Warp roles (512 threads, every role warp-converged): 0-3 epilogue, 4 weight producer (bulk copies),
 // 5 MMA issuer and TMEM owner, 6 activation producer (TMA), 7 idle, 8-15
 // converters. Every wait is bounded (2 s); on
 // time-out a CTA records MOE_ERR_TIMEOUT, drains its copies and MMAs, frees
@@ -51,9 +51,10 @@ constexpr int A_COLS = KSLAB / 2;      // TMEM columns per A buffer (bf16 pairs)
 // MODE 1: W2 ((h_hi, h_lo) rows -> per-pair outputs). NMAX: most token rows
 // per tile (experts with more rows get several tiles). NB: activation ring
 // slots (one 64-K slice each), NW: weight ring slots (one 128 x 128 slab
-// each), NA: TMEM A buffers, NACC: accumulators per tile (slab ka adds into
-// accumulator ka % NACC, summed by the epilogue; independent chains keep the
-// tensor pipe busy when N is small). TMEM columns: 2 * NACC * NMAX for the
+// each), NA: TMEM A buffers, NACC: accumulators per tile (consecutive MMAs
+// of a tile rotate over them and the epilogue sums them: with small N an MMA
+// is short, and its latency rather than its work would otherwise set the
+// pace). TMEM columns: 2 * NACC * NMAX for the
 // double-buffered accumulators, then NA * 64 for the A buffers (<= 512).
 template <int MODE_, int NMAX_, int NB_, int NW_, int NA_, int NACC_>
 struct Cfg {
@@ -65,9 +66,12 @@ struct Cfg {
     static_assert(NMAX % 16 == 0 && NMAX <= 256, "MMA N");
 };
 
-// decode: <= 32 rows per tile, deep rings, 6 A buffers, 2 accumulator chains
-using W13Small = Cfg<0, 32, 24, 12, 6, 2>;
-using W2Small = Cfg<1, 32, 12, 12, 6, 2>;
+// decode, <= 2 rows per expert on average: 16-row tiles, 8 accumulators
+using W13Tiny = Cfg<0, 16, 48, 12, 4, 8>;
+using W2Tiny = Cfg<1, 16, 24, 12, 4, 8>;
+// decode batches: <= 32 rows per tile, 4 accumulators
+using W13Small = Cfg<0, 32, 24, 12, 4, 4>;
+using W2Small = Cfg<1, 32, 12, 12, 4, 4>;
 // mid: <= 64 rows per tile
 using W13Mid = Cfg<0, 64, 12, 12, 4, 2>;
 using W2Mid = Cfg<1, 64, 6, 12, 4, 2>;
@@ -227,7 +231,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) moe_gemm_kernel(const __grid_
     ptx::tc_fence_after();
     const uint32_t tmem = *s_tmem;
     const int slabs = p.K / KSLAB;
-    const int nacc = slabs < C::NACC ? slabs : C::NACC;   // accumulators actually written
+    constexpr int MMAS_PER_SLAB = 8 * C::NOPS;             // K = 128 in steps of 16, per operand
+    const int nacc = slabs * MMAS_PER_SLAB < C::NACC ? slabs * MMAS_PER_SLAB : C::NACC;   // accumulators written
     const uint64_t LIM = WAIT_LIMIT_NS;
 
     auto fail = [&]() {
@@ -235,46 +240,54 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) moe_gemm_kernel(const __grid_
         record_error(p.dev_error, DEV_ERR_TIMEOUT);
     };
 
+    // Warps 4, 5 and 6 run their loops with all 32 lanes converged; one lane
+    // issues each copy / MMA / commit (see ptx::elect_one).
     if (warp == 4) {
         // ===================== weight producer: one 8704-byte bulk copy per 128 x 128 slab
-        if (lane == 0) {
-            int wi = 0;
-            uint32_t wph = 0;
-            long long issued = 0;
-            bool ok = true;
-            for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-                Tile tl = decode_tile<C>(t, tile_start, E, MB, p.offsets, p.padded);
-                const uint8_t *wsrc = p.wpack + ((size_t)tl.e * MB + tl.mb) * (size_t)slabs * TILE_BYTES;
-                for (int ka = 0; ka < slabs; ++ka) {
-                    if (!ptx::mbar_wait(&w_empty[wi], wph ^ 1u, s_abort, LIM)) { ok = false; break; }
+        const bool leader = ptx::elect_one();
+        int wi = 0;
+        uint32_t wph = 0;
+        long long issued = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+            Tile tl = decode_tile<C>(t, tile_start, E, MB, p.offsets, p.padded);
+            const uint8_t *wsrc = p.wpack + ((size_t)tl.e * MB + tl.mb) * (size_t)slabs * TILE_BYTES;
+            for (int ka = 0; ka < slabs; ++ka) {
+                if (!__all_sync(0xFFFFFFFFu, ptx::mbar_wait(&w_empty[wi], wph ^ 1u, s_abort, LIM))) { ok = false; break; }
+                if (leader) {
                     ptx::mbar_arrive_expect_tx(&w_full[wi], TILE_BYTES);
                     ptx::bulk_g2s(wring + wi * TILE_BYTES, wsrc + (size_t)ka * TILE_BYTES, TILE_BYTES, &w_full[wi]);
-                    ++issued;
-                    if (++wi == C::NW) { wi = 0; wph ^= 1u; }
                 }
+                __syncwarp();
+                ++issued;
+                if (++wi == C::NW) { wi = 0; wph ^= 1u; }
             }
-            if (!ok) fail();
-            volatile int never = 0;
-            // drain: every issued copy must land before shared memory is released
-            for (long long i = 1; i <= (issued < C::NW ? issued : C::NW); ++i) {
-                long long n = issued - i;
-                ptx::mbar_wait(&w_full[n % C::NW], (uint32_t)((n / C::NW) & 1), &never, LIM);
-            }
+        }
+        if (!ok && leader) fail();
+        volatile int never = 0;
+        // drain: every issued copy must land before shared memory is released
+        for (long long i = 1; i <= (issued < C::NW ? issued : C::NW); ++i) {
+            long long n = issued - i;
+            __all_sync(0xFFFFFFFFu, ptx::mbar_wait(&w_full[n % C::NW], (uint32_t)((n / C::NW) & 1), &never, LIM));
         }
     } else if (warp == 6) {
         // ===================== activation producer: 2-D TMA boxes of 64 K x 16 rows
-        if (lane == 0) {
+        const bool leader = ptx::elect_one();
+        if (leader) {
             ptx::prefetch_tmap(&p.tm_b0);
             if (C::NOPS > 1) ptx::prefetch_tmap(&p.tm_b1);
-            int bi = 0;
-            uint32_t bph = 0;
-            long long issued = 0;
-            bool ok = true;
-            for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-                Tile tl = decode_tile<C>(t, tile_start, E, MB, p.offsets, p.padded);
-                const uint32_t bbytes = (uint32_t)(C::NOPS * tl.n * 128);
-                for (int kb = 0; kb < 2 * slabs; ++kb) {
-                    if (!ptx::mbar_wait(&b_empty[bi], bph ^ 1u, s_abort, LIM)) { ok = false; break; }
+        }
+        __syncwarp();
+        int bi = 0;
+        uint32_t bph = 0;
+        long long issued = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+            Tile tl = decode_tile<C>(t, tile_start, E, MB, p.offsets, p.padded);
+            const uint32_t bbytes = (uint32_t)(C::NOPS * tl.n * 128);
+            for (int kb = 0; kb < 2 * slabs; ++kb) {
+                if (!__all_sync(0xFFFFFFFFu, ptx::mbar_wait(&b_empty[bi], bph ^ 1u, s_abort, LIM))) { ok = false; break; }
+                if (leader) {
                     ptx::mbar_arrive_expect_tx(&b_full[bi], bbytes);
                     uint8_t *dst = bring + bi * S::BSTAGE;
                     const int kx = kb * 64;
@@ -283,39 +296,39 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) moe_gemm_kernel(const __grid_
                     if (C::NOPS > 1)
                         for (int r = 0; r < tl.n; r += B_BOX_ROWS)
                             ptx::tma_load_2d(dst + C::NMAX * 128 + r * 128, &p.tm_b1, kx, tl.row0 + r, &b_full[bi]);
-                    ++issued;
-                    if (++bi == C::NB) { bi = 0; bph ^= 1u; }
                 }
+                __syncwarp();
+                ++issued;
+                if (++bi == C::NB) { bi = 0; bph ^= 1u; }
             }
-            if (!ok) fail();
-            volatile int never = 0;
-            for (long long i = 1; i <= (issued < C::NB ? issued : C::NB); ++i) {
-                long long n = issued - i;
-                ptx::mbar_wait(&b_full[n % C::NB], (uint32_t)((n / C::NB) & 1), &never, LIM);
-            }
+        }
+        if (!ok && leader) fail();
+        volatile int never = 0;
+        for (long long i = 1; i <= (issued < C::NB ? issued : C::NB); ++i) {
+            long long n = issued - i;
+            __all_sync(0xFFFFFFFFu, ptx::mbar_wait(&b_full[n % C::NB], (uint32_t)((n / C::NB) & 1), &never, LIM));
         }
     } else if (warp == 5) {
         // ===================== MMA issuer
-        if (lane == 0) {
-            int ai = 0, bi = 0, di = 0;
-            uint32_t aph = 0, bph = 0, dph = 0;
-            bool ok = true, issued = false;
-            for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-                Tile tl = decode_tile<C>(t, tile_start, E, MB, p.offsets, p.padded);
-                const uint32_t idesc = ptx::idesc_bf16_f32(128, (uint32_t)tl.n);
-                if (!ptx::mbar_wait(&d_empty[di], dph ^ 1u, s_abort, LIM)) { ok = false; break; }
+        const bool leader = ptx::elect_one();
+        int ai = 0, bi = 0, di = 0;
+        uint32_t aph = 0, bph = 0, dph = 0;
+        bool ok = true, issued = false;
+        for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+            Tile tl = decode_tile<C>(t, tile_start, E, MB, p.offsets, p.padded);
+            const uint32_t idesc = ptx::idesc_bf16_f32(128, (uint32_t)tl.n);
+            if (!__all_sync(0xFFFFFFFFu, ptx::mbar_wait(&d_empty[di], dph ^ 1u, s_abort, LIM))) { ok = false; break; }
+            ptx::tc_fence_after();
+            const uint32_t dt0 = tmem + (uint32_t)(di * C::D_COLS);
+            for (int ka = 0; ka < slabs && ok; ++ka) {
+                if (!__all_sync(0xFFFFFFFFu, ptx::mbar_wait(&a_full[ai], aph, s_abort, LIM))) { ok = false; break; }
                 ptx::tc_fence_after();
-                const uint32_t dt0 = tmem + (uint32_t)(di * C::D_COLS);
-                for (int ka = 0; ka < slabs && ok; ++ka) {
-                    if (!ptx::mbar_wait(&a_full[ai], aph, s_abort, LIM)) { ok = false; break; }
+                const uint32_t at0 = tmem + (uint32_t)(C::A_BASE + ai * A_COLS);
+                const int m0 = ka * MMAS_PER_SLAB;     // index of this slab's first MMA in the tile
+                for (int half = 0; half < 2; ++half) {
+                    if (!__all_sync(0xFFFFFFFFu, ptx::mbar_wait(&b_full[bi], bph, s_abort, LIM))) { ok = false; break; }
                     ptx::tc_fence_after();
-                    const uint32_t at0 = tmem + (uint32_t)(C::A_BASE + ai * A_COLS);
-                    const int acc = C::NACC > 1 ? ka % C::NACC : 0;
-                    const uint32_t dt = dt0 + (uint32_t)(acc * C::NMAX);
-                    const bool first = ka < C::NACC;      // first slab of this accumulator
-                    for (int half = 0; half < 2; ++half) {
-                        if (!ptx::mbar_wait(&b_full[bi], bph, s_abort, LIM)) { ok = false; break; }
-                        ptx::tc_fence_after();
+                    if (leader) {
                         const uint32_t bb = ptx::smem_u32(bring + bi * S::BSTAGE);
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk) {
@@ -323,27 +336,33 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) moe_gemm_kernel(const __grid_
 #pragma unroll
                             for (int op = 0; op < C::NOPS; ++op) {
                                 const uint64_t bd = ptx::smem_desc_sw128(bb + op * C::NMAX * 128 + kk * 32);
-                                ptx::mma_bf16_ts(dt, at, bd, idesc, !(first && half == 0 && kk == 0 && op == 0));
+                                const int m = m0 + (half * 4 + kk) * C::NOPS + op;
+                                const uint32_t dt = dt0 + (uint32_t)((m % C::NACC) * C::NMAX);
+                                ptx::mma_bf16_ts(dt, at, bd, idesc, m >= C::NACC);   // first MMA of an accumulator overwrites
                             }
                         }
-                        issued = true;
                         ptx::mma_commit(&b_empty[bi]);
-                        if (++bi == C::NB) { bi = 0; bph ^= 1u; }
                     }
-                    if (!ok) break;
-                    ptx::mma_commit(&a_empty[ai]);
-                    if (++ai == C::NA) { ai = 0; aph ^= 1u; }
+                    __syncwarp();
+                    issued = true;
+                    if (++bi == C::NB) { bi = 0; bph ^= 1u; }
                 }
                 if (!ok) break;
-                ptx::mma_commit(&d_full[di]);
-                if (++di == 2) { di = 0; dph ^= 1u; }
+                if (leader) ptx::mma_commit(&a_empty[ai]);
+                __syncwarp();
+                if (++ai == C::NA) { ai = 0; aph ^= 1u; }
             }
-            if (!ok) fail();
-            if (issued) {            // all MMAs retired before TMEM is released
-                volatile int never = 0;
-                ptx::mma_commit(mma_done);
-                ptx::mbar_wait(mma_done, 0, &never, LIM);
-            }
+            if (!ok) break;
+            if (leader) ptx::mma_commit(&d_full[di]);
+            __syncwarp();
+            if (++di == 2) { di = 0; dph ^= 1u; }
+        }
+        if (!ok && leader) fail();
+        if (issued) {            // all MMAs retired before TMEM is released
+            volatile int never = 0;
+            if (leader) ptx::mma_commit(mma_done);
+            __syncwarp();
+            __all_sync(0xFFFFFFFFu, ptx::mbar_wait(mma_done, 0, &never, LIM));
         }
     } else if (warp >= 8) {
         // ===================== converters: smem MXFP4 -> bf16 -> TMEM (A operand)
@@ -526,12 +545,13 @@ cudaError_t launch_gemm(const GemmParams &p, int grid, cudaStream_t s)
 
 // Tile shape by the average rows per expert (T*k/E): decode batches get
 // small tiles with deep pipelines, prefill batches large tiles.
-enum class Regime { Small, Mid, Large };
+enum class Regime { Tiny, Small, Mid, Large };
 
 Regime pick_regime(int T, int k, int E)
 {
     const double avg = (double)T * k / E;
-    if (avg <= 12.0) return Regime::Small;
+    if (avg <= 2.0) return Regime::Tiny;
+    if (avg <= 16.0) return Regime::Small;
     if (avg <= 64.0) return Regime::Mid;
     return Regime::Large;
 }
@@ -576,7 +596,8 @@ cudaError_t launch_forward(const ForwardArgs &a, cudaStream_t s)
     g.K = a.H;
     g.MB = a.I / 64;
     const Regime rg = pick_regime(a.T, a.k, a.E);
-    err = rg == Regime::Small ? launch_gemm<W13Small>(g, a.num_sms, s)
+    err = rg == Regime::Tiny  ? launch_gemm<W13Tiny>(g, a.num_sms, s)
+        : rg == Regime::Small ? launch_gemm<W13Small>(g, a.num_sms, s)
         : rg == Regime::Mid   ? launch_gemm<W13Mid>(g, a.num_sms, s)
                               : launch_gemm<W13Large>(g, a.num_sms, s);
     if (err != cudaSuccess) return err;
@@ -588,7 +609,8 @@ cudaError_t launch_forward(const ForwardArgs &a, cudaStream_t s)
     g.wpack = a.packed + packed_w13_bytes(a.E, a.H, a.I);
     g.K = a.I;
     g.MB = a.H / TILE_ROWS;
-    err = rg == Regime::Small ? launch_gemm<W2Small>(g, a.num_sms, s)
+    err = rg == Regime::Tiny  ? launch_gemm<W2Tiny>(g, a.num_sms, s)
+        : rg == Regime::Small ? launch_gemm<W2Small>(g, a.num_sms, s)
         : rg == Regime::Mid   ? launch_gemm<W2Mid>(g, a.num_sms, s)
                               : launch_gemm<W2Large>(g, a.num_sms, s);
     if (err != cudaSuccess) return err;

@@ -26,6 +26,22 @@ __device__ __forceinline__ uint32_t lane_id()
     return l;
 }
 
+// One lane of a converged warp (the same lane on every call with all lanes
+// active). Issue-once operations (TMA, tcgen05.mma, tcgen05.commit) go through
+// it from code the whole warp executes: issuing them from a lane that runs
+// its own loop while the rest of the warp waits elsewhere costs ~10x more
+// cycles per instruction.
+__device__ __forceinline__ bool elect_one()
+{
+    uint32_t pred;
+    asm volatile(
+        "{\n\t.reg .pred P;\n\t"
+        "elect.sync _|P, 0xffffffff;\n\t"
+        "selp.b32 %0, 1, 0, P;\n\t}"
+        : "=r"(pred));
+    return pred != 0;
+}
+
 // ----------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
 {
