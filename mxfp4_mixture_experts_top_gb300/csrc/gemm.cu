@@ -50,8 +50,8 @@ constexpr int A_COLS = KSLAB / 2;      // TMEM columns per A buffer (bf16 pairs)
 // Kernel configuration. MODE 0: W13 (activation rows -> SiLU(gate)*up),
 // MODE 1: W2 ((h_hi, h_lo) rows -> per-pair outputs). NMAX: most token rows
 // per tile (experts with more rows get several tiles). NB: activation ring
-// slots (one 64-K slice each), NW: weight ring slots (one 128 x 128 slab
-// each), NA: TMEM A buffers, NACC: accumulators per tile (consecutive MMAs
+// slots (the token rows of one 128-K slab each), NW: weight ring slots (one
+// 128 x 128 slab each), NA: TMEM A buffers, NACC: accumulators per tile (consecutive MMAs
 // of a tile rotate over them and the epilogue sums them: with small N an MMA
 // is short, and its latency rather than its work would otherwise set the
 // pace). TMEM columns: 2 * NACC * NMAX for the
@@ -67,17 +67,17 @@ struct Cfg {
 };
 
 // decode, <= 2 rows per expert on average: 16-row tiles, 8 accumulators
-using W13Tiny = Cfg<0, 16, 48, 12, 4, 8>;
-using W2Tiny = Cfg<1, 16, 24, 12, 4, 8>;
+using W13Tiny = Cfg<0, 16, 24, 12, 4, 8>;
+using W2Tiny = Cfg<1, 16, 12, 12, 4, 8>;
 // decode batches: <= 32 rows per tile, 4 accumulators
-using W13Small = Cfg<0, 32, 24, 12, 4, 4>;
-using W2Small = Cfg<1, 32, 12, 12, 4, 4>;
+using W13Small = Cfg<0, 32, 12, 12, 4, 4>;
+using W2Small = Cfg<1, 32, 6, 12, 4, 4>;
 // mid: <= 64 rows per tile
-using W13Mid = Cfg<0, 64, 12, 12, 4, 2>;
-using W2Mid = Cfg<1, 64, 6, 12, 4, 2>;
+using W13Mid = Cfg<0, 64, 6, 12, 4, 2>;
+using W2Mid = Cfg<1, 64, 3, 12, 4, 2>;
 // prefill: large tiles
-using W13Large = Cfg<0, 192, 4, 8, 2, 1>;
-using W2Large = Cfg<1, 128, 4, 8, 4, 1>;
+using W13Large = Cfg<0, 192, 2, 8, 2, 1>;
+using W2Large = Cfg<1, 128, 2, 8, 4, 1>;
 
 struct GemmParams {
     CUtensorMap tm_b0;        // W13: gathered x; W2: h_hi
@@ -97,7 +97,8 @@ struct GemmParams {
 
 template <class C>
 struct Smem {
-    static constexpr int BSTAGE = C::NOPS * C::NMAX * 128;
+    static constexpr int REGION = C::NMAX * 128;                 // one 64-K box column of NMAX rows
+    static constexpr int BSTAGE = 2 * C::NOPS * REGION;            // [K half][operand][rows][128 B]
     static constexpr int B_OFF = 0;
     static constexpr int W_OFF = B_OFF + C::NB * BSTAGE;
     static constexpr int BAR_OFF = W_OFF + C::NW * TILE_BYTES;
@@ -244,7 +245,6 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) moe_gemm_kernel(const __grid_
     // issues each copy / MMA / commit (see ptx::elect_one).
     if (warp == 4) {
         // ===================== weight producer: one 8704-byte bulk copy per 128 x 128 slab
-        const bool leader = ptx::elect_one();
         int wi = 0;
         uint32_t wph = 0;
         long long issued = 0;
@@ -254,7 +254,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) moe_gemm_kernel(const __grid_
             const uint8_t *wsrc = p.wpack + ((size_t)tl.e * MB + tl.mb) * (size_t)slabs * TILE_BYTES;
             for (int ka = 0; ka < slabs; ++ka) {
                 if (!__all_sync(0xFFFFFFFFu, ptx::mbar_wait(&w_empty[wi], wph ^ 1u, s_abort, LIM))) { ok = false; break; }
-                if (leader) {
+                if (ptx::elect_one()) {
                     ptx::mbar_arrive_expect_tx(&w_full[wi], TILE_BYTES);
                     ptx::bulk_g2s(wring + wi * TILE_BYTES, wsrc + (size_t)ka * TILE_BYTES, TILE_BYTES, &w_full[wi]);
                 }
@@ -263,7 +263,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) moe_gemm_kernel(const __grid_
                 if (++wi == C::NW) { wi = 0; wph ^= 1u; }
             }
         }
-        if (!ok && leader) fail();
+        if (!ok && lane == 0) fail();
         volatile int never = 0;
         // drain: every issued copy must land before shared memory is released
         for (long long i = 1; i <= (issued < C::NW ? issued : C::NW); ++i) {
@@ -271,9 +271,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) moe_gemm_kernel(const __grid_
             __all_sync(0xFFFFFFFFu, ptx::mbar_wait(&w_full[n % C::NW], (uint32_t)((n / C::NW) & 1), &never, LIM));
         }
     } else if (warp == 6) {
-        // ===================== activation producer: 2-D TMA boxes of 64 K x 16 rows
-        const bool leader = ptx::elect_one();
-        if (leader) {
+        // ===================== activation producer: the tile's token rows of one 128-K slab per
+        // stage, as 2-D TMA boxes of 64 K x 16 rows
+        if (ptx::elect_one()) {
             ptx::prefetch_tmap(&p.tm_b0);
             if (C::NOPS > 1) ptx::prefetch_tmap(&p.tm_b1);
         }
@@ -284,33 +284,35 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) moe_gemm_kernel(const __grid_
         bool ok = true;
         for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
             Tile tl = decode_tile<C>(t, tile_start, E, MB, p.offsets, p.padded);
-            const uint32_t bbytes = (uint32_t)(C::NOPS * tl.n * 128);
-            for (int kb = 0; kb < 2 * slabs; ++kb) {
+            const uint32_t bbytes = (uint32_t)(2 * C::NOPS * tl.n * 128);
+            for (int ka = 0; ka < slabs; ++ka) {
                 if (!__all_sync(0xFFFFFFFFu, ptx::mbar_wait(&b_empty[bi], bph ^ 1u, s_abort, LIM))) { ok = false; break; }
-                if (leader) {
+                if (ptx::elect_one()) {
                     ptx::mbar_arrive_expect_tx(&b_full[bi], bbytes);
-                    uint8_t *dst = bring + bi * S::BSTAGE;
-                    const int kx = kb * 64;
-                    for (int r = 0; r < tl.n; r += B_BOX_ROWS)
-                        ptx::tma_load_2d(dst + r * 128, &p.tm_b0, kx, tl.row0 + r, &b_full[bi]);
-                    if (C::NOPS > 1)
+                    uint8_t *stage = bring + bi * S::BSTAGE;
+                    for (int half = 0; half < 2; ++half) {
+                        const int kx = ka * KSLAB + half * 64;
+                        uint8_t *dst = stage + half * C::NOPS * S::REGION;
                         for (int r = 0; r < tl.n; r += B_BOX_ROWS)
-                            ptx::tma_load_2d(dst + C::NMAX * 128 + r * 128, &p.tm_b1, kx, tl.row0 + r, &b_full[bi]);
+                            ptx::tma_load_2d(dst + r * 128, &p.tm_b0, kx, tl.row0 + r, &b_full[bi]);
+                        if (C::NOPS > 1)
+                            for (int r = 0; r < tl.n; r += B_BOX_ROWS)
+                                ptx::tma_load_2d(dst + S::REGION + r * 128, &p.tm_b1, kx, tl.row0 + r, &b_full[bi]);
+                    }
                 }
                 __syncwarp();
                 ++issued;
                 if (++bi == C::NB) { bi = 0; bph ^= 1u; }
             }
         }
-        if (!ok && leader) fail();
+        if (!ok && lane == 0) fail();
         volatile int never = 0;
         for (long long i = 1; i <= (issued < C::NB ? issued : C::NB); ++i) {
             long long n = issued - i;
             __all_sync(0xFFFFFFFFu, ptx::mbar_wait(&b_full[n % C::NB], (uint32_t)((n / C::NB) & 1), &never, LIM));
         }
     } else if (warp == 5) {
-        // ===================== MMA issuer
-        const bool leader = ptx::elect_one();
+        // ===================== MMA issuer: per slab one A buffer, one activation stage
         int ai = 0, bi = 0, di = 0;
         uint32_t aph = 0, bph = 0, dph = 0;
         bool ok = true, issued = false;
@@ -320,47 +322,43 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) moe_gemm_kernel(const __grid_
             if (!__all_sync(0xFFFFFFFFu, ptx::mbar_wait(&d_empty[di], dph ^ 1u, s_abort, LIM))) { ok = false; break; }
             ptx::tc_fence_after();
             const uint32_t dt0 = tmem + (uint32_t)(di * C::D_COLS);
-            for (int ka = 0; ka < slabs && ok; ++ka) {
-                if (!__all_sync(0xFFFFFFFFu, ptx::mbar_wait(&a_full[ai], aph, s_abort, LIM))) { ok = false; break; }
+            for (int ka = 0; ka < slabs; ++ka) {
+                if (!__all_sync(0xFFFFFFFFu, ptx::mbar_wait(&a_full[ai], aph, s_abort, LIM) &&
+                                                 ptx::mbar_wait(&b_full[bi], bph, s_abort, LIM))) { ok = false; break; }
                 ptx::tc_fence_after();
-                const uint32_t at0 = tmem + (uint32_t)(C::A_BASE + ai * A_COLS);
-                const int m0 = ka * MMAS_PER_SLAB;     // index of this slab's first MMA in the tile
-                for (int half = 0; half < 2; ++half) {
-                    if (!__all_sync(0xFFFFFFFFu, ptx::mbar_wait(&b_full[bi], bph, s_abort, LIM))) { ok = false; break; }
-                    ptx::tc_fence_after();
-                    if (leader) {
-                        const uint32_t bb = ptx::smem_u32(bring + bi * S::BSTAGE);
+                if (ptx::elect_one()) {
+                    const uint32_t at0 = tmem + (uint32_t)(C::A_BASE + ai * A_COLS);
+                    const uint32_t bb = ptx::smem_u32(bring + bi * S::BSTAGE);
+                    const int m0 = ka * MMAS_PER_SLAB;     // index of this slab's first MMA in the tile
 #pragma unroll
-                        for (int kk = 0; kk < 4; ++kk) {
-                            const uint32_t at = at0 + (uint32_t)((half * 4 + kk) * 8);
+                    for (int half = 0; half < 2; ++half)
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)
 #pragma unroll
                             for (int op = 0; op < C::NOPS; ++op) {
-                                const uint64_t bd = ptx::smem_desc_sw128(bb + op * C::NMAX * 128 + kk * 32);
+                                const uint64_t bd = ptx::smem_desc_sw128(bb + (half * C::NOPS + op) * S::REGION + kk * 32);
                                 const int m = m0 + (half * 4 + kk) * C::NOPS + op;
                                 const uint32_t dt = dt0 + (uint32_t)((m % C::NACC) * C::NMAX);
-                                ptx::mma_bf16_ts(dt, at, bd, idesc, m >= C::NACC);   // first MMA of an accumulator overwrites
+                                // the first MMA into an accumulator overwrites it
+                                ptx::mma_bf16_ts(dt, at0 + (uint32_t)((half * 4 + kk) * 8), bd, idesc, m >= C::NACC);
                             }
-                        }
-                        ptx::mma_commit(&b_empty[bi]);
-                    }
-                    __syncwarp();
-                    issued = true;
-                    if (++bi == C::NB) { bi = 0; bph ^= 1u; }
+                    ptx::mma_commit(&b_empty[bi]);
+                    ptx::mma_commit(&a_empty[ai]);
                 }
-                if (!ok) break;
-                if (leader) ptx::mma_commit(&a_empty[ai]);
                 __syncwarp();
+                issued = true;
+                if (++bi == C::NB) { bi = 0; bph ^= 1u; }
                 if (++ai == C::NA) { ai = 0; aph ^= 1u; }
             }
             if (!ok) break;
-            if (leader) ptx::mma_commit(&d_full[di]);
+            if (ptx::elect_one()) ptx::mma_commit(&d_full[di]);
             __syncwarp();
             if (++di == 2) { di = 0; dph ^= 1u; }
         }
-        if (!ok && leader) fail();
+        if (!ok && lane == 0) fail();
         if (issued) {            // all MMAs retired before TMEM is released
             volatile int never = 0;
-            if (leader) ptx::mma_commit(mma_done);
+            if (ptx::elect_one()) ptx::mma_commit(mma_done);
             __syncwarp();
             __all_sync(0xFFFFFFFFu, ptx::mbar_wait(mma_done, 0, &never, LIM));
         }
