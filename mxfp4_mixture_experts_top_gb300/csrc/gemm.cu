@@ -364,49 +364,59 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) moe_gemm_kernel(const __grid_
         }
     } else if (warp >= 8) {
         // ===================== converters: smem MXFP4 -> bf16 -> TMEM (A operand)
+        // Software-pipelined over the CTA's flat sequence of slabs: while the
+        // tcgen05.st of slab i drains into TMEM, slab i+1 is loaded and decoded.
         const int cw = warp - 8, g = cw & 3, part = cw >> 2;
         const int row = g * 32 + lane;
         const uint32_t t_lane = (uint32_t)(g * 32) << 16;
+        const int my_tiles = (int)blockIdx.x < total ? (total - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+        const int n_slabs = my_tiles * slabs;
         int wi = 0, ai = 0;
         uint32_t wph = 0, aph = 0;
         bool ok = true;
-        for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-            for (int ka = 0; ka < slabs; ++ka) {
-                if (!__all_sync(0xFFFFFFFFu, ptx::mbar_wait(&w_full[wi], wph, s_abort, LIM))) { ok = false; break; }
-                const uint8_t *st = wring + wi * TILE_BYTES;
-                const uint4 q0 = *reinterpret_cast<const uint4 *>(st + ((2 * part) * TILE_ROWS + row) * 16);
-                const uint4 q1 = *reinterpret_cast<const uint4 *>(st + ((2 * part + 1) * TILE_ROWS + row) * 16);
-                const uint32_t sc2 = *reinterpret_cast<const uint16_t *>(st + TILE_NIB_BYTES + row * 4 + 2 * part);
-                __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(&w_empty[wi]);
-                if (++wi == C::NW) { wi = 0; wph ^= 1u; }
 
-                const uint32_t s0 = sc2 & 0xFFu, s1 = sc2 >> 8;
-                const bool big = __any_sync(0xFFFFFFFFu, s0 > 128u || s1 > 128u);
-                uint32_t v[32];
-                {
-                    const uint32_t m1 = scale_mult_lo(s0), m2 = scale_mult_hi(s0);
-                    decode_word(q0.x, m1, m2, big, v + 0);
-                    decode_word(q0.y, m1, m2, big, v + 4);
-                    decode_word(q0.z, m1, m2, big, v + 8);
-                    decode_word(q0.w, m1, m2, big, v + 12);
-                }
-                {
-                    const uint32_t m1 = scale_mult_lo(s1), m2 = scale_mult_hi(s1);
-                    decode_word(q1.x, m1, m2, big, v + 16);
-                    decode_word(q1.y, m1, m2, big, v + 20);
-                    decode_word(q1.z, m1, m2, big, v + 24);
-                    decode_word(q1.w, m1, m2, big, v + 28);
-                }
-                if (!__all_sync(0xFFFFFFFFu, ptx::mbar_wait(&a_empty[ai], aph ^ 1u, s_abort, LIM))) { ok = false; break; }
-                ptx::tc_fence_after();
-                ptx::tmem_st_32x32b_x32(tmem + t_lane + (uint32_t)(C::A_BASE + ai * A_COLS + part * 32), v);
-                ptx::tmem_wait_st();
-                ptx::tc_fence_before();
-                __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(&a_full[ai]);
-                if (++ai == C::NA) { ai = 0; aph ^= 1u; }
-            }
+        // wait for the next weight slab, read this lane's 64 elements, free the stage, decode
+        auto load_decode = [&](uint32_t (&v)[32]) -> bool {
+            if (!__all_sync(0xFFFFFFFFu, ptx::mbar_wait(&w_full[wi], wph, s_abort, LIM))) return false;
+            const uint8_t *st = wring + wi * TILE_BYTES;
+            const uint4 q0 = *reinterpret_cast<const uint4 *>(st + ((2 * part) * TILE_ROWS + row) * 16);
+            const uint4 q1 = *reinterpret_cast<const uint4 *>(st + ((2 * part + 1) * TILE_ROWS + row) * 16);
+            const uint32_t sc2 = *reinterpret_cast<const uint16_t *>(st + TILE_NIB_BYTES + row * 4 + 2 * part);
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&w_empty[wi]);
+            if (++wi == C::NW) { wi = 0; wph ^= 1u; }
+            const uint32_t s0 = sc2 & 0xFFu, s1 = sc2 >> 8;
+            const bool big = __any_sync(0xFFFFFFFFu, s0 > 128u || s1 > 128u);
+            const uint32_t m10 = scale_mult_lo(s0), m20 = scale_mult_hi(s0);
+            decode_word(q0.x, m10, m20, big, v + 0);
+            decode_word(q0.y, m10, m20, big, v + 4);
+            decode_word(q0.z, m10, m20, big, v + 8);
+            decode_word(q0.w, m10, m20, big, v + 12);
+            const uint32_t m11 = scale_mult_lo(s1), m21 = scale_mult_hi(s1);
+            decode_word(q1.x, m11, m21, big, v + 16);
+            decode_word(q1.y, m11, m21, big, v + 20);
+            decode_word(q1.z, m11, m21, big, v + 24);
+            decode_word(q1.w, m11, m21, big, v + 28);
+            return true;
+        };
+        // store slab i (decoded in cur) into its A buffer; decode slab i+1 into nxt meanwhile
+        auto step = [&](uint32_t (&cur)[32], uint32_t (&nxt)[32], int i) -> bool {
+            if (!__all_sync(0xFFFFFFFFu, ptx::mbar_wait(&a_empty[ai], aph ^ 1u, s_abort, LIM))) return false;
+            ptx::tc_fence_after();
+            ptx::tmem_st_32x32b_x32(tmem + t_lane + (uint32_t)(C::A_BASE + ai * A_COLS + part * 32), cur);
+            const bool more = i + 1 < n_slabs && load_decode(nxt);
+            ptx::tmem_wait_st();
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&a_full[ai]);
+            if (++ai == C::NA) { ai = 0; aph ^= 1u; }
+            return more || i + 1 >= n_slabs;
+        };
+        uint32_t va[32], vb[32];
+        if (n_slabs > 0) ok = load_decode(va);
+        for (int i = 0; i < n_slabs && ok; i += 2) {
+            if (!step(va, vb, i)) { ok = false; break; }
+            if (i + 1 < n_slabs && !step(vb, va, i + 1)) { ok = false; break; }
         }
         if (!ok && lane == 0) fail();
     } else if (warp < 4) {
