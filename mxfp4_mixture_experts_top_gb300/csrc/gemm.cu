@@ -42,7 +42,6 @@ namespace moe {
 
 namespace {
 
-constexpr int GEMM_THREADS = 512;
 constexpr int TMEM_COLS = 512;
 constexpr int B_BOX_ROWS = 16;         // TMA box: 64 K elements (128 B) x 16 rows
 constexpr int A_COLS = KSLAB / 2;      // TMEM columns per A buffer (bf16 pairs)
@@ -56,9 +55,15 @@ constexpr int A_COLS = KSLAB / 2;      // TMEM columns per A buffer (bf16 pairs)
 // is short, and its latency rather than its work would otherwise set the
 // pace). TMEM columns: 2 * NACC * NMAX for the
 // double-buffered accumulators, then NA * 64 for the A buffers (<= 512).
-template <int MODE_, int NMAX_, int NB_, int NW_, int NA_, int NACC_>
+template <int MODE_, int NMAX_, int NB_, int NW_, int NA_, int NACC_, int CONVW_>
 struct Cfg {
     static constexpr int MODE = MODE_, NMAX = NMAX_, NB = NB_, NW = NW_, NA = NA_, NACC = NACC_;
+    // converter warps (8 or 16) in groups of 8; group j takes the slabs i with
+    // i % GROUPS == j, so the latency chains of GROUPS slabs overlap. In a
+    // group, warp (g, part) decodes chunks 2*part, 2*part+1 of rows 32g..32g+31.
+    static constexpr int CONVW = CONVW_, GROUPS = CONVW_ / 8;
+    static constexpr int THREADS = (8 + CONVW_) * 32;
+    static_assert(CONVW_ == 8 || CONVW_ == 16, "converter warps");
     static constexpr int NOPS = MODE == 0 ? 1 : 2;
     static constexpr int D_COLS = NACC * NMAX;            // one accumulator set
     static constexpr int A_BASE = 2 * D_COLS;
@@ -66,18 +71,20 @@ struct Cfg {
     static_assert(NMAX % 16 == 0 && NMAX <= 256, "MMA N");
 };
 
-// decode, <= 2 rows per expert on average: 16-row tiles, 8 accumulators
-using W13Tiny = Cfg<0, 16, 24, 12, 4, 8>;
-using W2Tiny = Cfg<1, 16, 12, 12, 4, 8>;
-// decode batches: <= 32 rows per tile, 4 accumulators
-using W13Small = Cfg<0, 32, 12, 12, 4, 4>;
-using W2Small = Cfg<1, 32, 6, 12, 4, 4>;
+// Decode-sized tiles are bound by decoding MXFP4 at the HBM rate: 16
+// converter warps, 6 A buffers. Prefill tiles are bound by the tensor pipe.
+// decode, <= 2 rows per expert on average: 16-row tiles
+using W13Tiny = Cfg<0, 16, 24, 12, 6, 2, 16>;
+using W2Tiny = Cfg<1, 16, 12, 12, 6, 2, 16>;
+// decode batches: <= 32 rows per tile
+using W13Small = Cfg<0, 32, 12, 12, 6, 2, 16>;
+using W2Small = Cfg<1, 32, 6, 12, 6, 2, 16>;
 // mid: <= 64 rows per tile
-using W13Mid = Cfg<0, 64, 6, 12, 4, 2>;
-using W2Mid = Cfg<1, 64, 3, 12, 4, 2>;
+using W13Mid = Cfg<0, 64, 6, 12, 4, 2, 16>;
+using W2Mid = Cfg<1, 64, 3, 12, 4, 2, 16>;
 // prefill: large tiles
-using W13Large = Cfg<0, 192, 2, 8, 2, 1>;
-using W2Large = Cfg<1, 128, 2, 8, 4, 1>;
+using W13Large = Cfg<0, 192, 2, 8, 2, 1, 8>;
+using W2Large = Cfg<1, 128, 2, 8, 4, 1, 8>;
 
 struct GemmParams {
     CUtensorMap tm_b0;        // W13: gathered x; W2: h_hi
@@ -146,7 +153,7 @@ __device__ __forceinline__ Tile decode_tile(int t, const int *tile_start, int E,
 __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }
 
 template <class C>
-__global__ void __launch_bounds__(GEMM_THREADS, 1) moe_gemm_kernel(const __grid_constant__ GemmParams p)
+__global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_kernel(const __grid_constant__ GemmParams p)
 {
     constexpr int MODE = C::MODE;
     using S = Smem<C>;
@@ -187,13 +194,13 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) moe_gemm_kernel(const __grid_
         if (lane == 31) scan_tmp[warp] = incl;
         __syncthreads();
         if (warp == 0) {
-            int w = lane < GEMM_THREADS / 32 ? scan_tmp[lane] : 0;
+            int w = lane < C::THREADS / 32 ? scan_tmp[lane] : 0;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
                 int n = __shfl_up_sync(0xFFFFFFFFu, w, o);
                 if (lane >= o) w += n;
             }
-            if (lane < GEMM_THREADS / 32) scan_tmp[lane] = w;
+            if (lane < C::THREADS / 32) scan_tmp[lane] = w;
         }
         __syncthreads();
         int excl = incl - s + (warp > 0 ? scan_tmp[warp - 1] : 0);
@@ -364,59 +371,47 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) moe_gemm_kernel(const __grid_
         }
     } else if (warp >= 8) {
         // ===================== converters: smem MXFP4 -> bf16 -> TMEM (A operand)
-        // Software-pipelined over the CTA's flat sequence of slabs: while the
-        // tcgen05.st of slab i drains into TMEM, slab i+1 is loaded and decoded.
-        const int cw = warp - 8, g = cw & 3, part = cw >> 2;
+        const int cw = warp - 8, grp = cw >> 3, g = cw & 3, part = (cw >> 2) & 1;
         const int row = g * 32 + lane;
         const uint32_t t_lane = (uint32_t)(g * 32) << 16;
         const int my_tiles = (int)blockIdx.x < total ? (total - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
         const int n_slabs = my_tiles * slabs;
-        int wi = 0, ai = 0;
-        uint32_t wph = 0, aph = 0;
+        static_assert(C::NW % C::GROUPS == 0 && C::NA % C::GROUPS == 0, "rings must split evenly between groups");
         bool ok = true;
-
-        // wait for the next weight slab, read this lane's 64 elements, free the stage, decode
-        auto load_decode = [&](uint32_t (&v)[32]) -> bool {
-            if (!__all_sync(0xFFFFFFFFu, ptx::mbar_wait(&w_full[wi], wph, s_abort, LIM))) return false;
+        for (int i = grp; i < n_slabs; i += C::GROUPS) {
+            const int wi = i % C::NW, ai = i % C::NA;
+            const uint32_t wph = (uint32_t)((i / C::NW) & 1), aph = (uint32_t)((i / C::NA) & 1);
+            if (!__all_sync(0xFFFFFFFFu, ptx::mbar_wait(&w_full[wi], wph, s_abort, LIM))) { ok = false; break; }
             const uint8_t *st = wring + wi * TILE_BYTES;
             const uint4 q0 = *reinterpret_cast<const uint4 *>(st + ((2 * part) * TILE_ROWS + row) * 16);
             const uint4 q1 = *reinterpret_cast<const uint4 *>(st + ((2 * part + 1) * TILE_ROWS + row) * 16);
             const uint32_t sc2 = *reinterpret_cast<const uint16_t *>(st + TILE_NIB_BYTES + row * 4 + 2 * part);
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(&w_empty[wi]);
-            if (++wi == C::NW) { wi = 0; wph ^= 1u; }
             const uint32_t s0 = sc2 & 0xFFu, s1 = sc2 >> 8;
             const bool big = __any_sync(0xFFFFFFFFu, s0 > 128u || s1 > 128u);
-            const uint32_t m10 = scale_mult_lo(s0), m20 = scale_mult_hi(s0);
-            decode_word(q0.x, m10, m20, big, v + 0);
-            decode_word(q0.y, m10, m20, big, v + 4);
-            decode_word(q0.z, m10, m20, big, v + 8);
-            decode_word(q0.w, m10, m20, big, v + 12);
-            const uint32_t m11 = scale_mult_lo(s1), m21 = scale_mult_hi(s1);
-            decode_word(q1.x, m11, m21, big, v + 16);
-            decode_word(q1.y, m11, m21, big, v + 20);
-            decode_word(q1.z, m11, m21, big, v + 24);
-            decode_word(q1.w, m11, m21, big, v + 28);
-            return true;
-        };
-        // store slab i (decoded in cur) into its A buffer; decode slab i+1 into nxt meanwhile
-        auto step = [&](uint32_t (&cur)[32], uint32_t (&nxt)[32], int i) -> bool {
-            if (!__all_sync(0xFFFFFFFFu, ptx::mbar_wait(&a_empty[ai], aph ^ 1u, s_abort, LIM))) return false;
+            uint32_t v[32];
+            {
+                const uint32_t m1 = scale_mult_lo(s0), m2 = scale_mult_hi(s0);
+                decode_word(q0.x, m1, m2, big, v + 0);
+                decode_word(q0.y, m1, m2, big, v + 4);
+                decode_word(q0.z, m1, m2, big, v + 8);
+                decode_word(q0.w, m1, m2, big, v + 12);
+            }
+            {
+                const uint32_t m1 = scale_mult_lo(s1), m2 = scale_mult_hi(s1);
+                decode_word(q1.x, m1, m2, big, v + 16);
+                decode_word(q1.y, m1, m2, big, v + 20);
+                decode_word(q1.z, m1, m2, big, v + 24);
+                decode_word(q1.w, m1, m2, big, v + 28);
+            }
+            if (!__all_sync(0xFFFFFFFFu, ptx::mbar_wait(&a_empty[ai], aph ^ 1u, s_abort, LIM))) { ok = false; break; }
             ptx::tc_fence_after();
-            ptx::tmem_st_32x32b_x32(tmem + t_lane + (uint32_t)(C::A_BASE + ai * A_COLS + part * 32), cur);
-            const bool more = i + 1 < n_slabs && load_decode(nxt);
+            ptx::tmem_st_32x32b_x32(tmem + t_lane + (uint32_t)(C::A_BASE + ai * A_COLS + part * 32), v);
             ptx::tmem_wait_st();
             ptx::tc_fence_before();
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(&a_full[ai]);
-            if (++ai == C::NA) { ai = 0; aph ^= 1u; }
-            return more || i + 1 >= n_slabs;
-        };
-        uint32_t va[32], vb[32];
-        if (n_slabs > 0) ok = load_decode(va);
-        for (int i = 0; i < n_slabs && ok; i += 2) {
-            if (!step(va, vb, i)) { ok = false; break; }
-            if (i + 1 < n_slabs && !step(vb, va, i + 1)) { ok = false; break; }
         }
         if (!ok && lane == 0) fail();
     } else if (warp < 4) {
@@ -547,7 +542,7 @@ cudaError_t launch_gemm(const GemmParams &p, int grid, cudaStream_t s)
         if (e != cudaSuccess) return e;
         if (dev < 64) __atomic_fetch_or(&attr_set, 1ull << dev, __ATOMIC_RELAXED);
     }
-    moe_gemm_kernel<C><<<grid, GEMM_THREADS, smem, s>>>(p);
+    moe_gemm_kernel<C><<<grid, C::THREADS, smem, s>>>(p);
     return cudaGetLastError();
 }
 
