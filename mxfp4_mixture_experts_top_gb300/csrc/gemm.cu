@@ -61,7 +61,7 @@ struct Cfg {
     // converter warps (8 or 16) in groups of 8; group j takes the slabs i with
     // i % GROUPS == j, so the latency chains of GROUPS slabs overlap. In a
     // group, warp (g, part) decodes chunks 2*part, 2*part+1 of rows 32g..32g+31.
-    static constexpr int CONVW = CONVW_, GROUPS = CONVW_ / 8;
+    static constexpr int GROUPS = CONVW_ / 8;
     static constexpr int THREADS = (8 + CONVW_) * 32;
     static_assert(CONVW_ == 8 || CONVW_ == 16, "converter warps");
     static constexpr int NOPS = MODE == 0 ? 1 : 2;
@@ -320,6 +320,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_kernel(const __grid_co
         }
     } else if (warp == 5) {
         // ===================== MMA issuer: per slab one A buffer, one activation stage
+        const uint64_t bdesc_base = ptx::smem_desc_sw128(ptx::smem_u32(bring));   // stage 0, offset 0
         int ai = 0, bi = 0, di = 0;
         uint32_t aph = 0, bph = 0, dph = 0;
         bool ok = true, issued = false;
@@ -334,20 +335,23 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_kernel(const __grid_co
                                                  ptx::mbar_wait(&b_full[bi], bph, s_abort, LIM))) { ok = false; break; }
                 ptx::tc_fence_after();
                 if (ptx::elect_one()) {
+                    // All per-MMA offsets are compile-time constants off three per-slab bases;
+                    // this warp shares its scheduler with busy converter warps, so every
+                    // instruction here costs several cycles.
                     const uint32_t at0 = tmem + (uint32_t)(C::A_BASE + ai * A_COLS);
-                    const uint32_t bb = ptx::smem_u32(bring + bi * S::BSTAGE);
-                    const int m0 = ka * MMAS_PER_SLAB;     // index of this slab's first MMA in the tile
+                    const uint64_t bd0 = bdesc_base + (uint64_t)((uint32_t)(bi * S::BSTAGE) >> 4);
+                    const uint32_t first = ka == 0 ? 0u : 1u;    // accumulate unless first use of an accumulator
 #pragma unroll
                     for (int half = 0; half < 2; ++half)
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk)
 #pragma unroll
                             for (int op = 0; op < C::NOPS; ++op) {
-                                const uint64_t bd = ptx::smem_desc_sw128(bb + (half * C::NOPS + op) * S::REGION + kk * 32);
-                                const int m = m0 + (half * 4 + kk) * C::NOPS + op;
-                                const uint32_t dt = dt0 + (uint32_t)((m % C::NACC) * C::NMAX);
-                                // the first MMA into an accumulator overwrites it
-                                ptx::mma_bf16_ts(dt, at0 + (uint32_t)((half * 4 + kk) * 8), bd, idesc, m >= C::NACC);
+                                const int mm = (half * 4 + kk) * C::NOPS + op;        // MMA index within the slab
+                                const uint32_t boff = (uint32_t)(((half * C::NOPS + op) * S::REGION + kk * 32) >> 4);
+                                ptx::mma_bf16_ts(dt0 + (uint32_t)((mm % C::NACC) * C::NMAX),
+                                                 at0 + (uint32_t)((half * 4 + kk) * 8), bd0 + boff, idesc,
+                                                 mm >= C::NACC ? 1u : first);
                             }
                     ptx::mma_commit(&b_empty[bi]);
                     ptx::mma_commit(&a_empty[ai]);

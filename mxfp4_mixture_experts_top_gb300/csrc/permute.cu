@@ -8,7 +8,9 @@
 // routing (the page's fix masks with offs_local < BLOCK_SIZE in addition to
 // the global bound). Every lane below carries that two-sided mask.
 //
-// Pairs p = t*k + j are split into 32 contiguous warp ranges. Phase 1: each
+// Pairs p = t*k + j are split into nw <= 32 contiguous warp ranges (about 64
+// pairs per warp, so a decode batch touches one or two histogram rows per
+// expert instead of 32). Phase 1: each
 // warp histograms its range into its own shared-memory row with
 // __match_any_sync (one leader per distinct expert per 32 lanes). Phase 2:
 // per expert, a scan over the warp rows turns counts into warp bases; a block
@@ -66,11 +68,12 @@ permute_kernel(const int32_t *__restrict__ ids, int T, int E, int k, int block_m
 
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     const int64_t P = (int64_t)T * k;
-    const int64_t lo = P * wid / PERM_WARPS, hi = P * (wid + 1) / PERM_WARPS;
+    const int nw = (int)(P / 64 + 1 < PERM_WARPS ? P / 64 + 1 : PERM_WARPS);   // warps holding pairs
+    const int64_t lo = wid < nw ? P * wid / nw : P, hi = wid < nw ? P * (wid + 1) / nw : P;
     const unsigned lt_mask = (1u << lane) - 1u;
 
     if (tid == 0) s_err = 0;
-    for (int i = tid; i < PERM_WARPS * E; i += PERM_THREADS) hist[i] = 0;
+    for (int i = tid; i < nw * E; i += PERM_THREADS) hist[i] = 0;
     __syncthreads();
 
     // Phase 1: per-warp histogram; lanes past this warp's range are masked.
@@ -82,6 +85,7 @@ permute_kernel(const int32_t *__restrict__ ids, int T, int E, int k, int block_m
         if (valid && (e < 0 || e >= E)) { e = -1; s_err = 1; }
         unsigned m = __match_any_sync(0xFFFFFFFFu, e);
         if (e >= 0 && (m & lt_mask) == 0u) my[e] += __popc(m);
+        __syncwarp();                                  // next iteration's leader may be another lane
     }
     __syncthreads();
 
@@ -89,7 +93,7 @@ permute_kernel(const int32_t *__restrict__ ids, int T, int E, int k, int block_m
     int c = 0, pc = 0;
     for (int e = tid; e < E; e += PERM_THREADS) {      // E <= 1024: at most one expert per thread
         int run = 0;
-        for (int w = 0; w < PERM_WARPS; ++w) {
+        for (int w = 0; w < nw; ++w) {
             int v = hist[w * E + e];
             hist[w * E + e] = run;
             run += v;
