@@ -46,7 +46,7 @@
 extern "C" {
 #endif
 
-#define MOE_ABI_VERSION 1
+#define MOE_ABI_VERSION 2
 
 /* Size of the static scratch array behind moe_mxfp4_forward_noalloc. */
 #define MOE_NOALLOC_SCRATCH_BYTES (32u << 20)
@@ -139,7 +139,11 @@ size_t moe_mxfp4_packed_bytes(const moe_layer_desc *desc);
  *   d_w2_q  uint8 [E, H, I/2],  d_w2_s  uint8 [E, H, I/32].
  * d_packed must hold moe_mxfp4_packed_bytes(desc) bytes. Each 128-row tile
  * of W13 pairs 64 gate rows with their 64 up rows (the gate/up interleave of
- * txtmix.com §三).
+ * txtmix.com §三). Per matrix the buffer holds the E2M1 bytes of every
+ * (expert, 128-row tile, 128-element K slab) as 128 contiguous 64-byte rows,
+ * then the E8M0 bytes of the same slabs, 512 per slab, in the order the
+ * tensor core reads block scales from tensor memory; the GEMMs stream both
+ * with TMA and never decode a weight on the SM.
  */
 moe_status_t moe_mxfp4_prepack(const moe_layer_desc *desc,
                                const uint8_t *d_w13_q, const uint8_t *d_w13_s,
@@ -148,8 +152,9 @@ moe_status_t moe_mxfp4_prepack(const moe_layer_desc *desc,
 
 /*
  * Decode prepacked weights of one expert back to dense bfloat16 in canonical
- * row order (exact: every E2M1 x E8M0 product is a bfloat16 value). Uses the
- * same on-chip decoder as the GEMMs.
+ * row order (exact: every E2M1 x E8M0 product is a bfloat16 value, or an
+ * infinity where it exceeds the fp32 range). Reads the same prepacked bytes
+ * and scale order the GEMMs feed to the tensor core.
  *   which 0: W13, d_out uint16 (bf16 bits) [2I, H]; which 1: W2, [H, I].
  */
 moe_status_t moe_mxfp4_dequant_bf16(const moe_layer_desc *desc, const void *d_packed,
@@ -175,10 +180,13 @@ size_t moe_mxfp4_workspace_bytes(const moe_layer_desc *desc);
  *   d_y              fp32 [T, H], fully overwritten.
  * d_workspace: moe_mxfp4_workspace_bytes(desc) bytes, contents need not be
  * initialised; the call resets its device error word.
- * Numerics: weights decoded exactly to bf16 on chip; bf16 x bf16 tensor-core
- * products accumulated in fp32; the SiLU product kept as a two-term bf16 sum
- * for the second GEMM; output fp32. Result within 2e-2 * rms of the float64
- * oracle (measured errors are far smaller).
+ * Numerics: block-scaled tensor-core MMAs (tcgen05 kind::mxf8f6f4) of the
+ * E2M1 weights with their E8M0 scales against the activations written as sums
+ * of MXFP8 terms (E4M3 values, one E8M0 scale per 32 K-elements, term scales
+ * 2^-4 apart): x in 2 terms (exact for bf16 unless a 32-element block spans
+ * more than 2^17), SiLU(gate)*up in 3 terms (about 12 significant bits);
+ * fp32 accumulation; output fp32. Result within 2e-2 * rms of the float64
+ * oracle (measured errors are about 1e-4 * rms).
  * Launches 4 kernels on `stream`; deterministic (bit-identical reruns).
  */
 moe_status_t moe_mxfp4_forward(const moe_layer_desc *desc, const uint16_t *d_x,
@@ -201,11 +209,13 @@ moe_status_t moe_mxfp4_forward_timed(const moe_layer_desc *desc, const uint16_t 
                                      void *const *events, void *stream);
 
 /* Byte offsets of the forward's intermediates inside the workspace, for
- * inspection: out[0] error word, out[1] gathered activations (bf16 [R, H]),
- * out[2] SiLU product high part (bf16 [R, I]), out[3] low part (bf16 [R, I]),
- * out[4] per-pair W2 outputs (fp32 [T*k, H]), out[5] total bytes;
- * R = moe_permute_rows_capacity(T, E, k, block_m). */
-moe_status_t moe_mxfp4_workspace_layout(const moe_layer_desc *desc, size_t out[6]);
+ * inspection: out[0] error word; out[1] gathered activation terms (E4M3
+ * [2][R][H]: term, permutation row, hidden unit); out[2] their E8M0 scales
+ * ([2][R][H/32]); out[3] SiLU(gate)*up terms (E4M3 [3][R][I]); out[4] their
+ * scales ([3][R][I/32]); out[5] per-pair W2 outputs (fp32 [T*k, H]); out[6]
+ * total bytes. R = moe_permute_rows_capacity(T, E, k, block_m). A row's value
+ * is sum over terms of E4M3 value * 2^(scale byte - 127). */
+moe_status_t moe_mxfp4_workspace_layout(const moe_layer_desc *desc, size_t out[7]);
 
 /*
  * Forward without a caller workspace, for callers that cannot allocate device

@@ -42,12 +42,13 @@ EncodeTiledFn encode_fn()
 }
 
 struct MapKey {
-    int dev;
+    int dev, kind;
     const void *ptr;
-    uint64_t inner, rows;
+    uint64_t d0, d1, d2;
+    uint32_t b1;
     bool operator<(const MapKey &o) const
     {
-        return std::tie(dev, ptr, inner, rows) < std::tie(o.dev, o.ptr, o.inner, o.rows);
+        return std::tie(dev, kind, ptr, d0, d1, d2, b1) < std::tie(o.dev, o.kind, o.ptr, o.d0, o.d1, o.d2, o.b1);
     }
 };
 
@@ -58,12 +59,16 @@ struct MapEntry {
 std::mutex g_map_mu;
 std::map<MapKey, MapEntry> g_maps;
 
-// 2-D bf16 tensor [rows, inner] (inner contiguous), box 64 x 16, 128-byte swizzle.
-const CUtensorMap *bf16_rows_map(const void *ptr, uint64_t inner, uint64_t rows, moe_status_t *st)
+// Cached tensor map. kind 0: prepacked weight nibbles, a 2-D tensor of d1 rows of 128 E2M1 values
+// (64 B) read as "16 x U4, 16-byte aligned" (each 8-byte group lands in 16 bytes of shared memory),
+// box 128 x b1 rows. kind 1: activation terms, a 3-D uint8 tensor [d2 terms][d1 rows][d0 K], box
+// 128 x b1 x d2. Both with the 128-byte swizzle of the MMA operands.
+const CUtensorMap *get_map(int kind, const void *ptr, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t b1,
+                           moe_status_t *st)
 {
     int dev = 0;
     cudaGetDevice(&dev);
-    MapKey key{dev, ptr, inner, rows};
+    MapKey key{dev, kind, ptr, d0, d1, d2, b1};
     std::lock_guard<std::mutex> lk(g_map_mu);
     auto it = g_maps.find(key);
     if (it != g_maps.end()) return &it->second.map;
@@ -71,13 +76,23 @@ const CUtensorMap *bf16_rows_map(const void *ptr, uint64_t inner, uint64_t rows,
     if (!fn) { *st = MOE_ERR_CUDA; return nullptr; }
     if (g_maps.size() > 4096) g_maps.clear();
     MapEntry ent;
-    cuuint64_t dims[2] = {inner, rows};
-    cuuint64_t strides[1] = {inner * 2};
-    cuuint32_t box[2] = {64, 16};
-    cuuint32_t estr[2] = {1, 1};
-    CUresult r = fn(&ent.map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult r;
+    cuuint32_t estr[3] = {1, 1, 1};
+    if (kind == 0) {
+        cuuint64_t dims[2] = {128, d1};
+        cuuint64_t strides[1] = {64};
+        cuuint32_t box[2] = {128, b1};
+        r = fn(&ent.map, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 2, const_cast<void *>(ptr), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    } else {
+        cuuint64_t dims[3] = {d0, d1, d2};
+        cuuint64_t strides[2] = {d0, d0 * d1};
+        cuuint32_t box[3] = {128, b1, (cuuint32_t)d2};
+        r = fn(&ent.map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(ptr), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    }
     if (r != CUDA_SUCCESS) { *st = MOE_ERR_CUDA; return nullptr; }
     auto res = g_maps.emplace(key, ent);
     return &res.first->second.map;
@@ -110,7 +125,7 @@ moe_status_t check_desc(const moe_layer_desc *d)
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 struct Layout {
-    size_t err, xp, hhi, hlo, staging, total;
+    size_t err, xq, xs, hq, hs, staging, total;
 };
 
 Layout workspace_layout(const moe_layer_desc *d)
@@ -119,10 +134,11 @@ Layout workspace_layout(const moe_layer_desc *d)
     const int64_t R = moe_permute_rows_capacity(d->T, d->E, d->k, d->block_m);
     Layout L;
     L.err = 0;
-    L.xp = 1024;
-    L.hhi = align_up(L.xp + (size_t)R * d->H * 2, 1024);
-    L.hlo = align_up(L.hhi + (size_t)R * d->I * 2, 1024);
-    L.staging = align_up(L.hlo + (size_t)R * d->I * 2, 1024);
+    L.xq = 1024;
+    L.xs = align_up(L.xq + (size_t)NT_X * R * d->H, 1024);
+    L.hq = align_up(L.xs + (size_t)NT_X * R * (d->H / 32), 1024);
+    L.hs = align_up(L.hq + (size_t)NT_H * R * d->I, 1024);
+    L.staging = align_up(L.hs + (size_t)NT_H * R * (d->I / 32), 1024);
     L.total = align_up(L.staging + (size_t)P * d->H * 4, 1024);
     return L;
 }
@@ -231,18 +247,19 @@ size_t moe_mxfp4_workspace_bytes(const moe_layer_desc *d)
     return workspace_layout(d).total;
 }
 
-moe_status_t moe_mxfp4_workspace_layout(const moe_layer_desc *d, size_t out[6])
+moe_status_t moe_mxfp4_workspace_layout(const moe_layer_desc *d, size_t out[7])
 {
     moe_status_t st = check_desc(d);
     if (st != MOE_OK) return st;
     if (!out) return MOE_ERR_INVALID_ARG;
     Layout L = workspace_layout(d);
     out[0] = L.err;
-    out[1] = L.xp;
-    out[2] = L.hhi;
-    out[3] = L.hlo;
-    out[4] = L.staging;
-    out[5] = L.total;
+    out[1] = L.xq;
+    out[2] = L.xs;
+    out[3] = L.hq;
+    out[4] = L.hs;
+    out[5] = L.staging;
+    out[6] = L.total;
     return MOE_OK;
 }
 
@@ -282,18 +299,26 @@ moe_status_t moe_mxfp4_forward_timed(const moe_layer_desc *d, const uint16_t *d_
     a.row_to_pair = d_row_to_pair;
     a.y = d_y;
     a.dev_error = reinterpret_cast<int32_t *>(ws + L.err);
-    a.xp = reinterpret_cast<uint16_t *>(ws + L.xp);
-    a.h_hi = reinterpret_cast<uint16_t *>(ws + L.hhi);
-    a.h_lo = reinterpret_cast<uint16_t *>(ws + L.hlo);
+    a.xq = ws + L.xq;
+    a.xs = ws + L.xs;
+    a.hq = ws + L.hq;
+    a.hs = ws + L.hs;
     a.staging = reinterpret_cast<float *>(ws + L.staging);
     a.num_sms = sm_count();
     a.events = events;
-    a.tmap_xp = bf16_rows_map(a.xp, (uint64_t)d->H, (uint64_t)R, &st);
-    if (!a.tmap_xp) return st;
-    a.tmap_hhi = bf16_rows_map(a.h_hi, (uint64_t)d->I, (uint64_t)R, &st);
-    if (!a.tmap_hhi) return st;
-    a.tmap_hlo = bf16_rows_map(a.h_lo, (uint64_t)d->I, (uint64_t)R, &st);
-    if (!a.tmap_hlo) return st;
+    a.regime = pick_regime(d->T, d->k, d->E);
+    const uint32_t sps = (uint32_t)regime_sps(a.regime);
+    const uint8_t *w13 = a.packed, *w2 = a.packed + packed_w13_bytes(d->E, d->H, d->I);
+    const uint64_t rows13 = (uint64_t)d->E * 2 * d->I * (d->H / KSLAB);   // 128-element rows of W13 nibbles
+    const uint64_t rows2 = (uint64_t)d->E * d->H * (d->I / KSLAB);
+    if (!(a.tmap_w13 = get_map(0, w13, 128, rows13, 1, 128 * sps, &st))) return st;
+    if (!(a.tmap_w13_1 = get_map(0, w13, 128, rows13, 1, 128, &st))) return st;
+    if (!(a.tmap_w2 = get_map(0, w2, 128, rows2, 1, 128 * sps, &st))) return st;
+    if (!(a.tmap_w2_1 = get_map(0, w2, 128, rows2, 1, 128, &st))) return st;
+    if (!(a.tmap_xq = get_map(1, a.xq, (uint64_t)d->H, (uint64_t)R, NT_X, (uint32_t)regime_nmax(a.regime, 0), &st)))
+        return st;
+    if (!(a.tmap_hq = get_map(1, a.hq, (uint64_t)d->I, (uint64_t)R, NT_H, (uint32_t)regime_nmax(a.regime, 1), &st)))
+        return st;
     if (cudaMemsetAsync(a.dev_error, 0, sizeof(int32_t), s) != cudaSuccess) return MOE_ERR_CUDA;
     return from_cuda(launch_forward(a, s));
 }

@@ -1,5 +1,6 @@
-// Grouped MXFP4 expert GEMMs on tcgen05 (sm_103a), plus the gather and the
-// routing-weighted combine.
+// Grouped MXFP4 expert GEMMs on tcgen05 block-scaled MMAs (sm_103a), plus the
+// gather that turns activations into MXFP8 terms and the routing-weighted
+// combine.
 //
 // Method: "DeepSeek V4 Flash 单卡 MI300X" (txtmix.com) §三 — grouped MXFP4
 // expert GEMMs, W13 with SiLU(gate)*up fused into its epilogue over a gate/up
@@ -7,35 +8,39 @@
 // combine y[t] = sum_j w[t,j] o_j is the routing-weighted scatter back to
 // token order.
 //
-// Design (swap-AB, weights as the tcgen05 A operand in TMEM):
-//   * A = 128 weight rows x K. MXFP4 tiles stream HBM -> shared memory by
-//     1-D bulk copies (8704 B per 128 x 128 slab); 8 converter warps decode
-//     E2M1 x E8M0 to exact bf16 in registers and write them straight into
-//     tensor memory with tcgen05.st, so the dequantised operand never touches
-//     shared memory (shared-memory bandwidth stays free for B).
-//   * B = the expert's N token rows (N <= 192 for W13, <= 128 for W2, a
-//     multiple of 16) loaded by 2-D TMA with the 128-byte swizzle.
-//   * D = fp32 accumulator in TMEM, double-buffered so the epilogue of one
-//     tile overlaps the main loop of the next.
-//   * One elected thread issues tcgen05.mma kind::f16 (M=128, N, K=16);
-//     completion is signalled with tcgen05.commit on mbarriers.
+// Design (swap-AB: weights are the M = 128 side, token rows the N side):
+//   * A = 128 weight rows x K as E2M1, fetched by TMA straight from the
+//     prepacked HBM layout into the padded shared-memory operand layout of
+//     tcgen05 kind::mxf8f6f4; A's E8M0 scales ride in the same stage and four
+//     warps copy them into a tensor-memory ring of scale-factor cells. No
+//     instruction of the SM decodes a weight: the tensor core applies the
+//     scales (block_scale, one scale per 32 K-elements, K = 32 per MMA).
+//   * B = the tile's token rows as NT MXFP8 terms (x: 2 terms, h: 3; see
+//     mxfp8_terms.cuh), stacked along N: B row t * NMAX + n is term t of token
+//     row n, so one MMA per 32-K block covers all terms and reads A once.
+//   * D = fp32 accumulators in TMEM, double-buffered so the epilogue of one
+//     tile overlaps the main loop of the next; the epilogue adds the NT term
+//     columns and the NACC accumulators of each token.
 //   * Persistent CTAs (one per SM) walk a tile list built on the device from
-//     the permutation offsets (no host synchronisation): expert-major, then
-//     token block, then weight row tile, so concurrent CTAs share B tiles in
-//     L2.
-//   * W2 consumes the SiLU product as hi + lo bf16 terms (two MMAs into the
-//     same accumulator), keeping ~16 bits of its precision.
-// Warp roles (512 threads, every role warp-converged): 0-3 epilogue, 4 weight producer (bulk copies),
-// 5 MMA issuer and TMEM owner, 6 activation producer (TMA), 7 idle, 8-15
-// converters. Every wait is bounded (2 s); on
-// time-out a CTA records MOE_ERR_TIMEOUT, drains its copies and MMAs, frees
-// TMEM and exits.
+//     the permutation offsets: expert-major, then token block, then weight
+//     row tile, so concurrent CTAs share B tiles in L2.
+//   * W13's epilogue applies SiLU(gate)*up, then splits h into 3 MXFP8 terms
+//     for W2 (block maxima over 32 features span two epilogue warps, which
+//     exchange them through shared memory).
+// Warp roles (352 threads): 0-3 epilogue, 4-7 scale-factor copiers (one per
+// TMEM lane quarter: the tensor core's sub-partition q reads the scale factors
+// of its 32 A rows, and of every B row, from lane quarter q, so each quarter
+// holds a full copy), 8 MMA issuer and TMEM owner, 9 activation producer (3-D
+// TMA), 10 weight producer (2-D TMA + bulk copy).
+// Every wait is bounded (2 s); on time-out a CTA records MOE_ERR_TIMEOUT,
+// drains its copies and MMAs, frees TMEM and exits.
 #include <cuda_bf16.h>
 
 #include <cstdint>
 
 #include "moe_internal.h"
 #include "mxfp4_tile.cuh"
+#include "mxfp8_terms.cuh"
 #include "ptx.cuh"
 
 namespace moe {
@@ -43,77 +48,79 @@ namespace moe {
 namespace {
 
 constexpr int TMEM_COLS = 512;
-constexpr int B_BOX_ROWS = 16;         // TMA box: 64 K elements (128 B) x 16 rows
-constexpr int A_COLS = KSLAB / 2;      // TMEM columns per A buffer (bf16 pairs)
 
-// Kernel configuration. MODE 0: W13 (activation rows -> SiLU(gate)*up),
-// MODE 1: W2 ((h_hi, h_lo) rows -> per-pair outputs). NMAX: most token rows
-// per tile (experts with more rows get several tiles). NB: activation ring
-// slots (the token rows of one 128-K slab each), NW: weight ring slots (one
-// 128 x 128 slab each), NA: TMEM A buffers, NACC: accumulators per tile (consecutive MMAs
-// of a tile rotate over them and the epilogue sums them: with small N an MMA
-// is short, and its latency rather than its work would otherwise set the
-// pace). TMEM columns: 2 * NACC * NMAX for the
-// double-buffered accumulators, then NA * 64 for the A buffers (<= 512).
-template <int MODE_, int NMAX_, int NB_, int NW_, int NA_, int NACC_, int CONVW_>
+// Kernel configuration. MODE 0: W13 (x terms -> SiLU(gate)*up -> h terms),
+// MODE 1: W2 (h terms -> per-pair outputs). NMAX: most token rows per tile
+// (experts with more rows get several tiles). NT: activation terms. SPS:
+// K-slabs per ring stage (a stage is one producer step; its fixed cost is
+// paid once per SPS slabs). NA / NB: weight / activation ring stages. NSF:
+// scale-factor cells in TMEM. NACC: accumulators per tile (consecutive
+// 32-K blocks rotate over them, so short MMAs do not wait on each other).
+template <int MODE_, int NMAX_, int NT_, int SPS_, int NA_, int NB_, int NSF_, int NACC_>
 struct Cfg {
-    static constexpr int MODE = MODE_, NMAX = NMAX_, NB = NB_, NW = NW_, NA = NA_, NACC = NACC_;
-    // converter warps (8 or 16) in groups of 8; group j takes the slabs i with
-    // i % GROUPS == j, so the latency chains of GROUPS slabs overlap. In a
-    // group, warp (g, part) decodes chunks 2*part, 2*part+1 of rows 32g..32g+31.
-    static constexpr int GROUPS = CONVW_ / 8;
-    static constexpr int THREADS = (8 + CONVW_) * 32;
-    static_assert(CONVW_ == 8 || CONVW_ == 16, "converter warps");
-    static constexpr int NOPS = MODE == 0 ? 1 : 2;
-    static constexpr int D_COLS = NACC * NMAX;            // one accumulator set
-    static constexpr int A_BASE = 2 * D_COLS;
-    static_assert(A_BASE + NA * A_COLS <= TMEM_COLS, "TMEM budget");
-    static_assert(NMAX % 16 == 0 && NMAX <= 256, "MMA N");
+    static constexpr int MODE = MODE_, NMAX = NMAX_, NT = NT_, SPS = SPS_, NA = NA_, NB = NB_, NSF = NSF_,
+                         NACC = NACC_;
+    static constexpr int NP = NT * NMAX;                       // MMA N: all terms of NMAX rows
+    static constexpr int SFB_COLS = (NP + 31) / 32;            // B scale cells: row j in column j / 32
+    static constexpr int SF_COLS = (4 + SFB_COLS + 3) / 4 * 4; // one ring cell: A (4 columns), then B
+    static constexpr int D_COLS = NACC * NP;                   // one accumulator set
+    static constexpr int SF_BASE = 2 * D_COLS;
+    static constexpr int THREADS = 352;
+    static_assert(NP % 16 == 0 && NP <= 256, "MMA N");
+    static_assert(NMAX % 16 == 0, "token rows per tile");
+    static_assert(SF_BASE + NSF * SF_COLS <= TMEM_COLS, "TMEM budget");
+    static_assert(SPS == 1 || SPS == 2, "slabs per stage");
 };
 
-// Decode-sized tiles are bound by decoding MXFP4 at the HBM rate: 16
-// converter warps, 6 A buffers. Prefill tiles are bound by the tensor pipe.
-// decode, <= 2 rows per expert on average: 16-row tiles
-using W13Tiny = Cfg<0, 16, 24, 12, 6, 2, 16>;
-using W2Tiny = Cfg<1, 16, 12, 12, 6, 2, 16>;
-// decode batches: <= 32 rows per tile
-using W13Small = Cfg<0, 32, 12, 12, 6, 2, 16>;
-using W2Small = Cfg<1, 32, 6, 12, 6, 2, 16>;
-// mid: <= 64 rows per tile
-using W13Mid = Cfg<0, 64, 6, 12, 4, 2, 16>;
-using W2Mid = Cfg<1, 64, 3, 12, 4, 2, 16>;
-// prefill: large tiles
-using W13Large = Cfg<0, 192, 2, 8, 2, 1, 8>;
-using W2Large = Cfg<1, 128, 2, 8, 4, 1, 8>;
+// decode, <= 2 rows per expert on average
+using W13Tiny = Cfg<0, 16, NT_X, 2, 5, 4, 8, 2>;
+using W2Tiny = Cfg<1, 16, NT_H, 2, 5, 3, 8, 2>;
+// decode batches: <= 16 rows per expert
+using W13Small = Cfg<0, 32, NT_X, 2, 4, 4, 8, 2>;
+using W2Small = Cfg<1, 32, NT_H, 2, 4, 3, 8, 2>;
+// <= 64 rows per expert
+using W13Mid = Cfg<0, 64, NT_X, 1, 6, 5, 8, 1>;
+using W2Mid = Cfg<1, 64, NT_H, 1, 5, 5, 8, 1>;
+// prefill
+using W13Large = Cfg<0, 96, NT_X, 1, 5, 5, 8, 1>;
+using W2Large = Cfg<1, 64, NT_H, 1, 5, 5, 8, 1>;
+static_assert(W13Large::NMAX == 96 && W2Large::NMAX == 64, "regime_nmax() mirrors these");
 
 struct GemmParams {
-    CUtensorMap tm_b0;        // W13: gathered x; W2: h_hi
-    CUtensorMap tm_b1;        // W2: h_lo
-    const uint8_t *wpack;     // this matrix's prepacked tiles
+    CUtensorMap tm_a;         // weight nibbles, box 128 x (128 * SPS) rows
+    CUtensorMap tm_a1;        // weight nibbles, box 128 x 128 rows (a stage that straddles two tiles)
+    CUtensorMap tm_b;         // activation terms [NT][rows][K] bytes, box 128 x NMAX x NT
+    const uint8_t *wsf;       // this matrix's prepacked scale region
+    const uint8_t *bsf;       // activation term scales [NT][rows_cap][K/32]
     const int32_t *offsets;   // [E+1]
     const int32_t *padded;    // [E+1]
     const int32_t *row_to_pair;
     int E, K, MB;             // MB: 128-row weight tiles per expert
     int I, H, k;
     float swiglu_limit;
-    int64_t P;
-    __nv_bfloat16 *h_hi, *h_lo;   // W13 out [rows, I]
-    float *staging;               // W2 out [P, H]
+    int64_t P, rows_cap;
+    uint8_t *hq;              // W13 out: h terms [NT_H][rows_cap][I]
+    uint8_t *hs;              // W13 out: h term scales [NT_H][rows_cap][I/32]
+    float *staging;           // W2 out [P, H]
     int32_t *dev_error;
 };
 
 template <class C>
 struct Smem {
-    static constexpr int REGION = C::NMAX * 128;                 // one 64-K box column of NMAX rows
-    static constexpr int BSTAGE = 2 * C::NOPS * REGION;            // [K half][operand][rows][128 B]
-    static constexpr int B_OFF = 0;
-    static constexpr int W_OFF = B_OFF + C::NB * BSTAGE;
-    static constexpr int BAR_OFF = W_OFF + C::NW * TILE_BYTES;
-    static constexpr int NBARS = 2 * C::NW + 2 * C::NB + 2 * C::NA + 2 * 2 + 1;
+    static constexpr int ASTAGE = C::SPS * SLAB_SMEM_BYTES;    // expanded E2M1 slabs
+    static constexpr int BSLAB = C::NP * 128;                 // [term][row][128 K bytes]
+    static constexpr int BSTAGE = C::SPS * BSLAB;
+    static constexpr int SFSTAGE = C::SPS * SLAB_SF_BYTES;
+    static constexpr int A_OFF = 0;
+    static constexpr int B_OFF = A_OFF + C::NA * ASTAGE;
+    static constexpr int SF_OFF = B_OFF + C::NB * BSTAGE;
+    static constexpr int BAR_OFF = SF_OFF + C::NA * SFSTAGE;
+    static constexpr int NBARS = 2 * C::NA + 2 * C::NB + 2 * C::NSF + 2 * 2 + 1;
     static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;
-    static constexpr int PREFIX_OFF = MISC_OFF + 16;
+    static constexpr int PAIRMAX_OFF = MISC_OFF + 16;         // W13 epilogue: [2 buffers][4 warps][16] floats
+    static constexpr int PREFIX_OFF = PAIRMAX_OFF + 2 * 4 * 16 * 4;
     static size_t bytes(int E) { return 1024 + PREFIX_OFF + sizeof(int) * (size_t)(E + 1 + 32); }
-    static_assert(BSTAGE % 1024 == 0, "B stages must keep the 1024-byte swizzle alignment");
+    static_assert(BSLAB % 1024 == 0 && ASTAGE % 1024 == 0, "stages must keep the 1024-byte swizzle alignment");
 };
 
 __device__ __forceinline__ void record_error(int32_t *dev_error, int code)
@@ -128,8 +135,8 @@ struct Tile {
 };
 
 template <class C>
-__device__ __forceinline__ Tile decode_tile(int t, const int *tile_start, int E, int MB,
-                                            const int32_t *offsets, const int32_t *padded)
+__device__ __forceinline__ Tile decode_tile(int t, const int *tile_start, int E, int MB, const int32_t *offsets,
+                                            const int32_t *padded)
 {
     constexpr int NMAX = C::NMAX;
     int lo = 0, hi = E - 1;                 // largest e with tile_start[e] <= t
@@ -155,40 +162,43 @@ __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g));
 template <class C>
 __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_kernel(const __grid_constant__ GemmParams p)
 {
-    constexpr int MODE = C::MODE;
+    constexpr int MODE = C::MODE, NMAX = C::NMAX, NT = C::NT, SPS = C::SPS, NP = C::NP;
     using S = Smem<C>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *aring = smem + S::A_OFF;
     uint8_t *bring = smem + S::B_OFF;
-    uint8_t *wring = smem + S::W_OFF;
+    uint8_t *sfring = smem + S::SF_OFF;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + S::BAR_OFF);
-    uint64_t *w_full = bars, *w_empty = w_full + C::NW;
-    uint64_t *b_full = w_empty + C::NW, *b_empty = b_full + C::NB;
-    uint64_t *a_full = b_empty + C::NB, *a_empty = a_full + C::NA;
-    uint64_t *d_full = a_empty + C::NA, *d_empty = d_full + 2;
+    uint64_t *a_full = bars, *a_empty = a_full + C::NA;
+    uint64_t *b_full = a_empty + C::NA, *b_empty = b_full + C::NB;
+    uint64_t *sf_full = b_empty + C::NB, *sf_empty = sf_full + C::NSF;
+    uint64_t *d_full = sf_empty + C::NSF, *d_empty = d_full + 2;
     uint64_t *mma_done = d_empty + 2;
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(smem + S::MISC_OFF);
     volatile int *s_abort = reinterpret_cast<volatile int *>(smem + S::MISC_OFF + 4);
+    float *pairmax = reinterpret_cast<float *>(smem + S::PAIRMAX_OFF);
     int *tile_start = reinterpret_cast<int *>(smem + S::PREFIX_OFF);
     int *scan_tmp = tile_start + p.E + 1;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int E = p.E, MB = p.MB;
 
-    // ---- tile prefix over experts (E <= 1024: two experts per thread)
+    // ---- tile prefix over experts (E <= 1024: four experts per thread)
     {
-        int v[2];
+        int v[4];
+        int s = 0;
 #pragma unroll
-        for (int q = 0; q < 2; ++q) {
-            int e = tid * 2 + q;
-            int cnt = e < E ? (__ldg(p.offsets + e + 1) - __ldg(p.offsets + e)) : 0;
-            v[q] = (cnt + C::NMAX - 1) / C::NMAX * MB;
+        for (int q = 0; q < 4; ++q) {
+            const int e = tid * 4 + q;
+            const int cnt = e < E ? (__ldg(p.offsets + e + 1) - __ldg(p.offsets + e)) : 0;
+            v[q] = (cnt + NMAX - 1) / NMAX * MB;
+            s += v[q];
         }
-        int s = v[0] + v[1];
         int incl = s;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            int n = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+            const int n = __shfl_up_sync(0xFFFFFFFFu, incl, o);
             if (lane >= o) incl += n;
         }
         if (lane == 31) scan_tmp[warp] = incl;
@@ -197,18 +207,20 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_kernel(const __grid_co
             int w = lane < C::THREADS / 32 ? scan_tmp[lane] : 0;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
-                int n = __shfl_up_sync(0xFFFFFFFFu, w, o);
+                const int n = __shfl_up_sync(0xFFFFFFFFu, w, o);
                 if (lane >= o) w += n;
             }
             if (lane < C::THREADS / 32) scan_tmp[lane] = w;
         }
         __syncthreads();
-        int excl = incl - s + (warp > 0 ? scan_tmp[warp - 1] : 0);
-        int e0 = tid * 2;
-        if (e0 < E) tile_start[e0] = excl;
-        if (e0 + 1 < E) tile_start[e0 + 1] = excl + v[0];
-        if (e0 + 1 == E) tile_start[E] = excl + v[0];
-        if (e0 + 2 == E) tile_start[E] = excl + v[0] + v[1];
+        int run = incl - s + (warp > 0 ? scan_tmp[warp - 1] : 0);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int e = tid * 4 + q;
+            if (e < E) tile_start[e] = run;
+            run += v[q];
+        }
+        if (tid == C::THREADS - 1) tile_start[E] = run;   // the total
         __syncthreads();
     }
     const int total = tile_start[E];
@@ -216,12 +228,9 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_kernel(const __grid_co
 
     // ---- barriers and TMEM
     if (tid == 0) {
-        for (int i = 0; i < C::NW; ++i) { ptx::mbar_init(&w_full[i], 1); ptx::mbar_init(&w_empty[i], 8); }
+        for (int i = 0; i < C::NA; ++i) { ptx::mbar_init(&a_full[i], 1); ptx::mbar_init(&a_empty[i], 1); }
         for (int i = 0; i < C::NB; ++i) { ptx::mbar_init(&b_full[i], 1); ptx::mbar_init(&b_empty[i], 1); }
-        for (int i = 0; i < C::NA; ++i) {
-            ptx::mbar_init(&a_full[i], 8);
-            ptx::mbar_init(&a_empty[i], 1);
-        }
+        for (int i = 0; i < C::NSF; ++i) { ptx::mbar_init(&sf_full[i], 4); ptx::mbar_init(&sf_empty[i], 1); }
         for (int i = 0; i < 2; ++i) {
             ptx::mbar_init(&d_full[i], 1);
             ptx::mbar_init(&d_empty[i], 4);
@@ -230,7 +239,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_kernel(const __grid_co
         *s_abort = 0;
         ptx::fence_mbar_init();
     }
-    if (warp == 5) {
+    if (warp == 8) {
         ptx::tmem_alloc(s_tmem, TMEM_COLS);
         ptx::tmem_relinquish();
     }
@@ -239,127 +248,204 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_kernel(const __grid_co
     ptx::tc_fence_after();
     const uint32_t tmem = *s_tmem;
     const int slabs = p.K / KSLAB;
-    constexpr int MMAS_PER_SLAB = 8 * C::NOPS;             // K = 128 in steps of 16, per operand
-    const int nacc = slabs * MMAS_PER_SLAB < C::NACC ? slabs * MMAS_PER_SLAB : C::NACC;   // accumulators written
+    // This CTA's slabs, in order: tiles blockIdx.x, blockIdx.x + gridDim.x, ..., each with `slabs`
+    // K-slabs; slab i sits in ring stage i / SPS at position i % SPS.
+    const int my_tiles = (total - 1 - (int)blockIdx.x) / (int)gridDim.x + 1;
+    const int n_slabs = my_tiles * slabs;
     const uint64_t LIM = WAIT_LIMIT_NS;
 
     auto fail = [&]() {
         *s_abort = 1;
         record_error(p.dev_error, DEV_ERR_TIMEOUT);
     };
+    // first 128-element row of (tile, slab) in the 2-D view of the nibble region
+    auto a_row = [&](const Tile &tl, int ka) { return ((tl.e * MB + tl.mb) * slabs + ka) * TILE_ROWS; };
 
-    // Warps 4, 5 and 6 run their loops with all 32 lanes converged; one lane
-    // issues each copy / MMA / commit (see ptx::elect_one).
-    if (warp == 4) {
-        // ===================== weight producer: one 8704-byte bulk copy per 128 x 128 slab
-        int wi = 0;
-        uint32_t wph = 0;
+    if (warp == 10) {
+        // ===================== weight producer: per stage one TMA box of SPS slabs (E2M1 rows,
+        // expanded in shared memory) and one bulk copy of their scales; two of each when the stage
+        // straddles two tiles
+        if (ptx::elect_one()) {
+            ptx::prefetch_tmap(&p.tm_a);
+            ptx::prefetch_tmap(&p.tm_a1);
+        }
+        __syncwarp();
+        int ai = 0;
+        uint32_t aph = 0;
         long long issued = 0;
         bool ok = true;
-        for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-            Tile tl = decode_tile<C>(t, tile_start, E, MB, p.offsets, p.padded);
-            const uint8_t *wsrc = p.wpack + ((size_t)tl.e * MB + tl.mb) * (size_t)slabs * TILE_BYTES;
-            for (int ka = 0; ka < slabs; ++ka) {
-                if (!__all_sync(0xFFFFFFFFu, ptx::mbar_wait(&w_empty[wi], wph ^ 1u, s_abort, LIM))) { ok = false; break; }
-                if (ptx::elect_one()) {
-                    ptx::mbar_arrive_expect_tx(&w_full[wi], TILE_BYTES);
-                    ptx::bulk_g2s(wring + wi * TILE_BYTES, wsrc + (size_t)ka * TILE_BYTES, TILE_BYTES, &w_full[wi]);
+        int tcur = blockIdx.x, ka = 0;
+        Tile tl = decode_tile<C>(tcur, tile_start, E, MB, p.offsets, p.padded);
+        for (int i0 = 0; i0 < n_slabs; i0 += SPS) {
+            if (!__all_sync(0xFFFFFFFFu, ptx::mbar_wait(&a_empty[ai], aph ^ 1u, s_abort, LIM))) { ok = false; break; }
+            const int nsl = n_slabs - i0 < SPS ? n_slabs - i0 : SPS;
+            if (ptx::elect_one()) {
+                uint8_t *dst = aring + ai * S::ASTAGE;
+                uint8_t *sdst = sfring + ai * S::SFSTAGE;
+                // the TMA counts the bytes it reads (8 KB per slab), not the expanded 16 KB it writes
+                ptx::mbar_arrive_expect_tx(&a_full[ai], (uint32_t)(nsl * (SLAB_NIB_BYTES + SLAB_SF_BYTES)));
+                const int r0 = a_row(tl, ka);
+                if (nsl == SPS && ka + SPS <= slabs) {
+                    ptx::tma_load_2d(dst, &p.tm_a, 0, r0, &a_full[ai]);
+                    ptx::bulk_g2s(sdst, p.wsf + (size_t)(r0 / TILE_ROWS) * SLAB_SF_BYTES,
+                                  (uint32_t)(SPS * SLAB_SF_BYTES), &a_full[ai]);
+                } else {
+                    ptx::tma_load_2d(dst, &p.tm_a1, 0, r0, &a_full[ai]);
+                    ptx::bulk_g2s(sdst, p.wsf + (size_t)(r0 / TILE_ROWS) * SLAB_SF_BYTES, SLAB_SF_BYTES, &a_full[ai]);
+                    if (nsl == 2) {                  // the second slab opens the next tile
+                        const Tile t2 = decode_tile<C>(tcur + (int)gridDim.x, tile_start, E, MB, p.offsets, p.padded);
+                        const int r1 = a_row(t2, 0);
+                        ptx::tma_load_2d(dst + SLAB_SMEM_BYTES, &p.tm_a1, 0, r1, &a_full[ai]);
+                        ptx::bulk_g2s(sdst + SLAB_SF_BYTES, p.wsf + (size_t)(r1 / TILE_ROWS) * SLAB_SF_BYTES,
+                                      SLAB_SF_BYTES, &a_full[ai]);
+                    }
                 }
-                __syncwarp();
-                ++issued;
-                if (++wi == C::NW) { wi = 0; wph ^= 1u; }
             }
+            __syncwarp();
+            ++issued;
+            ka += nsl;
+            bool next_tile = false;
+            while (ka >= slabs) {
+                ka -= slabs;
+                tcur += gridDim.x;
+                next_tile = true;
+            }
+            if (next_tile && tcur < total) tl = decode_tile<C>(tcur, tile_start, E, MB, p.offsets, p.padded);
+            if (++ai == C::NA) { ai = 0; aph ^= 1u; }
         }
         if (!ok && lane == 0) fail();
         volatile int never = 0;
         // drain: every issued copy must land before shared memory is released
-        for (long long i = 1; i <= (issued < C::NW ? issued : C::NW); ++i) {
-            long long n = issued - i;
-            __all_sync(0xFFFFFFFFu, ptx::mbar_wait(&w_full[n % C::NW], (uint32_t)((n / C::NW) & 1), &never, LIM));
+        for (long long i = 1; i <= (issued < C::NA ? issued : C::NA); ++i) {
+            const long long n = issued - i;
+            __all_sync(0xFFFFFFFFu, ptx::mbar_wait(&a_full[n % C::NA], (uint32_t)((n / C::NA) & 1), &never, LIM));
         }
-    } else if (warp == 6) {
-        // ===================== activation producer: the tile's token rows of one 128-K slab per
-        // stage, as 2-D TMA boxes of 64 K x 16 rows
-        if (ptx::elect_one()) {
-            ptx::prefetch_tmap(&p.tm_b0);
-            if (C::NOPS > 1) ptx::prefetch_tmap(&p.tm_b1);
-        }
+    } else if (warp == 9) {
+        // ===================== activation producer: per slab one 3-D TMA box (128 K x NMAX rows x NT
+        // terms); one arrival per stage of SPS slabs
+        if (ptx::elect_one()) ptx::prefetch_tmap(&p.tm_b);
         __syncwarp();
-        int bi = 0;
+        int bi = 0, pos = 0, i = 0;
         uint32_t bph = 0;
         long long issued = 0;
         bool ok = true;
+        constexpr uint32_t BBYTES = (uint32_t)(NP * 128);
         for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-            Tile tl = decode_tile<C>(t, tile_start, E, MB, p.offsets, p.padded);
-            const uint32_t bbytes = (uint32_t)(2 * C::NOPS * tl.n * 128);
-            for (int ka = 0; ka < slabs; ++ka) {
-                if (!__all_sync(0xFFFFFFFFu, ptx::mbar_wait(&b_empty[bi], bph ^ 1u, s_abort, LIM))) { ok = false; break; }
+            const Tile tl = decode_tile<C>(t, tile_start, E, MB, p.offsets, p.padded);
+            for (int ka = 0; ka < slabs; ++ka, ++i) {
+                if (pos == 0) {
+                    if (!__all_sync(0xFFFFFFFFu, ptx::mbar_wait(&b_empty[bi], bph ^ 1u, s_abort, LIM))) { ok = false; break; }
+                }
+                const bool last = pos == SPS - 1 || i == n_slabs - 1;   // this slab closes the stage
                 if (ptx::elect_one()) {
-                    ptx::mbar_arrive_expect_tx(&b_full[bi], bbytes);
-                    uint8_t *stage = bring + bi * S::BSTAGE;
-                    for (int half = 0; half < 2; ++half) {
-                        const int kx = ka * KSLAB + half * 64;
-                        uint8_t *dst = stage + half * C::NOPS * S::REGION;
-                        for (int r = 0; r < tl.n; r += B_BOX_ROWS)
-                            ptx::tma_load_2d(dst + r * 128, &p.tm_b0, kx, tl.row0 + r, &b_full[bi]);
-                        if (C::NOPS > 1)
-                            for (int r = 0; r < tl.n; r += B_BOX_ROWS)
-                                ptx::tma_load_2d(dst + S::REGION + r * 128, &p.tm_b1, kx, tl.row0 + r, &b_full[bi]);
-                    }
+                    if (last) ptx::mbar_arrive_expect_tx(&b_full[bi], BBYTES);
+                    else ptx::mbar_expect_tx(&b_full[bi], BBYTES);
+                    ptx::tma_load_3d(bring + bi * S::BSTAGE + pos * S::BSLAB, &p.tm_b, ka * KSLAB, tl.row0, 0, &b_full[bi]);
                 }
                 __syncwarp();
-                ++issued;
-                if (++bi == C::NB) { bi = 0; bph ^= 1u; }
+                if (last) {
+                    ++issued;
+                    pos = 0;
+                    if (++bi == C::NB) { bi = 0; bph ^= 1u; }
+                } else {
+                    ++pos;
+                }
             }
         }
         if (!ok && lane == 0) fail();
         volatile int never = 0;
-        for (long long i = 1; i <= (issued < C::NB ? issued : C::NB); ++i) {
-            long long n = issued - i;
+        // a stage is left only after its closing arrival, so every issued stage can complete
+        for (long long i2 = 1; i2 <= (issued < C::NB ? issued : C::NB); ++i2) {
+            const long long n = issued - i2;
             __all_sync(0xFFFFFFFFu, ptx::mbar_wait(&b_full[n % C::NB], (uint32_t)((n / C::NB) & 1), &never, LIM));
         }
-    } else if (warp == 5) {
-        // ===================== MMA issuer: per slab one A buffer, one activation stage
-        const uint64_t bdesc_base = ptx::smem_desc_sw128(ptx::smem_u32(bring));   // stage 0, offset 0
-        int ai = 0, bi = 0, di = 0;
-        uint32_t aph = 0, bph = 0, dph = 0;
+    } else if (warp >= 4 && warp < 8) {
+        // ===================== scale-factor copiers: per slab, A's cells from the weight stage and B's
+        // (one 32-bit cell per B row: its 4 K-block scales) from global memory, into the next ring
+        // cell of this warp's TMEM lane quarter; lane r of every quarter holds rows r, r + 32, ... in
+        // consecutive columns.
+        int i = 0, si = 0;
+        uint32_t sph = 0;
+        bool ok = true;
+        const int kq = p.K / 32;                     // scale bytes per activation row
+        for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+            const Tile tl = decode_tile<C>(t, tile_start, E, MB, p.offsets, p.padded);
+            for (int ka = 0; ka < slabs; ++ka, ++i) {
+                uint32_t bw[C::SFB_COLS];
+#pragma unroll
+                for (int c = 0; c < C::SFB_COLS; ++c) {
+                    const int j = lane + 32 * c;          // B row: term j / NMAX of token row j % NMAX
+                    const int64_t row = (int64_t)tl.row0 + (j % NMAX);
+                    bw[c] = (j < NP && row < p.rows_cap)
+                                ? __ldg(reinterpret_cast<const uint32_t *>(
+                                      p.bsf + ((int64_t)(j / NMAX) * p.rows_cap + row) * kq + ka * 4))
+                                : 0u;
+                }
+                const int st = i / SPS, ai = st % C::NA;
+                const uint32_t aph = (uint32_t)((st / C::NA) & 1);
+                if (!__all_sync(0xFFFFFFFFu, ptx::mbar_wait(&sf_empty[si], sph ^ 1u, s_abort, LIM) &&
+                                                 ptx::mbar_wait(&a_full[ai], aph, s_abort, LIM))) { ok = false; break; }
+                const uint4 aw = *reinterpret_cast<const uint4 *>(sfring + ai * S::SFSTAGE + (i % SPS) * SLAB_SF_BYTES +
+                                                                  lane * 16);
+                ptx::tc_fence_after();
+                const uint32_t cell = tmem + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)(C::SF_BASE + si * C::SF_COLS);
+                ptx::tmem_st_32x32b_x4(cell, aw.x, aw.y, aw.z, aw.w);
+#pragma unroll
+                for (int c = 0; c < C::SFB_COLS; ++c) ptx::tmem_st_32x32b_x1(cell + 4 + (uint32_t)c, bw[c]);
+                ptx::tmem_wait_st();
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(&sf_full[si]);
+                if (++si == C::NSF) { si = 0; sph ^= 1u; }
+            }
+        }
+        if (!ok && lane == 0) fail();
+    } else if (warp == 8) {
+        // ===================== MMA issuer: per slab four block-scaled MMAs (K = 32 each)
+        const uint64_t adesc0 = ptx::smem_desc_sw128(ptx::smem_u32(aring));
+        const uint64_t bdesc0 = ptx::smem_desc_sw128(ptx::smem_u32(bring));
+        int i = 0, si = 0, bi = 0, di = 0, pos = 0;
+        uint32_t sph = 0, bph = 0, dph = 0;
         bool ok = true, issued = false;
         for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-            Tile tl = decode_tile<C>(t, tile_start, E, MB, p.offsets, p.padded);
-            const uint32_t idesc = ptx::idesc_bf16_f32(128, (uint32_t)tl.n);
             if (!__all_sync(0xFFFFFFFFu, ptx::mbar_wait(&d_empty[di], dph ^ 1u, s_abort, LIM))) { ok = false; break; }
             ptx::tc_fence_after();
             const uint32_t dt0 = tmem + (uint32_t)(di * C::D_COLS);
-            for (int ka = 0; ka < slabs; ++ka) {
-                if (!__all_sync(0xFFFFFFFFu, ptx::mbar_wait(&a_full[ai], aph, s_abort, LIM) &&
-                                                 ptx::mbar_wait(&b_full[bi], bph, s_abort, LIM))) { ok = false; break; }
+            for (int ka = 0; ka < slabs; ++ka, ++i) {
+                const int st = i / SPS, ai = st % C::NA;
+                const uint32_t aph = (uint32_t)((st / C::NA) & 1);
+                if (!__all_sync(0xFFFFFFFFu, ptx::mbar_wait(&sf_full[si], sph, s_abort, LIM) &&
+                                                 ptx::mbar_wait(&a_full[ai], aph, s_abort, LIM) &&
+                                                 (pos != 0 || ptx::mbar_wait(&b_full[bi], bph, s_abort, LIM)))) { ok = false; break; }
                 ptx::tc_fence_after();
+                const bool last = pos == SPS - 1 || i == n_slabs - 1;
                 if (ptx::elect_one()) {
-                    // All per-MMA offsets are compile-time constants off three per-slab bases;
-                    // this warp shares its scheduler with busy converter warps, so every
-                    // instruction here costs several cycles.
-                    const uint32_t at0 = tmem + (uint32_t)(C::A_BASE + ai * A_COLS);
-                    const uint64_t bd0 = bdesc_base + (uint64_t)((uint32_t)(bi * S::BSTAGE) >> 4);
-                    const uint32_t first = ka == 0 ? 0u : 1u;    // accumulate unless first use of an accumulator
+                    const uint64_t ad = adesc0 + (uint64_t)((uint32_t)(ai * S::ASTAGE + pos * SLAB_SMEM_BYTES) >> 4);
+                    const uint64_t bd = bdesc0 + (uint64_t)((uint32_t)(bi * S::BSTAGE + pos * S::BSLAB) >> 4);
+                    const uint32_t sfa = tmem + (uint32_t)(C::SF_BASE + si * C::SF_COLS), sfb = sfa + 4;
 #pragma unroll
-                    for (int half = 0; half < 2; ++half)
-#pragma unroll
-                        for (int kk = 0; kk < 4; ++kk)
-#pragma unroll
-                            for (int op = 0; op < C::NOPS; ++op) {
-                                const int mm = (half * 4 + kk) * C::NOPS + op;        // MMA index within the slab
-                                const uint32_t boff = (uint32_t)(((half * C::NOPS + op) * S::REGION + kk * 32) >> 4);
-                                ptx::mma_bf16_ts(dt0 + (uint32_t)((mm % C::NACC) * C::NMAX),
-                                                 at0 + (uint32_t)((half * 4 + kk) * 8), bd0 + boff, idesc,
-                                                 mm >= C::NACC ? 1u : first);
-                            }
-                    ptx::mma_commit(&b_empty[bi]);
-                    ptx::mma_commit(&a_empty[ai]);
+                    for (int kb = 0; kb < 4; ++kb) {
+                        const int kk = ka * 4 + kb;          // 32-K block index in the tile
+                        // overwrite on the first use of each accumulator in the tile
+                        ptx::mma_mx_ss(dt0 + (uint32_t)((kk % C::NACC) * NP), ad + (uint64_t)(kb * 2),
+                                       bd + (uint64_t)(kb * 2), ptx::idesc_mx_e2m1_e4m3(128, NP, (uint32_t)kb), sfa, sfb,
+                                       kk >= C::NACC ? 1u : 0u);
+                    }
+                    ptx::mma_commit(&sf_empty[si]);
+                    if (last) {
+                        ptx::mma_commit(&a_empty[ai]);
+                        ptx::mma_commit(&b_empty[bi]);
+                    }
                 }
                 __syncwarp();
                 issued = true;
-                if (++bi == C::NB) { bi = 0; bph ^= 1u; }
-                if (++ai == C::NA) { ai = 0; aph ^= 1u; }
+                if (++si == C::NSF) { si = 0; sph ^= 1u; }
+                if (last) {
+                    pos = 0;
+                    if (++bi == C::NB) { bi = 0; bph ^= 1u; }
+                } else {
+                    ++pos;
+                }
             }
             if (!ok) break;
             if (ptx::elect_one()) ptx::mma_commit(&d_full[di]);
@@ -373,79 +459,43 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_kernel(const __grid_co
             __syncwarp();
             __all_sync(0xFFFFFFFFu, ptx::mbar_wait(mma_done, 0, &never, LIM));
         }
-    } else if (warp >= 8) {
-        // ===================== converters: smem MXFP4 -> bf16 -> TMEM (A operand)
-        const int cw = warp - 8, grp = cw >> 3, g = cw & 3, part = (cw >> 2) & 1;
-        const int row = g * 32 + lane;
-        const uint32_t t_lane = (uint32_t)(g * 32) << 16;
-        const int my_tiles = (int)blockIdx.x < total ? (total - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
-        const int n_slabs = my_tiles * slabs;
-        static_assert(C::NW % C::GROUPS == 0 && C::NA % C::GROUPS == 0, "rings must split evenly between groups");
-        bool ok = true;
-        for (int i = grp; i < n_slabs; i += C::GROUPS) {
-            const int wi = i % C::NW, ai = i % C::NA;
-            const uint32_t wph = (uint32_t)((i / C::NW) & 1), aph = (uint32_t)((i / C::NA) & 1);
-            if (!__all_sync(0xFFFFFFFFu, ptx::mbar_wait(&w_full[wi], wph, s_abort, LIM))) { ok = false; break; }
-            const uint8_t *st = wring + wi * TILE_BYTES;
-            const uint4 q0 = *reinterpret_cast<const uint4 *>(st + ((2 * part) * TILE_ROWS + row) * 16);
-            const uint4 q1 = *reinterpret_cast<const uint4 *>(st + ((2 * part + 1) * TILE_ROWS + row) * 16);
-            const uint32_t sc2 = *reinterpret_cast<const uint16_t *>(st + TILE_NIB_BYTES + row * 4 + 2 * part);
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(&w_empty[wi]);
-            const uint32_t s0 = sc2 & 0xFFu, s1 = sc2 >> 8;
-            const bool big = __any_sync(0xFFFFFFFFu, s0 > 128u || s1 > 128u);
-            uint32_t v[32];
-            {
-                const uint32_t m1 = scale_mult_lo(s0), m2 = scale_mult_hi(s0);
-                decode_word(q0.x, m1, m2, big, v + 0);
-                decode_word(q0.y, m1, m2, big, v + 4);
-                decode_word(q0.z, m1, m2, big, v + 8);
-                decode_word(q0.w, m1, m2, big, v + 12);
-            }
-            {
-                const uint32_t m1 = scale_mult_lo(s1), m2 = scale_mult_hi(s1);
-                decode_word(q1.x, m1, m2, big, v + 16);
-                decode_word(q1.y, m1, m2, big, v + 20);
-                decode_word(q1.z, m1, m2, big, v + 24);
-                decode_word(q1.w, m1, m2, big, v + 28);
-            }
-            if (!__all_sync(0xFFFFFFFFu, ptx::mbar_wait(&a_empty[ai], aph ^ 1u, s_abort, LIM))) { ok = false; break; }
-            ptx::tc_fence_after();
-            ptx::tmem_st_32x32b_x32(tmem + t_lane + (uint32_t)(C::A_BASE + ai * A_COLS + part * 32), v);
-            ptx::tmem_wait_st();
-            ptx::tc_fence_before();
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(&a_full[ai]);
-        }
-        if (!ok && lane == 0) fail();
     } else if (warp < 4) {
-        // ===================== epilogue: TMEM -> registers -> global
+        // ===================== epilogue: TMEM -> registers -> global. The W13 epilogue pairs warps
+        // at a named barrier, so no warp leaves the tile loop early: after a failed wait a warp
+        // skips the work but still meets its partner at every barrier.
         const uint32_t t_lane = (uint32_t)(warp * 32) << 16;
-        int di = 0;
+        int di = 0, chunk = 0;
         uint32_t dph = 0;
         bool ok = true;
-        for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-            Tile tl = decode_tile<C>(t, tile_start, E, MB, p.offsets, p.padded);
-            if (!__all_sync(0xFFFFFFFFu, ptx::mbar_wait(&d_full[di], dph, s_abort, LIM))) { ok = false; break; }
+        for (int t = blockIdx.x; t < total; t += gridDim.x) {
+            const Tile tl = decode_tile<C>(t, tile_start, E, MB, p.offsets, p.padded);
+            ok = ok && __all_sync(0xFFFFFFFFu, ptx::mbar_wait(&d_full[di], dph, s_abort, LIM));
             ptx::tc_fence_after();
             const uint32_t dt = tmem + t_lane + (uint32_t)(di * C::D_COLS);
-            for (int c0 = 0; c0 < tl.n; c0 += 16) {
+            for (int c0 = 0; c0 < tl.n; c0 += 16, ++chunk) {
                 uint32_t raw[16];
-                ptx::tmem_ld_32x32b_x16(dt + (uint32_t)c0, raw);
-                ptx::tmem_wait_ld();
-                for (int acc = 1; acc < nacc; ++acc) {          // sum the split accumulators
-                    uint32_t part[16];
-                    ptx::tmem_ld_32x32b_x16(dt + (uint32_t)(acc * C::NMAX + c0), part);
-                    ptx::tmem_wait_ld();
 #pragma unroll
-                    for (int j = 0; j < 16; ++j)
-                        raw[j] = __float_as_uint(__uint_as_float(raw[j]) + __uint_as_float(part[j]));
+                for (int q = 0; q < 16; ++q) raw[q] = 0u;
+                if (ok) {
+#pragma unroll
+                    for (int a = 0; a < C::NACC; ++a)
+#pragma unroll
+                        for (int term = 0; term < NT; ++term) {   // sum the accumulators and the term columns
+                            uint32_t part[16];
+                            ptx::tmem_ld_32x32b_x16(dt + (uint32_t)(a * NP + term * NMAX + c0), part);
+                            ptx::tmem_wait_ld();
+#pragma unroll
+                            for (int q = 0; q < 16; ++q)
+                                raw[q] = __float_as_uint(__uint_as_float(raw[q]) + __uint_as_float(part[q]));
+                        }
                 }
                 if (MODE == 0) {
-                    // lane i < 16: gate of feature f; lane i + 16: up of the same f.
+                    // lane i < 16: gate of feature f; lane i + 16: up of the same f. Lane i ends with
+                    // h[f] for tokens c0 .. c0+7, lane i + 16 for tokens c0+8 .. c0+15.
                     const bool is_gate = lane < 16;
                     const int f = tl.mb * 64 + warp * 16 + (lane & 15);
                     const float L = p.swiglu_limit;
+                    float h[8], am[8];
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
                         const float send = __uint_as_float(is_gate ? raw[8 + j] : raw[j]);
@@ -456,14 +506,39 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_kernel(const __grid_co
                             gt = fminf(gt, L);
                             up = fminf(fmaxf(up, -L), L);
                         }
-                        const float h = silu_f(gt) * up;
-                        const __nv_bfloat16 hh = __float2bfloat16_rn(h);
-                        const __nv_bfloat16 hl = __float2bfloat16_rn(h - __bfloat162float(hh));
-                        const int64_t r = (int64_t)tl.row0 + c0 + (is_gate ? j : 8 + j);
-                        p.h_hi[r * p.I + f] = hh;
-                        p.h_lo[r * p.I + f] = hl;
+                        h[j] = silu_f(gt) * up;
+                        am[j] = fabsf(h[j]);
                     }
-                } else {
+                    // W2 scale blocks are 32 consecutive features: 16 in this half-warp, 16 in the
+                    // partner warp (warps 0+1 and 2+3), which trade maxima through shared memory
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+#pragma unroll
+                        for (int o = 1; o < 16; o <<= 1) am[j] = fmaxf(am[j], __shfl_xor_sync(0xFFFFFFFFu, am[j], o));
+                    float *pm = pairmax + (chunk & 1) * 64;
+                    if ((lane & 15) == 0)
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) pm[warp * 16 + (lane >> 4) * 8 + j] = am[j];
+                    ptx::bar_sync_n(1 + (warp >> 1), 64);
+                    if (ok) {
+                        const int blk = f >> 5;                      // W2 K-block of this feature
+                        const bool writes_scale = (lane & 15) == 0 && (warp & 1) == 0;
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            const int e1 = mxfp8_block_exp(fmaxf(am[j], pm[(warp ^ 1) * 16 + (lane >> 4) * 8 + j]));
+                            const int64_t row = (int64_t)tl.row0 + c0 + (lane >> 4) * 8 + j;
+                            float r = h[j];
+#pragma unroll
+                            for (int term = 0; term < NT_H; ++term) {
+                                uint32_t sb;
+                                const uint32_t q = mxfp8_term1(r, e1, term, sb);
+                                p.hq[((int64_t)term * p.rows_cap + row) * p.I + f] = (uint8_t)q;
+                                if (writes_scale)
+                                    p.hs[((int64_t)term * p.rows_cap + row) * (p.I / 32) + blk] = (uint8_t)sb;
+                            }
+                        }
+                    }
+                } else if (ok) {
                     const int c = tl.mb * TILE_ROWS + warp * 32 + lane;
                     const int my_pair = (lane < 16) ? __ldg(p.row_to_pair + tl.row0 + c0 + lane) : -1;
 #pragma unroll
@@ -478,7 +553,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_kernel(const __grid_co
             }
             ptx::tc_fence_before();
             __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(&d_empty[di]);
+            if (ok && lane == 0) ptx::mbar_arrive(&d_empty[di]);
             if (++di == 2) { di = 0; dph ^= 1u; }
         }
         if (!ok && lane == 0) fail();
@@ -487,26 +562,59 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_kernel(const __grid_co
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
-    if (warp == 5) ptx::tmem_dealloc(tmem, TMEM_COLS);
+    if (warp == 8) ptx::tmem_dealloc(tmem, TMEM_COLS);
 }
 
-// Gathered activations: row r of the permutation gets x[token(r)], padding
-// rows (row_to_pair == -1) get zeros. Rows past padded[E] are not touched.
-__global__ void gather_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ row_to_pair,
-                              const int32_t *__restrict__ padded, int E, int H, int k, int64_t P,
-                              uint16_t *__restrict__ xp, int32_t *dev_error)
+// Gathered activations as NT_X MXFP8 terms: row r of the permutation gets
+// the terms of x[token(r)], padding rows (row_to_pair == -1) get zeros. One
+// thread per (row, 32-element block). Rows past padded[E] are not touched.
+__global__ void gather_quant_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ row_to_pair,
+                                    const int32_t *__restrict__ padded, int E, int H, int k, int64_t P,
+                                    int64_t rows_cap, uint8_t *__restrict__ xq, uint8_t *__restrict__ xs,
+                                    int32_t *dev_error)
 {
     const int64_t R = __ldg(padded + E);
-    const int vec = H / 8;
-    for (int64_t r = blockIdx.x; r < R; r += gridDim.x) {
+    const int nblk = H / 32;
+    const int64_t n = R * nblk;
+    for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < n; idx += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t r = idx / nblk;
+        const int b = (int)(idx - r * nblk);
         const int32_t pr = __ldg(row_to_pair + r);
-        uint4 *dst = reinterpret_cast<uint4 *>(xp + r * H);
+        float v[32];
         if (pr >= 0 && pr < P) {
-            const uint4 *src = reinterpret_cast<const uint4 *>(x + (int64_t)(pr / k) * H);
-            for (int v = threadIdx.x; v < vec; v += blockDim.x) dst[v] = __ldg(src + v);
+            const uint4 *src = reinterpret_cast<const uint4 *>(x + (int64_t)(pr / k) * H + b * 32);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const uint4 u = __ldg(src + q);
+                const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                for (int z = 0; z < 4; ++z) {
+                    v[q * 8 + 2 * z] = __uint_as_float(w[z] << 16);
+                    v[q * 8 + 2 * z + 1] = __uint_as_float(w[z] & 0xFFFF0000u);
+                }
+            }
         } else {
-            if (pr >= P && threadIdx.x == 0) record_error(dev_error, DEV_ERR_ID_RANGE);
-            for (int v = threadIdx.x; v < vec; v += blockDim.x) dst[v] = make_uint4(0, 0, 0, 0);
+            if (pr >= P && b == 0) record_error(dev_error, DEV_ERR_ID_RANGE);
+#pragma unroll
+            for (int q = 0; q < 32; ++q) v[q] = 0.f;
+        }
+        float mx = 0.f;
+#pragma unroll
+        for (int q = 0; q < 32; ++q) mx = fmaxf(mx, fabsf(v[q]));
+        const int e1 = mxfp8_block_exp(mx);
+#pragma unroll
+        for (int t = 0; t < NT_X; ++t) {
+            uint32_t wq[8], sbyte = 0;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const uint32_t lo = mxfp8_term_pair(v[4 * q], v[4 * q + 1], e1, t, sbyte);
+                const uint32_t hi = mxfp8_term_pair(v[4 * q + 2], v[4 * q + 3], e1, t, sbyte);
+                wq[q] = lo | (hi << 16);
+            }
+            uint4 *dst = reinterpret_cast<uint4 *>(xq + ((int64_t)t * rows_cap + r) * H + b * 32);
+            dst[0] = make_uint4(wq[0], wq[1], wq[2], wq[3]);
+            dst[1] = make_uint4(wq[4], wq[5], wq[6], wq[7]);
+            xs[((int64_t)t * rows_cap + r) * nblk + b] = (uint8_t)sbyte;
         }
     }
 }
@@ -550,9 +658,7 @@ cudaError_t launch_gemm(const GemmParams &p, int grid, cudaStream_t s)
     return cudaGetLastError();
 }
 
-// Tile shape by the average rows per expert (T*k/E): decode batches get
-// small tiles with deep pipelines, prefill batches large tiles.
-enum class Regime { Tiny, Small, Mid, Large };
+}  // namespace
 
 Regime pick_regime(int T, int k, int E)
 {
@@ -563,7 +669,17 @@ Regime pick_regime(int T, int k, int E)
     return Regime::Large;
 }
 
-}  // namespace
+int regime_nmax(Regime rg, int which)
+{
+    switch (rg) {
+    case Regime::Tiny: return 16;
+    case Regime::Small: return 32;
+    case Regime::Mid: return 64;
+    default: return which == 0 ? 96 : 64;
+    }
+}
+
+int regime_sps(Regime rg) { return (rg == Regime::Tiny || rg == Regime::Small) ? 2 : 1; }
 
 static void mark(const ForwardArgs &a, int i, cudaStream_t s)
 {
@@ -576,8 +692,12 @@ cudaError_t launch_forward(const ForwardArgs &a, cudaStream_t s)
     cudaError_t err;
     mark(a, 0, s);
     {
-        int grid = (int)(a.rows_cap < 8192 ? a.rows_cap : 8192);
-        gather_kernel<<<grid, 128, 0, s>>>(a.x, a.row_to_pair, a.padded, a.E, a.H, a.k, P, a.xp, a.dev_error);
+        const int64_t n = a.rows_cap * (a.H / 32);
+        int grid = (int)((n + 255) / 256);
+        if (grid > 8 * 1024) grid = 8 * 1024;
+        if (grid < 1) grid = 1;
+        gather_quant_kernel<<<grid, 256, 0, s>>>(a.x, a.row_to_pair, a.padded, a.E, a.H, a.k, P, a.rows_cap, a.xq,
+                                                 a.xs, a.dev_error);
         if ((err = cudaGetLastError()) != cudaSuccess) return err;
     }
     mark(a, 1, s);
@@ -591,18 +711,21 @@ cudaError_t launch_forward(const ForwardArgs &a, cudaStream_t s)
     g.k = a.k;
     g.swiglu_limit = a.swiglu_limit;
     g.P = P;
-    g.h_hi = reinterpret_cast<__nv_bfloat16 *>(a.h_hi);
-    g.h_lo = reinterpret_cast<__nv_bfloat16 *>(a.h_lo);
+    g.rows_cap = a.rows_cap;
+    g.hq = a.hq;
+    g.hs = a.hs;
     g.staging = a.staging;
     g.dev_error = a.dev_error;
 
     // W13: K = H, 64 features (128 rows) per weight tile
-    g.tm_b0 = *a.tmap_xp;
-    g.tm_b1 = *a.tmap_xp;
-    g.wpack = a.packed;
+    g.tm_a = *a.tmap_w13;
+    g.tm_a1 = *a.tmap_w13_1;
+    g.tm_b = *a.tmap_xq;
+    g.wsf = a.packed + (size_t)a.E * 2 * a.I * (a.H / 2);
+    g.bsf = a.xs;
     g.K = a.H;
     g.MB = a.I / 64;
-    const Regime rg = pick_regime(a.T, a.k, a.E);
+    const Regime rg = a.regime;
     err = rg == Regime::Tiny  ? launch_gemm<W13Tiny>(g, a.num_sms, s)
         : rg == Regime::Small ? launch_gemm<W13Small>(g, a.num_sms, s)
         : rg == Regime::Mid   ? launch_gemm<W13Mid>(g, a.num_sms, s)
@@ -611,9 +734,11 @@ cudaError_t launch_forward(const ForwardArgs &a, cudaStream_t s)
     mark(a, 2, s);
 
     // W2: K = I, 128 output features per weight tile
-    g.tm_b0 = *a.tmap_hhi;
-    g.tm_b1 = *a.tmap_hlo;
-    g.wpack = a.packed + packed_w13_bytes(a.E, a.H, a.I);
+    g.tm_a = *a.tmap_w2;
+    g.tm_a1 = *a.tmap_w2_1;
+    g.tm_b = *a.tmap_hq;
+    g.wsf = a.packed + packed_w13_bytes(a.E, a.H, a.I) + (size_t)a.E * a.H * (a.I / 2);
+    g.bsf = a.hs;
     g.K = a.I;
     g.MB = a.H / TILE_ROWS;
     err = rg == Regime::Tiny  ? launch_gemm<W2Tiny>(g, a.num_sms, s)

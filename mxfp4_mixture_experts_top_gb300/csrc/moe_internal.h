@@ -12,6 +12,18 @@ namespace moe {
 constexpr int DEV_ERR_ID_RANGE = 6;   // MOE_ERR_DEVICE
 constexpr int DEV_ERR_TIMEOUT = 7;    // MOE_ERR_TIMEOUT
 
+// Activations enter the block-scaled GEMMs as sums of MXFP8 terms (mxfp8_terms.cuh):
+// x (bf16) in NT_X terms, h (fp32 SiLU(gate)*up) in NT_H terms.
+constexpr int NT_X = 2;
+constexpr int NT_H = 3;
+
+// GEMM tile shapes by the average rows per expert (T*k/E): decode batches get
+// small tiles with deep pipelines, prefill batches large tiles.
+enum class Regime { Tiny, Small, Mid, Large };
+Regime pick_regime(int T, int k, int E);
+int regime_nmax(Regime rg, int which);   // token rows per tile; which 0: W13, 1: W2
+int regime_sps(Regime rg);               // K-slabs per weight stage
+
 // Bounded pipeline waits give up after this much wall time.
 constexpr unsigned long long WAIT_LIMIT_NS = 2000000000ull;   // 2 s
 
@@ -44,9 +56,12 @@ struct ForwardArgs {
     const int32_t *offsets, *padded, *row_to_pair;
     float *y;
     int32_t *dev_error;
-    uint16_t *xp, *h_hi, *h_lo;
+    uint8_t *xq, *xs;      // x terms [NT_X][rows_cap][H], their scales [NT_X][rows_cap][H/32]
+    uint8_t *hq, *hs;      // h terms [NT_H][rows_cap][I], their scales [NT_H][rows_cap][I/32]
     float *staging;
-    const CUtensorMap *tmap_xp, *tmap_hhi, *tmap_hlo;
+    const CUtensorMap *tmap_w13, *tmap_w13_1, *tmap_w2, *tmap_w2_1;   // weight nibbles: stage / single-slab boxes
+    const CUtensorMap *tmap_xq, *tmap_hq;                            // activation terms
+    Regime regime;
     int num_sms;
     void *const *events;   // optional: 5 cudaEvent_t recorded between kernels
 };

@@ -51,10 +51,10 @@ extern "C" moe_status_t moe_mxfp4_forward_noalloc(const moe_layer_desc *desc, co
                                                   const int32_t *d_offsets, const int32_t *d_padded_offsets,
                                                   const int32_t *d_row_to_pair, float *d_y, void *stream)
 {
-    size_t layout[6];
+    size_t layout[7];
     const moe_status_t valid = moe_mxfp4_workspace_layout(desc, layout);   // same checks as the forward
     if (valid != MOE_OK) return valid;
-    if (layout[5] > (size_t)MOE_NOALLOC_SCRATCH_BYTES) return MOE_ERR_WORKSPACE;   // layer too large for the array
+    if (layout[6] > (size_t)MOE_NOALLOC_SCRATCH_BYTES) return MOE_ERR_WORKSPACE;   // layer too large for the array
     void *scratch = nullptr;
     const moe_status_t st = scratch_on_current_device(&scratch);
     if (st != MOE_OK) return st;

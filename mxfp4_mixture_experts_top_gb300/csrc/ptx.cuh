@@ -64,6 +64,19 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t by
                  ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
 }
 
+// Raise the transaction count of the current phase without arriving (a later
+// arrive.expect_tx of the same phase carries the arrival).
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+
+// Named barrier `id` over `nthreads` threads (whole warps).
+__device__ __forceinline__ void bar_sync_n(uint32_t id, uint32_t nthreads)
+{
+    asm volatile("barrier.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
 {
     uint32_t ok;
@@ -130,6 +143,17 @@ __device__ __forceinline__ void tma_load_2d(void *smem_dst, const void *tmap, in
         : "memory");
 }
 
+// 3-D tiled tensor load at element coords (x, y, z).
+__device__ __forceinline__ void tma_load_3d(void *smem_dst, const void *tmap, int32_t x, int32_t y, int32_t z,
+                                            uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];"
+        ::"r"(smem_u32(smem_dst)), "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+        : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tmap(const void *tmap)
 {
     asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
@@ -176,6 +200,19 @@ __device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
         : "memory");
 }
 
+// D(tmem) (+)= (A(smem) x 2^sfA) * (B(smem) x 2^sfB), kind::mxf8f6f4 with block scaling: one E8M0
+// scale per 32 K-elements of every A row and B row, read from tensor memory (K = 32 per MMA).
+__device__ __forceinline__ void mma_mx_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                          uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.u32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
+        ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
 // Arrive on `bar` once all previously issued tcgen05 async ops of this thread complete.
 __device__ __forceinline__ void mma_commit(uint64_t *bar)
 {
@@ -196,6 +233,23 @@ __device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const uint32_
         "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]),
         "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
         : "memory");
+}
+
+// Store 1, 2 or 4 consecutive 32-bit columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_st_32x32b_x1(uint32_t taddr, uint32_t a)
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(a) : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_32x32b_x2(uint32_t taddr, uint32_t a, uint32_t b)
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x2.b32 [%0], {%1, %2};" ::"r"(taddr), "r"(a), "r"(b) : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_32x32b_x4(uint32_t taddr, uint32_t a, uint32_t b, uint32_t c, uint32_t d)
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};"
+                 ::"r"(taddr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
 // Store 16 consecutive 32-bit columns of this thread's TMEM lane.
@@ -254,6 +308,20 @@ __host__ __device__ __forceinline__ uint32_t idesc_bf16_f32(uint32_t M, uint32_t
          | (1u << 10)             // B format bf16
          | ((N >> 3) << 17)       // N / 8
          | ((M >> 4) << 24);      // M / 16
+}
+
+// Instruction descriptor for kind::mxf8f6f4 with block scaling: A = E2M1, B = E4M3, D = f32, both
+// K-major, M x N, scale-factor type UE8M0 (bit 23), and the byte (0..3) of each 32-bit scale cell that
+// holds this MMA's K-block, for B (bits 4-5) and A (bits 29-30).
+__host__ __device__ __forceinline__ uint32_t idesc_mx_e2m1_e4m3(uint32_t M, uint32_t N, uint32_t sf_byte)
+{
+    return (sf_byte << 4)         // B scale-factor byte
+         | (5u << 7)              // A format E2M1
+         | (0u << 10)             // B format E4M3
+         | ((N >> 3) << 17)       // N / 8
+         | (1u << 23)             // scale factors are UE8M0
+         | ((M >> 4) << 24)       // M / 16
+         | (sf_byte << 29);       // A scale-factor byte
 }
 
 }  // namespace ptx

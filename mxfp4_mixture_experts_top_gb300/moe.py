@@ -66,7 +66,7 @@ def load(path: str = LIB_PATH):
             "moe_mxfp4_workspace_bytes": ([D], sz),
             "moe_mxfp4_forward": ([D, P, P, P, P, P, P, P, P, sz, P], i32),
             "moe_mxfp4_forward_timed": ([D, P, P, P, P, P, P, P, P, sz, P, P], i32),
-            "moe_mxfp4_workspace_layout": ([D, ctypes.POINTER(ctypes.c_size_t * 6)], i32),
+            "moe_mxfp4_workspace_layout": ([D, ctypes.POINTER(ctypes.c_size_t * 7)], i32),
             "moe_read_device_error": ([P, ctypes.POINTER(ctypes.c_int), P], i32),
             "moe_launch_count": ([], ctypes.c_uint64),
             "moe_mxfp4_forward_noalloc": ([D, P, P, P, P, P, P, P, P], i32),
@@ -165,9 +165,9 @@ def workspace_bytes(desc: LayerDesc) -> int:
 
 
 def workspace_layout(desc: LayerDesc):
-    arr = (ctypes.c_size_t * 6)()
+    arr = (ctypes.c_size_t * 7)()
     _check(load().moe_mxfp4_workspace_layout(ctypes.byref(desc), ctypes.byref(arr)), "moe_mxfp4_workspace_layout")
-    return dict(error=arr[0], xp=arr[1], h_hi=arr[2], h_lo=arr[3], staging=arr[4], total=arr[5])
+    return dict(error=arr[0], xq=arr[1], xs=arr[2], hq=arr[3], hs=arr[4], staging=arr[5], total=arr[6])
 
 
 def prepack(desc: LayerDesc, w13_q, w13_s, w2_q, w2_s, stream=None) -> torch.Tensor:

@@ -35,7 +35,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert moe.abi_version() == 1
+    assert moe.abi_version() == 2
     for s in range(8):
         assert lib.moe_status_string(s)
     assert b"unknown" in lib.moe_status_string(99)
@@ -55,8 +55,11 @@ def test_packed_and_workspace_sizes():
                                          + 4096 * 2048 // 2 + 4096 * 2048 // 32)
     lay = moe.workspace_layout(d)
     R = moe.rows_capacity(8, 256, 6, 16)
-    assert lay["xp"] >= 256 and lay["h_hi"] >= lay["xp"] + R * 4096 * 2
-    assert lay["staging"] >= lay["h_lo"] + R * 2048 * 2
+    # x as 2 MXFP8 terms, SiLU(gate)*up as 3 terms, each with one scale byte per 32 elements
+    assert lay["xq"] >= 256 and lay["xs"] >= lay["xq"] + 2 * R * 4096
+    assert lay["hq"] >= lay["xs"] + 2 * R * 4096 // 32
+    assert lay["hs"] >= lay["hq"] + 3 * R * 2048
+    assert lay["staging"] >= lay["hs"] + 3 * R * 2048 // 32
     assert lay["total"] >= lay["staging"] + 48 * 4096 * 4
     assert moe.workspace_bytes(d) == lay["total"]
     assert all(v % 256 == 0 for v in lay.values())
@@ -74,7 +77,7 @@ def test_packed_and_workspace_sizes():
 ])
 def test_desc_validation(lib, T, H, I, E, k, bm, code):
     d = moe.make_desc(T, H, I, E, k, bm)
-    arr = (ctypes.c_size_t * 6)()
+    arr = (ctypes.c_size_t * 7)()
     assert lib.moe_mxfp4_workspace_layout(ctypes.byref(d), ctypes.byref(arr)) == code
 
 

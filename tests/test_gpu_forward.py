@@ -107,24 +107,48 @@ def test_forward_tiny_all_outputs(gpu_lib, gpu_layers, block_m):
     _compare(f"tiny bm{block_m}", r["y"].cpu().numpy(), oracle.forward(L, ids_r, w_r))
 
 
+def _e4m3_values():
+    """All 256 E4M3 codes (OCP FP8: bias 7, 3 mantissa bits, subnormals; S.1111.111 is NaN)."""
+    c = np.arange(256)
+    s, e, m = c >> 7, (c >> 3) & 15, c & 7
+    v = np.where(e == 0, np.ldexp(m / 8.0, -6), np.ldexp(1 + m / 8.0, e - 7))
+    v = np.where(s == 1, -v, v)
+    v[(c & 0x7F) == 0x7F] = np.nan
+    return v
+
+
+def _terms(ws, off_q, off_s, nt, R, K):
+    """Sum of the MXFP8 terms stored at (off_q, off_s): value[row, k]."""
+    q = ws[off_q:off_q + nt * R * K].cpu().numpy().reshape(nt, R, K)
+    sc = ws[off_s:off_s + nt * R * (K // 32)].cpu().numpy().reshape(nt, R, K // 32).astype(int)
+    v = _e4m3_values()[q] * np.ldexp(1.0, np.repeat(sc, 32, axis=2) - 127)
+    return v.sum(0)
+
+
 def test_forward_tiny_intermediates(gpu_lib, gpu_layers):
-    """Diagnostic: the W13 epilogue's SiLU product (hi + lo) against float64."""
+    """Diagnostic: the activation terms of both GEMMs against float64. The x
+    terms reproduce every bf16 input (2 terms: 4 + 4 significant bits); the h
+    terms keep SiLU(gate)*up to about 12 bits (3 terms)."""
     moe = gpu_lib
     L = synth.make_config("tiny_t37_h512_e32")
     r = _run_layer(moe, gpu_layers, L, 16)
     lay = moe.workspace_layout(r["desc"])
-    R = int(r["perm"]["padded_offsets"][-1].item())
+    R = moe.rows_capacity(L["T"], L["E"], L["k"], 16)
+    Rv = int(r["perm"]["padded_offsets"][-1].item())
     I, H, k = L["I"], L["H"], L["k"]
     ws = r["ws"]
-    hh = ws[lay["h_hi"]:lay["h_hi"] + R * I * 2].view(torch.bfloat16).float().view(R, I)
-    hl = ws[lay["h_lo"]:lay["h_lo"] + R * I * 2].view(torch.bfloat16).float().view(R, I)
-    h_gpu = (hh.double() + hl.double()).cpu().numpy()
-    r2p = r["perm"]["row_to_pair"].cpu().numpy()[:R]
+    x = synth.bf16_bits_to_f64(L["x_bits"])
+    r2p = r["perm"]["row_to_pair"].cpu().numpy()[:Rv]
+    xg = _terms(ws, lay["xq"], lay["xs"], 2, R, H)[:Rv]
+    want = np.where(r2p[:, None] >= 0, x[np.maximum(r2p, 0) // k], 0.0)
+    # exact unless a 32-element block spans more than E4M3's range (then the smallest values keep
+    # fewer bits): measured on these inputs about 2 in 10^4 elements, each off by < 1e-6 * max|x|
+    assert np.mean(xg == want) > 0.999 and np.abs(xg - want).max() <= 1e-6 * np.abs(x).max()
+    h_gpu = _terms(ws, lay["hq"], lay["hs"], 3, R, I)[:Rv]
     ids = r["ids"].cpu().numpy()
     e2m1 = np.array([oracle.e2m1_value(c) for c in range(16)])
-    x = synth.bf16_bits_to_f64(L["x_bits"])
     worst = 0.0
-    for row in range(R):
+    for row in range(Rv):
         p = r2p[row]
         if p < 0:
             assert np.all(h_gpu[row] == 0), f"padding row {row} not zero"
@@ -135,8 +159,8 @@ def test_forward_tiny_intermediates(gpu_lib, gpu_layers):
         gu = W @ x[t]
         h = gu[:I] / (1 + np.exp(-gu[:I])) * gu[I:]
         worst = max(worst, np.abs(h_gpu[row] - h).max() / np.sqrt(np.mean(h ** 2)))
-    print(f"[tiny h] max|h_gpu-h|/rms(h) = {worst:.3e}")
-    assert worst < 1e-4
+    print(f"[tiny h] max|h_terms-h|/rms(h) = {worst:.3e}")
+    assert worst < 3e-3
 
 
 def test_forward_decode_t8_all_outputs(gpu_lib, gpu_layers):
