@@ -62,7 +62,8 @@ std::map<MapKey, MapEntry> g_maps;
 // Cached tensor map. kind 0: prepacked weight nibbles, a 2-D tensor of d1 rows of 128 E2M1 values
 // (64 B) read as "16 x U4, 16-byte aligned" (each 8-byte group lands in 16 bytes of shared memory),
 // box 128 x b1 rows. kind 1: activation terms, a 3-D uint8 tensor [d2 terms][d1 rows][d0 K], box
-// 128 x b1 x d2. Both with the 128-byte swizzle of the MMA operands.
+// 128 x b1 x d2. Both with the 128-byte swizzle of the MMA operands. kind 2: activation scale
+// words, a 3-D uint32 tensor [slabs][d1 terms][d0 rows], box b1 rows x d1 terms x 1, no swizzle.
 const CUtensorMap *get_map(int kind, const void *ptr, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t b1,
                            moe_status_t *st)
 {
@@ -85,12 +86,19 @@ const CUtensorMap *get_map(int kind, const void *ptr, uint64_t d0, uint64_t d1, 
         r = fn(&ent.map, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 2, const_cast<void *>(ptr), dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    } else {
+    } else if (kind == 1) {
         cuuint64_t dims[3] = {d0, d1, d2};
         cuuint64_t strides[2] = {d0, d0 * d1};
         cuuint32_t box[3] = {128, b1, (cuuint32_t)d2};
         r = fn(&ent.map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(ptr), dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    } else {
+        cuuint64_t dims[3] = {d0, d1, d2};
+        cuuint64_t strides[2] = {d0 * 4, d0 * d1 * 4};
+        cuuint32_t box[3] = {b1, (cuuint32_t)d1, 1};
+        r = fn(&ent.map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<void *>(ptr), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     }
     if (r != CUDA_SUCCESS) { *st = MOE_ERR_CUDA; return nullptr; }
@@ -128,17 +136,25 @@ struct Layout {
     size_t err, xq, xs, hq, hs, staging, total;
 };
 
+// Rows of the activation scale-word arrays: the permutation rows rounded up to 4 (TMA strides are
+// multiples of 16 bytes).
+int64_t scale_rows(const moe_layer_desc *d)
+{
+    return (moe_permute_rows_capacity(d->T, d->E, d->k, d->block_m) + 3) / 4 * 4;
+}
+
 Layout workspace_layout(const moe_layer_desc *d)
 {
     const int64_t P = (int64_t)d->T * d->k;
     const int64_t R = moe_permute_rows_capacity(d->T, d->E, d->k, d->block_m);
+    const int64_t RS = scale_rows(d);
     Layout L;
     L.err = 0;
     L.xq = 1024;
     L.xs = align_up(L.xq + (size_t)NT_X * R * d->H, 1024);
-    L.hq = align_up(L.xs + (size_t)NT_X * R * (d->H / 32), 1024);
+    L.hq = align_up(L.xs + (size_t)NT_X * RS * (d->H / 32), 1024);
     L.hs = align_up(L.hq + (size_t)NT_H * R * d->I, 1024);
-    L.staging = align_up(L.hs + (size_t)NT_H * R * (d->I / 32), 1024);
+    L.staging = align_up(L.hs + (size_t)NT_H * RS * (d->I / 32), 1024);
     L.total = align_up(L.staging + (size_t)P * d->H * 4, 1024);
     return L;
 }
@@ -291,6 +307,7 @@ moe_status_t moe_mxfp4_forward_timed(const moe_layer_desc *d, const uint16_t *d_
     a.block_m = d->block_m;
     a.swiglu_limit = d->swiglu_limit;
     a.rows_cap = R;
+    a.rows_sf = scale_rows(d);
     a.x = d_x;
     a.packed = static_cast<const uint8_t *>(d_packed);
     a.topk_w = d_topk_w;
@@ -318,6 +335,12 @@ moe_status_t moe_mxfp4_forward_timed(const moe_layer_desc *d, const uint16_t *d_
     if (!(a.tmap_xq = get_map(1, a.xq, (uint64_t)d->H, (uint64_t)R, NT_X, (uint32_t)regime_nmax(a.regime, 0), &st)))
         return st;
     if (!(a.tmap_hq = get_map(1, a.hq, (uint64_t)d->I, (uint64_t)R, NT_H, (uint32_t)regime_nmax(a.regime, 1), &st)))
+        return st;
+    if (!(a.tmap_xs = get_map(2, a.xs, (uint64_t)a.rows_sf, NT_X, (uint64_t)(d->H / KSLAB),
+                              (uint32_t)regime_nmax(a.regime, 0), &st)))
+        return st;
+    if (!(a.tmap_hs = get_map(2, a.hs, (uint64_t)a.rows_sf, NT_H, (uint64_t)(d->I / KSLAB),
+                              (uint32_t)regime_nmax(a.regime, 1), &st)))
         return st;
     if (cudaMemsetAsync(a.dev_error, 0, sizeof(int32_t), s) != cudaSuccess) return MOE_ERR_CUDA;
     return from_cuda(launch_forward(a, s));

@@ -52,55 +52,59 @@ constexpr int TMEM_COLS = 512;
 // Kernel configuration. MODE 0: W13 (x terms -> SiLU(gate)*up -> h terms),
 // MODE 1: W2 (h terms -> per-pair outputs). NMAX: most token rows per tile
 // (experts with more rows get several tiles). NT: activation terms. SPS:
-// K-slabs per ring stage (a stage is one producer step; its fixed cost is
-// paid once per SPS slabs). NA / NB: weight / activation ring stages. NSF:
-// scale-factor cells in TMEM. NACC: accumulators per tile (consecutive
-// 32-K blocks rotate over them, so short MMAs do not wait on each other).
+// K-slabs per ring stage. Every ring (weights, activations with their scales,
+// TMEM scale-factor cells) advances one stage per producer / copier / MMA
+// step, so each step's fixed cost (barrier waits and arrivals, copy issue: a
+// few hundred cycles) is paid once per SPS slabs. NA / NB: weight /
+// activation ring stages. NSF: TMEM scale-factor cells (one stage each).
+// NACC: accumulators per tile (consecutive 32-K blocks rotate over them, so
+// short MMAs do not wait on each other).
 template <int MODE_, int NMAX_, int NT_, int SPS_, int NA_, int NB_, int NSF_, int NACC_>
 struct Cfg {
     static constexpr int MODE = MODE_, NMAX = NMAX_, NT = NT_, SPS = SPS_, NA = NA_, NB = NB_, NSF = NSF_,
                          NACC = NACC_;
     static constexpr int NP = NT * NMAX;                       // MMA N: all terms of NMAX rows
     static constexpr int SFB_COLS = (NP + 31) / 32;            // B scale cells: row j in column j / 32
-    static constexpr int SF_COLS = (4 + SFB_COLS + 3) / 4 * 4; // one ring cell: A (4 columns), then B
+    static constexpr int SF_COLS = (4 + SFB_COLS + 3) / 4 * 4; // one slab's cells: A (4 columns), then B
+    static constexpr int CELL_COLS = SPS * SF_COLS;            // one stage
     static constexpr int D_COLS = NACC * NP;                   // one accumulator set
     static constexpr int SF_BASE = 2 * D_COLS;
     static constexpr int THREADS = 352;
     static_assert(NP % 16 == 0 && NP <= 256, "MMA N");
     static_assert(NMAX % 16 == 0, "token rows per tile");
-    static_assert(SF_BASE + NSF * SF_COLS <= TMEM_COLS, "TMEM budget");
+    static_assert(SF_BASE + NSF * CELL_COLS <= TMEM_COLS, "TMEM budget");
     static_assert(SPS == 1 || SPS == 2, "slabs per stage");
 };
 
 // decode, <= 2 rows per expert on average
-using W13Tiny = Cfg<0, 16, NT_X, 2, 5, 4, 8, 2>;
-using W2Tiny = Cfg<1, 16, NT_H, 2, 5, 3, 8, 2>;
+using W13Tiny = Cfg<0, 16, NT_X, 2, 5, 4, 6, 2>;
+using W2Tiny = Cfg<1, 16, NT_H, 2, 5, 3, 6, 2>;
 // decode batches: <= 16 rows per expert
-using W13Small = Cfg<0, 32, NT_X, 2, 4, 4, 8, 2>;
-using W2Small = Cfg<1, 32, NT_H, 2, 4, 3, 8, 2>;
+using W13Small = Cfg<0, 32, NT_X, 2, 4, 4, 6, 2>;
+using W2Small = Cfg<1, 32, NT_H, 2, 4, 3, 4, 2>;
 // <= 64 rows per expert
-using W13Mid = Cfg<0, 64, NT_X, 1, 6, 5, 8, 1>;
-using W2Mid = Cfg<1, 64, NT_H, 1, 5, 5, 8, 1>;
+using W13Mid = Cfg<0, 64, NT_X, 2, 3, 3, 6, 1>;
+using W2Mid = Cfg<1, 64, NT_H, 2, 3, 2, 4, 1>;
 // prefill
-using W13Large = Cfg<0, 96, NT_X, 1, 5, 5, 8, 1>;
-using W2Large = Cfg<1, 64, NT_H, 1, 5, 5, 8, 1>;
+using W13Large = Cfg<0, 96, NT_X, 2, 3, 2, 4, 1>;
+using W2Large = Cfg<1, 64, NT_H, 2, 3, 2, 4, 1>;
 static_assert(W13Large::NMAX == 96 && W2Large::NMAX == 64, "regime_nmax() mirrors these");
 
 struct GemmParams {
     CUtensorMap tm_a;         // weight nibbles, box 128 x (128 * SPS) rows
     CUtensorMap tm_a1;        // weight nibbles, box 128 x 128 rows (a stage that straddles two tiles)
     CUtensorMap tm_b;         // activation terms [NT][rows][K] bytes, box 128 x NMAX x NT
+    CUtensorMap tm_bs;        // activation scale words [K/128][NT][rows_sf] (uint32), box NMAX x NT x 1
     const uint8_t *wsf;       // this matrix's prepacked scale region
-    const uint8_t *bsf;       // activation term scales [NT][rows_cap][K/32]
     const int32_t *offsets;   // [E+1]
     const int32_t *padded;    // [E+1]
     const int32_t *row_to_pair;
     int E, K, MB;             // MB: 128-row weight tiles per expert
     int I, H, k;
     float swiglu_limit;
-    int64_t P, rows_cap;
+    int64_t P, rows_cap, rows_sf;
     uint8_t *hq;              // W13 out: h terms [NT_H][rows_cap][I]
-    uint8_t *hs;              // W13 out: h term scales [NT_H][rows_cap][I/32]
+    uint8_t *hs;              // W13 out: h term scale words [I/128][NT_H][rows_sf], byte = K-block % 4
     float *staging;           // W2 out [P, H]
     int32_t *dev_error;
 };
@@ -110,11 +114,15 @@ struct Smem {
     static constexpr int ASTAGE = C::SPS * SLAB_SMEM_BYTES;    // expanded E2M1 slabs
     static constexpr int BSLAB = C::NP * 128;                 // [term][row][128 K bytes]
     static constexpr int BSTAGE = C::SPS * BSLAB;
+    static constexpr int BSBYTES = C::NP * 4;                 // B scale words [term][row] of one slab
+    static constexpr int BSSLAB = (BSBYTES + 127) / 128 * 128; // TMA destinations stay 128-byte aligned
+    static constexpr int BSSTAGE = C::SPS * BSSLAB;
     static constexpr int SFSTAGE = C::SPS * SLAB_SF_BYTES;
     static constexpr int A_OFF = 0;
     static constexpr int B_OFF = A_OFF + C::NA * ASTAGE;
     static constexpr int SF_OFF = B_OFF + C::NB * BSTAGE;
-    static constexpr int BAR_OFF = SF_OFF + C::NA * SFSTAGE;
+    static constexpr int BS_OFF = SF_OFF + C::NA * SFSTAGE;
+    static constexpr int BAR_OFF = BS_OFF + C::NB * BSSTAGE;
     static constexpr int NBARS = 2 * C::NA + 2 * C::NB + 2 * C::NSF + 2 * 2 + 1;
     static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;
     static constexpr int PAIRMAX_OFF = MISC_OFF + 16;         // W13 epilogue: [2 buffers][4 warps][16] floats
@@ -169,6 +177,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_kernel(const __grid_co
     uint8_t *aring = smem + S::A_OFF;
     uint8_t *bring = smem + S::B_OFF;
     uint8_t *sfring = smem + S::SF_OFF;
+    uint8_t *bsring = smem + S::BS_OFF;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + S::BAR_OFF);
     uint64_t *a_full = bars, *a_empty = a_full + C::NA;
     uint64_t *b_full = a_empty + C::NA, *b_empty = b_full + C::NB;
@@ -321,136 +330,129 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_kernel(const __grid_co
             __all_sync(0xFFFFFFFFu, ptx::mbar_wait(&a_full[n % C::NA], (uint32_t)((n / C::NA) & 1), &never, LIM));
         }
     } else if (warp == 9) {
-        // ===================== activation producer: per slab one 3-D TMA box (128 K x NMAX rows x NT
-        // terms); one arrival per stage of SPS slabs
-        if (ptx::elect_one()) ptx::prefetch_tmap(&p.tm_b);
+        // ===================== activation producer: per stage, for each of its slabs one 3-D TMA box
+        // of the term rows (128 K x NMAX rows x NT terms) and one of their scale words (NMAX x NT)
+        if (ptx::elect_one()) {
+            ptx::prefetch_tmap(&p.tm_b);
+            ptx::prefetch_tmap(&p.tm_bs);
+        }
         __syncwarp();
-        int bi = 0, pos = 0, i = 0;
+        int bi = 0;
         uint32_t bph = 0;
         long long issued = 0;
         bool ok = true;
-        constexpr uint32_t BBYTES = (uint32_t)(NP * 128);
-        for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-            const Tile tl = decode_tile<C>(t, tile_start, E, MB, p.offsets, p.padded);
-            for (int ka = 0; ka < slabs; ++ka, ++i) {
-                if (pos == 0) {
-                    if (!__all_sync(0xFFFFFFFFu, ptx::mbar_wait(&b_empty[bi], bph ^ 1u, s_abort, LIM))) { ok = false; break; }
-                }
-                const bool last = pos == SPS - 1 || i == n_slabs - 1;   // this slab closes the stage
+        int tcur = blockIdx.x, ka = 0;
+        Tile tl = decode_tile<C>(tcur, tile_start, E, MB, p.offsets, p.padded);
+        for (int i0 = 0; i0 < n_slabs; i0 += SPS) {
+            if (!__all_sync(0xFFFFFFFFu, ptx::mbar_wait(&b_empty[bi], bph ^ 1u, s_abort, LIM))) { ok = false; break; }
+            const int nsl = n_slabs - i0 < SPS ? n_slabs - i0 : SPS;
+            if (ptx::elect_one()) ptx::mbar_arrive_expect_tx(&b_full[bi], (uint32_t)(nsl * (S::BSLAB + S::BSBYTES)));
+            for (int pos = 0; pos < nsl; ++pos) {
                 if (ptx::elect_one()) {
-                    if (last) ptx::mbar_arrive_expect_tx(&b_full[bi], BBYTES);
-                    else ptx::mbar_expect_tx(&b_full[bi], BBYTES);
                     ptx::tma_load_3d(bring + bi * S::BSTAGE + pos * S::BSLAB, &p.tm_b, ka * KSLAB, tl.row0, 0, &b_full[bi]);
+                    ptx::tma_load_3d(bsring + bi * S::BSSTAGE + pos * S::BSSLAB, &p.tm_bs, tl.row0, 0, ka, &b_full[bi]);
                 }
                 __syncwarp();
-                if (last) {
-                    ++issued;
-                    pos = 0;
-                    if (++bi == C::NB) { bi = 0; bph ^= 1u; }
-                } else {
-                    ++pos;
+                if (++ka == slabs) {
+                    ka = 0;
+                    tcur += gridDim.x;
+                    if (tcur < total) tl = decode_tile<C>(tcur, tile_start, E, MB, p.offsets, p.padded);
                 }
             }
+            ++issued;
+            if (++bi == C::NB) { bi = 0; bph ^= 1u; }
         }
         if (!ok && lane == 0) fail();
         volatile int never = 0;
-        // a stage is left only after its closing arrival, so every issued stage can complete
         for (long long i2 = 1; i2 <= (issued < C::NB ? issued : C::NB); ++i2) {
             const long long n = issued - i2;
             __all_sync(0xFFFFFFFFu, ptx::mbar_wait(&b_full[n % C::NB], (uint32_t)((n / C::NB) & 1), &never, LIM));
         }
     } else if (warp >= 4 && warp < 8) {
-        // ===================== scale-factor copiers: per slab, A's cells from the weight stage and B's
-        // (one 32-bit cell per B row: its 4 K-block scales) from global memory, into the next ring
-        // cell of this warp's TMEM lane quarter; lane r of every quarter holds rows r, r + 32, ... in
-        // consecutive columns.
-        int i = 0, si = 0;
-        uint32_t sph = 0;
+        // ===================== scale-factor copiers: per stage, A's cells (weight stage) and B's cells
+        // (one 32-bit word per B row: its 4 K-block scales; activation stage) of each slab into the
+        // next TMEM cell, in this warp's lane quarter; lane r of every quarter holds rows r, r + 32,
+        // ... in consecutive columns.
+        int ai = 0, bi = 0, sc = 0;
+        uint32_t aph = 0, bph = 0, sph = 0;
         bool ok = true;
-        const int kq = p.K / 32;                     // scale bytes per activation row
-        for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-            const Tile tl = decode_tile<C>(t, tile_start, E, MB, p.offsets, p.padded);
-            for (int ka = 0; ka < slabs; ++ka, ++i) {
-                uint32_t bw[C::SFB_COLS];
-#pragma unroll
-                for (int c = 0; c < C::SFB_COLS; ++c) {
-                    const int j = lane + 32 * c;          // B row: term j / NMAX of token row j % NMAX
-                    const int64_t row = (int64_t)tl.row0 + (j % NMAX);
-                    bw[c] = (j < NP && row < p.rows_cap)
-                                ? __ldg(reinterpret_cast<const uint32_t *>(
-                                      p.bsf + ((int64_t)(j / NMAX) * p.rows_cap + row) * kq + ka * 4))
-                                : 0u;
-                }
-                const int st = i / SPS, ai = st % C::NA;
-                const uint32_t aph = (uint32_t)((st / C::NA) & 1);
-                if (!__all_sync(0xFFFFFFFFu, ptx::mbar_wait(&sf_empty[si], sph ^ 1u, s_abort, LIM) &&
-                                                 ptx::mbar_wait(&a_full[ai], aph, s_abort, LIM))) { ok = false; break; }
-                const uint4 aw = *reinterpret_cast<const uint4 *>(sfring + ai * S::SFSTAGE + (i % SPS) * SLAB_SF_BYTES +
-                                                                  lane * 16);
-                ptx::tc_fence_after();
-                const uint32_t cell = tmem + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)(C::SF_BASE + si * C::SF_COLS);
+        const uint32_t quarter = (uint32_t)((warp & 3) * 32) << 16;
+        for (int i0 = 0; i0 < n_slabs; i0 += SPS) {
+            const int nsl = n_slabs - i0 < SPS ? n_slabs - i0 : SPS;
+            if (!__all_sync(0xFFFFFFFFu, ptx::mbar_wait(&sf_empty[sc], sph ^ 1u, s_abort, LIM) &&
+                                             ptx::mbar_wait(&a_full[ai], aph, s_abort, LIM) &&
+                                             ptx::mbar_wait(&b_full[bi], bph, s_abort, LIM))) { ok = false; break; }
+            ptx::tc_fence_after();
+            for (int pos = 0; pos < nsl; ++pos) {
+                const uint4 aw = *reinterpret_cast<const uint4 *>(sfring + ai * S::SFSTAGE + pos * SLAB_SF_BYTES + lane * 16);
+                const uint32_t *bs = reinterpret_cast<const uint32_t *>(bsring + bi * S::BSSTAGE + pos * S::BSSLAB);
+                const uint32_t cell = tmem + quarter + (uint32_t)(C::SF_BASE + sc * C::CELL_COLS + pos * C::SF_COLS);
                 ptx::tmem_st_32x32b_x4(cell, aw.x, aw.y, aw.z, aw.w);
 #pragma unroll
-                for (int c = 0; c < C::SFB_COLS; ++c) ptx::tmem_st_32x32b_x1(cell + 4 + (uint32_t)c, bw[c]);
-                ptx::tmem_wait_st();
-                ptx::tc_fence_before();
-                __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(&sf_full[si]);
-                if (++si == C::NSF) { si = 0; sph ^= 1u; }
+                for (int c = 0; c < C::SFB_COLS; ++c) {
+                    const int j = lane + 32 * c;              // B row: term j / NMAX of token row j % NMAX
+                    ptx::tmem_st_32x32b_x1(cell + 4 + (uint32_t)c, j < NP ? bs[j] : 0u);
+                }
             }
+            ptx::tmem_wait_st();
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&sf_full[sc]);
+            if (++ai == C::NA) { ai = 0; aph ^= 1u; }
+            if (++bi == C::NB) { bi = 0; bph ^= 1u; }
+            if (++sc == C::NSF) { sc = 0; sph ^= 1u; }
         }
         if (!ok && lane == 0) fail();
     } else if (warp == 8) {
-        // ===================== MMA issuer: per slab four block-scaled MMAs (K = 32 each)
+        // ===================== MMA issuer: per stage, four block-scaled MMAs (K = 32 each) per slab
         const uint64_t adesc0 = ptx::smem_desc_sw128(ptx::smem_u32(aring));
         const uint64_t bdesc0 = ptx::smem_desc_sw128(ptx::smem_u32(bring));
-        int i = 0, si = 0, bi = 0, di = 0, pos = 0;
-        uint32_t sph = 0, bph = 0, dph = 0;
+        int ai = 0, bi = 0, sc = 0, di = 0, ka = 0;
+        uint32_t aph = 0, bph = 0, sph = 0, dph = 0;
         bool ok = true, issued = false;
-        for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-            if (!__all_sync(0xFFFFFFFFu, ptx::mbar_wait(&d_empty[di], dph ^ 1u, s_abort, LIM))) { ok = false; break; }
+        for (int i0 = 0; i0 < n_slabs && ok; i0 += SPS) {
+            const int nsl = n_slabs - i0 < SPS ? n_slabs - i0 : SPS;
+            if (!__all_sync(0xFFFFFFFFu, ptx::mbar_wait(&sf_full[sc], sph, s_abort, LIM) &&
+                                             ptx::mbar_wait(&a_full[ai], aph, s_abort, LIM) &&
+                                             ptx::mbar_wait(&b_full[bi], bph, s_abort, LIM))) { ok = false; break; }
             ptx::tc_fence_after();
-            const uint32_t dt0 = tmem + (uint32_t)(di * C::D_COLS);
-            for (int ka = 0; ka < slabs; ++ka, ++i) {
-                const int st = i / SPS, ai = st % C::NA;
-                const uint32_t aph = (uint32_t)((st / C::NA) & 1);
-                if (!__all_sync(0xFFFFFFFFu, ptx::mbar_wait(&sf_full[si], sph, s_abort, LIM) &&
-                                                 ptx::mbar_wait(&a_full[ai], aph, s_abort, LIM) &&
-                                                 (pos != 0 || ptx::mbar_wait(&b_full[bi], bph, s_abort, LIM)))) { ok = false; break; }
-                ptx::tc_fence_after();
-                const bool last = pos == SPS - 1 || i == n_slabs - 1;
+            for (int pos = 0; pos < nsl; ++pos) {
+                if (ka == 0) {                        // a tile starts: its accumulators must be free
+                    if (!__all_sync(0xFFFFFFFFu, ptx::mbar_wait(&d_empty[di], dph ^ 1u, s_abort, LIM))) { ok = false; break; }
+                    ptx::tc_fence_after();
+                }
                 if (ptx::elect_one()) {
                     const uint64_t ad = adesc0 + (uint64_t)((uint32_t)(ai * S::ASTAGE + pos * SLAB_SMEM_BYTES) >> 4);
                     const uint64_t bd = bdesc0 + (uint64_t)((uint32_t)(bi * S::BSTAGE + pos * S::BSLAB) >> 4);
-                    const uint32_t sfa = tmem + (uint32_t)(C::SF_BASE + si * C::SF_COLS), sfb = sfa + 4;
+                    const uint32_t sfa = tmem + (uint32_t)(C::SF_BASE + sc * C::CELL_COLS + pos * C::SF_COLS);
+                    const uint32_t dt0 = tmem + (uint32_t)(di * C::D_COLS);
 #pragma unroll
                     for (int kb = 0; kb < 4; ++kb) {
                         const int kk = ka * 4 + kb;          // 32-K block index in the tile
                         // overwrite on the first use of each accumulator in the tile
                         ptx::mma_mx_ss(dt0 + (uint32_t)((kk % C::NACC) * NP), ad + (uint64_t)(kb * 2),
-                                       bd + (uint64_t)(kb * 2), ptx::idesc_mx_e2m1_e4m3(128, NP, (uint32_t)kb), sfa, sfb,
-                                       kk >= C::NACC ? 1u : 0u);
+                                       bd + (uint64_t)(kb * 2), ptx::idesc_mx_e2m1_e4m3(128, NP, (uint32_t)kb), sfa,
+                                       sfa + 4, kk >= C::NACC ? 1u : 0u);
                     }
-                    ptx::mma_commit(&sf_empty[si]);
-                    if (last) {
-                        ptx::mma_commit(&a_empty[ai]);
-                        ptx::mma_commit(&b_empty[bi]);
-                    }
+                    if (ka == slabs - 1) ptx::mma_commit(&d_full[di]);
                 }
                 __syncwarp();
                 issued = true;
-                if (++si == C::NSF) { si = 0; sph ^= 1u; }
-                if (last) {
-                    pos = 0;
-                    if (++bi == C::NB) { bi = 0; bph ^= 1u; }
-                } else {
-                    ++pos;
+                if (++ka == slabs) {
+                    ka = 0;
+                    if (++di == 2) { di = 0; dph ^= 1u; }
                 }
             }
             if (!ok) break;
-            if (ptx::elect_one()) ptx::mma_commit(&d_full[di]);
+            if (ptx::elect_one()) {
+                ptx::mma_commit(&sf_empty[sc]);
+                ptx::mma_commit(&a_empty[ai]);
+                ptx::mma_commit(&b_empty[bi]);
+            }
             __syncwarp();
-            if (++di == 2) { di = 0; dph ^= 1u; }
+            if (++ai == C::NA) { ai = 0; aph ^= 1u; }
+            if (++bi == C::NB) { bi = 0; bph ^= 1u; }
+            if (++sc == C::NSF) { sc = 0; sph ^= 1u; }
         }
         if (!ok && lane == 0) fail();
         if (issued) {            // all MMAs retired before TMEM is released
@@ -534,7 +536,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_kernel(const __grid_co
                                 const uint32_t q = mxfp8_term1(r, e1, term, sb);
                                 p.hq[((int64_t)term * p.rows_cap + row) * p.I + f] = (uint8_t)q;
                                 if (writes_scale)
-                                    p.hs[((int64_t)term * p.rows_cap + row) * (p.I / 32) + blk] = (uint8_t)sb;
+                                    p.hs[(((int64_t)(blk >> 2) * NT_H + term) * p.rows_sf + row) * 4 + (blk & 3)] = (uint8_t)sb;
                             }
                         }
                     }
@@ -567,11 +569,15 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_kernel(const __grid_co
 
 // Gathered activations as NT_X MXFP8 terms: row r of the permutation gets
 // the terms of x[token(r)], padding rows (row_to_pair == -1) get zeros. One
-// thread per (row, 32-element block). Rows past padded[E] are not touched.
+// thread per (row, 32-element block). Terms are [NT_X][rows_cap][H] E4M3
+// bytes; scales are 32-bit words [H/128][NT_X][rows_sf], byte b % 4 of word
+// (b / 4, t, r) for 32-element block b (one TMA box then fetches a slab's
+// scales for all rows and terms of a tile). Rows past padded[E] are not
+// touched.
 __global__ void gather_quant_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ row_to_pair,
                                     const int32_t *__restrict__ padded, int E, int H, int k, int64_t P,
-                                    int64_t rows_cap, uint8_t *__restrict__ xq, uint8_t *__restrict__ xs,
-                                    int32_t *dev_error)
+                                    int64_t rows_cap, int64_t rows_sf, uint8_t *__restrict__ xq,
+                                    uint8_t *__restrict__ xs, int32_t *dev_error)
 {
     const int64_t R = __ldg(padded + E);
     const int nblk = H / 32;
@@ -614,7 +620,7 @@ __global__ void gather_quant_kernel(const uint16_t *__restrict__ x, const int32_
             uint4 *dst = reinterpret_cast<uint4 *>(xq + ((int64_t)t * rows_cap + r) * H + b * 32);
             dst[0] = make_uint4(wq[0], wq[1], wq[2], wq[3]);
             dst[1] = make_uint4(wq[4], wq[5], wq[6], wq[7]);
-            xs[((int64_t)t * rows_cap + r) * nblk + b] = (uint8_t)sbyte;
+            xs[(((int64_t)(b >> 2) * NT_X + t) * rows_sf + r) * 4 + (b & 3)] = (uint8_t)sbyte;
         }
     }
 }
@@ -679,7 +685,7 @@ int regime_nmax(Regime rg, int which)
     }
 }
 
-int regime_sps(Regime rg) { return (rg == Regime::Tiny || rg == Regime::Small) ? 2 : 1; }
+int regime_sps(Regime) { return 2; }
 
 static void mark(const ForwardArgs &a, int i, cudaStream_t s)
 {
@@ -696,8 +702,8 @@ cudaError_t launch_forward(const ForwardArgs &a, cudaStream_t s)
         int grid = (int)((n + 255) / 256);
         if (grid > 8 * 1024) grid = 8 * 1024;
         if (grid < 1) grid = 1;
-        gather_quant_kernel<<<grid, 256, 0, s>>>(a.x, a.row_to_pair, a.padded, a.E, a.H, a.k, P, a.rows_cap, a.xq,
-                                                 a.xs, a.dev_error);
+        gather_quant_kernel<<<grid, 256, 0, s>>>(a.x, a.row_to_pair, a.padded, a.E, a.H, a.k, P, a.rows_cap,
+                                                 a.rows_sf, a.xq, a.xs, a.dev_error);
         if ((err = cudaGetLastError()) != cudaSuccess) return err;
     }
     mark(a, 1, s);
@@ -712,6 +718,7 @@ cudaError_t launch_forward(const ForwardArgs &a, cudaStream_t s)
     g.swiglu_limit = a.swiglu_limit;
     g.P = P;
     g.rows_cap = a.rows_cap;
+    g.rows_sf = a.rows_sf;
     g.hq = a.hq;
     g.hs = a.hs;
     g.staging = a.staging;
@@ -721,8 +728,8 @@ cudaError_t launch_forward(const ForwardArgs &a, cudaStream_t s)
     g.tm_a = *a.tmap_w13;
     g.tm_a1 = *a.tmap_w13_1;
     g.tm_b = *a.tmap_xq;
+    g.tm_bs = *a.tmap_xs;
     g.wsf = a.packed + (size_t)a.E * 2 * a.I * (a.H / 2);
-    g.bsf = a.xs;
     g.K = a.H;
     g.MB = a.I / 64;
     const Regime rg = a.regime;
@@ -737,8 +744,8 @@ cudaError_t launch_forward(const ForwardArgs &a, cudaStream_t s)
     g.tm_a = *a.tmap_w2;
     g.tm_a1 = *a.tmap_w2_1;
     g.tm_b = *a.tmap_hq;
+    g.tm_bs = *a.tmap_hs;
     g.wsf = a.packed + packed_w13_bytes(a.E, a.H, a.I) + (size_t)a.E * a.H * (a.I / 2);
-    g.bsf = a.hs;
     g.K = a.I;
     g.MB = a.H / TILE_ROWS;
     err = rg == Regime::Tiny  ? launch_gemm<W2Tiny>(g, a.num_sms, s)

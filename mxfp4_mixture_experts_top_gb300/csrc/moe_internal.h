@@ -49,18 +49,19 @@ size_t packed_w2_bytes(int E, int H, int I);
 struct ForwardArgs {
     int T, H, I, E, k, block_m;
     float swiglu_limit;
-    int64_t rows_cap;
+    int64_t rows_cap, rows_sf;   // permutation rows; rows of the scale-word arrays (a multiple of 4)
     const uint16_t *x;
     const uint8_t *packed;
     const float *topk_w;
     const int32_t *offsets, *padded, *row_to_pair;
     float *y;
     int32_t *dev_error;
-    uint8_t *xq, *xs;      // x terms [NT_X][rows_cap][H], their scales [NT_X][rows_cap][H/32]
-    uint8_t *hq, *hs;      // h terms [NT_H][rows_cap][I], their scales [NT_H][rows_cap][I/32]
+    uint8_t *xq, *xs;      // x terms [NT_X][rows_cap][H], scale words [H/128][NT_X][rows_sf]
+    uint8_t *hq, *hs;      // h terms [NT_H][rows_cap][I], scale words [I/128][NT_H][rows_sf]
     float *staging;
     const CUtensorMap *tmap_w13, *tmap_w13_1, *tmap_w2, *tmap_w2_1;   // weight nibbles: stage / single-slab boxes
     const CUtensorMap *tmap_xq, *tmap_hq;                            // activation terms
+    const CUtensorMap *tmap_xs, *tmap_hs;                            // their scale words
     Regime regime;
     int num_sms;
     void *const *events;   // optional: 5 cudaEvent_t recorded between kernels
