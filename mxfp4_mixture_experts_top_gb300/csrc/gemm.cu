@@ -31,7 +31,8 @@
 // TMEM lane quarter: the tensor core's sub-partition q reads the scale factors
 // of its 32 A rows, and of every B row, from lane quarter q, so each quarter
 // holds a full copy), 8 MMA issuer and TMEM owner, 9 activation producer (3-D
-// TMA), 10 weight producer (2-D TMA + bulk copy).
+// TMA), 10 weight producer (2-D TMA + bulk copy), 11 second MMA issuer (decode
+// configurations).
 // Every wait is bounded (2 s); on time-out a CTA records MOE_ERR_TIMEOUT,
 // drains its copies and MMAs, frees TMEM and exits.
 #include <cuda_bf16.h>
@@ -57,37 +58,40 @@ constexpr int TMEM_COLS = 512;
 // step, so each step's fixed cost (barrier waits and arrivals, copy issue: a
 // few hundred cycles) is paid once per SPS slabs. NA / NB: weight /
 // activation ring stages. NSF: TMEM scale-factor cells (one stage each).
-// NACC: accumulators per tile (consecutive 32-K blocks rotate over them, so
-// short MMAs do not wait on each other).
-template <int MODE_, int NMAX_, int NT_, int SPS_, int NA_, int NB_, int NSF_, int NACC_>
+// NACC: accumulators per tile and MMA warp (consecutive 32-K blocks rotate
+// over them, so short MMAs do not wait on each other). MW: MMA warps; stage s
+// is issued by warp s % MW into its own accumulator sets, so while one warp
+// waits and does its bookkeeping the other keeps the tensor pipe fed.
+template <int MODE_, int NMAX_, int NT_, int SPS_, int NA_, int NB_, int NSF_, int NACC_, int MW_>
 struct Cfg {
     static constexpr int MODE = MODE_, NMAX = NMAX_, NT = NT_, SPS = SPS_, NA = NA_, NB = NB_, NSF = NSF_,
-                         NACC = NACC_;
+                         NACC = NACC_, MW = MW_;
     static constexpr int NP = NT * NMAX;                       // MMA N: all terms of NMAX rows
     static constexpr int SFB_COLS = (NP + 31) / 32;            // B scale cells: row j in column j / 32
     static constexpr int SF_COLS = (4 + SFB_COLS + 3) / 4 * 4; // one slab's cells: A (4 columns), then B
     static constexpr int CELL_COLS = SPS * SF_COLS;            // one stage
     static constexpr int D_COLS = NACC * NP;                   // one accumulator set
-    static constexpr int SF_BASE = 2 * D_COLS;
-    static constexpr int THREADS = 352;
+    static constexpr int SF_BASE = 2 * MW * D_COLS;            // [MMA warp][double buffer][set]
+    static constexpr int THREADS = 352 + 32 * (MW - 1);
     static_assert(NP % 16 == 0 && NP <= 256, "MMA N");
     static_assert(NMAX % 16 == 0, "token rows per tile");
     static_assert(SF_BASE + NSF * CELL_COLS <= TMEM_COLS, "TMEM budget");
     static_assert(SPS == 1 || SPS == 2, "slabs per stage");
+    static_assert(MW == 1 || MW == 2, "MMA warps");
 };
 
 // decode, <= 2 rows per expert on average
-using W13Tiny = Cfg<0, 16, NT_X, 2, 5, 4, 6, 2>;
-using W2Tiny = Cfg<1, 16, NT_H, 2, 5, 3, 6, 2>;
+using W13Tiny = Cfg<0, 16, NT_X, 2, 5, 4, 6, 2, 2>;
+using W2Tiny = Cfg<1, 16, NT_H, 2, 5, 3, 6, 2, 2>;
 // decode batches: <= 16 rows per expert
-using W13Small = Cfg<0, 32, NT_X, 2, 4, 4, 6, 2>;
-using W2Small = Cfg<1, 32, NT_H, 2, 4, 3, 4, 2>;
+using W13Small = Cfg<0, 32, NT_X, 2, 4, 4, 6, 1, 2>;
+using W2Small = Cfg<1, 32, NT_H, 2, 4, 3, 4, 1, 2>;
 // <= 64 rows per expert
-using W13Mid = Cfg<0, 64, NT_X, 2, 3, 3, 6, 1>;
-using W2Mid = Cfg<1, 64, NT_H, 2, 3, 2, 4, 1>;
+using W13Mid = Cfg<0, 64, NT_X, 2, 3, 3, 6, 1, 1>;
+using W2Mid = Cfg<1, 64, NT_H, 2, 3, 2, 4, 1, 1>;
 // prefill
-using W13Large = Cfg<0, 96, NT_X, 2, 3, 2, 4, 1>;
-using W2Large = Cfg<1, 64, NT_H, 2, 3, 2, 4, 1>;
+using W13Large = Cfg<0, 96, NT_X, 2, 3, 2, 4, 1, 1>;
+using W2Large = Cfg<1, 64, NT_H, 2, 3, 2, 4, 1, 1>;
 static_assert(W13Large::NMAX == 96 && W2Large::NMAX == 64, "regime_nmax() mirrors these");
 
 struct GemmParams {
@@ -241,10 +245,10 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_kernel(const __grid_co
         for (int i = 0; i < C::NB; ++i) { ptx::mbar_init(&b_full[i], 1); ptx::mbar_init(&b_empty[i], 1); }
         for (int i = 0; i < C::NSF; ++i) { ptx::mbar_init(&sf_full[i], 4); ptx::mbar_init(&sf_empty[i], 1); }
         for (int i = 0; i < 2; ++i) {
-            ptx::mbar_init(&d_full[i], 1);
+            ptx::mbar_init(&d_full[i], C::MW);    // one commit per MMA warp and tile
             ptx::mbar_init(&d_empty[i], 4);
         }
-        ptx::mbar_init(mma_done, 1);
+        ptx::mbar_init(mma_done, C::MW);
         *s_abort = 0;
         ptx::fence_mbar_init();
     }
@@ -403,64 +407,81 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_kernel(const __grid_co
             if (++sc == C::NSF) { sc = 0; sph ^= 1u; }
         }
         if (!ok && lane == 0) fail();
-    } else if (warp == 8) {
-        // ===================== MMA issuer: per stage, four block-scaled MMAs (K = 32 each) per slab
+    } else if (warp == 8 || (C::MW == 2 && warp == 11)) {
+        // ===================== MMA issuers: stage s belongs to warp s % MW, which waits for it, issues
+        // its four block-scaled MMAs (K = 32 each) per slab into the warp's own accumulator set and
+        // frees it. Both warps walk every slab to follow the tiles: at each tile's start a warp waits
+        // for the tile's accumulator buffer to be free, at its end it commits the tile (with or without
+        // MMAs of its own in it), so the epilogue sees one arrival per warp and tile.
+        const int q = warp == 8 ? 0 : 1;
         const uint64_t adesc0 = ptx::smem_desc_sw128(ptx::smem_u32(aring));
         const uint64_t bdesc0 = ptx::smem_desc_sw128(ptx::smem_u32(bring));
-        int ai = 0, bi = 0, sc = 0, di = 0, ka = 0;
+        int ai = 0, bi = 0, sc = 0, di = 0, ka = 0, st = 0, mine_in_tile = 0;
         uint32_t aph = 0, bph = 0, sph = 0, dph = 0;
         bool ok = true, issued = false;
-        for (int i0 = 0; i0 < n_slabs && ok; i0 += SPS) {
+        for (int i0 = 0; i0 < n_slabs && ok; i0 += SPS, ++st) {
             const int nsl = n_slabs - i0 < SPS ? n_slabs - i0 : SPS;
-            if (!__all_sync(0xFFFFFFFFu, ptx::mbar_wait(&sf_full[sc], sph, s_abort, LIM) &&
-                                             ptx::mbar_wait(&a_full[ai], aph, s_abort, LIM) &&
-                                             ptx::mbar_wait(&b_full[bi], bph, s_abort, LIM))) { ok = false; break; }
-            ptx::tc_fence_after();
+            const bool mine = (st % C::MW) == q;
+            if (mine) {
+                if (!__all_sync(0xFFFFFFFFu, ptx::mbar_wait(&sf_full[sc], sph, s_abort, LIM) &&
+                                                 ptx::mbar_wait(&a_full[ai], aph, s_abort, LIM) &&
+                                                 ptx::mbar_wait(&b_full[bi], bph, s_abort, LIM))) { ok = false; break; }
+                ptx::tc_fence_after();
+            }
             for (int pos = 0; pos < nsl; ++pos) {
                 if (ka == 0) {                        // a tile starts: its accumulators must be free
                     if (!__all_sync(0xFFFFFFFFu, ptx::mbar_wait(&d_empty[di], dph ^ 1u, s_abort, LIM))) { ok = false; break; }
                     ptx::tc_fence_after();
+                    mine_in_tile = 0;
                 }
-                if (ptx::elect_one()) {
-                    const uint64_t ad = adesc0 + (uint64_t)((uint32_t)(ai * S::ASTAGE + pos * SLAB_SMEM_BYTES) >> 4);
-                    const uint64_t bd = bdesc0 + (uint64_t)((uint32_t)(bi * S::BSTAGE + pos * S::BSLAB) >> 4);
-                    const uint32_t sfa = tmem + (uint32_t)(C::SF_BASE + sc * C::CELL_COLS + pos * C::SF_COLS);
-                    const uint32_t dt0 = tmem + (uint32_t)(di * C::D_COLS);
+                if (mine) {
+                    if (ptx::elect_one()) {
+                        const uint64_t ad = adesc0 + (uint64_t)((uint32_t)(ai * S::ASTAGE + pos * SLAB_SMEM_BYTES) >> 4);
+                        const uint64_t bd = bdesc0 + (uint64_t)((uint32_t)(bi * S::BSTAGE + pos * S::BSLAB) >> 4);
+                        const uint32_t sfa = tmem + (uint32_t)(C::SF_BASE + sc * C::CELL_COLS + pos * C::SF_COLS);
+                        const uint32_t dt0 = tmem + (uint32_t)((q * 2 + di) * C::D_COLS);
 #pragma unroll
-                    for (int kb = 0; kb < 4; ++kb) {
-                        const int kk = ka * 4 + kb;          // 32-K block index in the tile
-                        // overwrite on the first use of each accumulator in the tile
-                        ptx::mma_mx_ss(dt0 + (uint32_t)((kk % C::NACC) * NP), ad + (uint64_t)(kb * 2),
-                                       bd + (uint64_t)(kb * 2), ptx::idesc_mx_e2m1_e4m3(128, NP, (uint32_t)kb), sfa,
-                                       sfa + 4, kk >= C::NACC ? 1u : 0u);
+                        for (int kb = 0; kb < 4; ++kb) {
+                            const int kk = mine_in_tile + kb;    // this warp's 32-K blocks in the tile so far
+                            // overwrite on the first use of each accumulator in the tile
+                            ptx::mma_mx_ss(dt0 + (uint32_t)((kk % C::NACC) * NP), ad + (uint64_t)(kb * 2),
+                                           bd + (uint64_t)(kb * 2), ptx::idesc_mx_e2m1_e4m3(128, NP, (uint32_t)kb),
+                                           sfa, sfa + 4, kk >= C::NACC ? 1u : 0u);
+                        }
                     }
-                    if (ka == slabs - 1) ptx::mma_commit(&d_full[di]);
+                    __syncwarp();
+                    mine_in_tile += 4;
+                    issued = true;
                 }
-                __syncwarp();
-                issued = true;
+                if (ka == slabs - 1) {                // the tile ends: one commit per warp
+                    if (ptx::elect_one()) ptx::mma_commit(&d_full[di]);
+                    __syncwarp();
+                }
                 if (++ka == slabs) {
                     ka = 0;
                     if (++di == 2) { di = 0; dph ^= 1u; }
                 }
             }
             if (!ok) break;
-            if (ptx::elect_one()) {
-                ptx::mma_commit(&sf_empty[sc]);
-                ptx::mma_commit(&a_empty[ai]);
-                ptx::mma_commit(&b_empty[bi]);
+            if (mine) {
+                if (ptx::elect_one()) {
+                    ptx::mma_commit(&sf_empty[sc]);
+                    ptx::mma_commit(&a_empty[ai]);
+                    ptx::mma_commit(&b_empty[bi]);
+                }
+                __syncwarp();
             }
-            __syncwarp();
             if (++ai == C::NA) { ai = 0; aph ^= 1u; }
             if (++bi == C::NB) { bi = 0; bph ^= 1u; }
             if (++sc == C::NSF) { sc = 0; sph ^= 1u; }
         }
         if (!ok && lane == 0) fail();
-        if (issued) {            // all MMAs retired before TMEM is released
-            volatile int never = 0;
-            if (ptx::elect_one()) ptx::mma_commit(mma_done);
-            __syncwarp();
-            __all_sync(0xFFFFFFFFu, ptx::mbar_wait(mma_done, 0, &never, LIM));
-        }
+        // one arrival per MMA warp once its MMAs have retired (TMEM is released after that)
+        volatile int never = 0;
+        if (ptx::elect_one()) ptx::mma_commit(mma_done);
+        __syncwarp();
+        if (q == 0) __all_sync(0xFFFFFFFFu, ptx::mbar_wait(mma_done, 0, &never, LIM));
+        (void)issued;
     } else if (warp < 4) {
         // ===================== epilogue: TMEM -> registers -> global. The W13 epilogue pairs warps
         // at a named barrier, so no warp leaves the tile loop early: after a failed wait a warp
@@ -469,27 +490,35 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_kernel(const __grid_co
         int di = 0, chunk = 0;
         uint32_t dph = 0;
         bool ok = true;
-        for (int t = blockIdx.x; t < total; t += gridDim.x) {
+        int j = 0;
+        for (int t = blockIdx.x; t < total; t += gridDim.x, ++j) {
             const Tile tl = decode_tile<C>(t, tile_start, E, MB, p.offsets, p.padded);
+            // MMA warp q wrote into the tile iff one of the tile's stages is one of its stages
+            const int s_first = (j * slabs) / SPS, s_last = (j * slabs + slabs - 1) / SPS;
+            const unsigned wrote = (C::MW == 1 || s_last > s_first) ? ((1u << C::MW) - 1u) : (1u << (s_first % C::MW));
             ok = ok && __all_sync(0xFFFFFFFFu, ptx::mbar_wait(&d_full[di], dph, s_abort, LIM));
             ptx::tc_fence_after();
-            const uint32_t dt = tmem + t_lane + (uint32_t)(di * C::D_COLS);
             for (int c0 = 0; c0 < tl.n; c0 += 16, ++chunk) {
                 uint32_t raw[16];
 #pragma unroll
                 for (int q = 0; q < 16; ++q) raw[q] = 0u;
                 if (ok) {
 #pragma unroll
-                    for (int a = 0; a < C::NACC; ++a)
+                    for (int w = 0; w < C::MW; ++w) {
+                        if (!((wrote >> w) & 1u)) continue;
+                        const uint32_t dt = tmem + t_lane + (uint32_t)((w * 2 + di) * C::D_COLS);
 #pragma unroll
-                        for (int term = 0; term < NT; ++term) {   // sum the accumulators and the term columns
-                            uint32_t part[16];
-                            ptx::tmem_ld_32x32b_x16(dt + (uint32_t)(a * NP + term * NMAX + c0), part);
-                            ptx::tmem_wait_ld();
+                        for (int a = 0; a < C::NACC; ++a)
 #pragma unroll
-                            for (int q = 0; q < 16; ++q)
-                                raw[q] = __float_as_uint(__uint_as_float(raw[q]) + __uint_as_float(part[q]));
-                        }
+                            for (int term = 0; term < NT; ++term) {   // sum the accumulators and the term columns
+                                uint32_t part[16];
+                                ptx::tmem_ld_32x32b_x16(dt + (uint32_t)(a * NP + term * NMAX + c0), part);
+                                ptx::tmem_wait_ld();
+#pragma unroll
+                                for (int q = 0; q < 16; ++q)
+                                    raw[q] = __float_as_uint(__uint_as_float(raw[q]) + __uint_as_float(part[q]));
+                            }
+                    }
                 }
                 if (MODE == 0) {
                     // lane i < 16: gate of feature f; lane i + 16: up of the same f. Lane i ends with
