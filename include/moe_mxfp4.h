@@ -126,6 +126,19 @@ moe_status_t moe_permute(const int32_t *d_topk_ids, int T, int E, int k, int blo
                          int32_t *d_row_to_pair, int32_t *d_pair_to_row, int32_t *d_error,
                          void *stream);
 
+/*
+ * moe_route followed by moe_permute on the ids it writes, in one launch (one
+ * thread block) for T <= 128 and in two launches above: same arguments, same
+ * outputs, same bit-exactness. The fused form saves a decode step one kernel
+ * boundary (the first of the two steps of the fused decode path).
+ * T == 0 writes counts, offsets and padded offsets (all zero) like moe_permute.
+ */
+moe_status_t moe_route_permute(const float *d_logits, int T, int E, int k, int block_m,
+                               int32_t *d_topk_ids, float *d_topk_w, uint32_t *d_bitmatrix,
+                               int32_t *d_counts, int32_t *d_offsets, int32_t *d_padded_offsets,
+                               int32_t *d_row_to_pair, int32_t *d_pair_to_row, int32_t *d_error,
+                               void *stream);
+
 /* Bytes of the prepacked weight buffer for desc (T is ignored). */
 size_t moe_mxfp4_packed_bytes(const moe_layer_desc *desc);
 

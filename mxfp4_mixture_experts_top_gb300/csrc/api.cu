@@ -224,6 +224,27 @@ moe_status_t moe_permute(const int32_t *d_topk_ids, int T, int E, int k, int blo
                                     d_row_to_pair, cap, d_pair_to_row, d_error, (cudaStream_t)stream));
 }
 
+moe_status_t moe_route_permute(const float *d_logits, int T, int E, int k, int block_m, int32_t *d_topk_ids,
+                               float *d_topk_w, uint32_t *d_bitmatrix, int32_t *d_counts, int32_t *d_offsets,
+                               int32_t *d_padded_offsets, int32_t *d_row_to_pair, int32_t *d_pair_to_row,
+                               int32_t *d_error, void *stream)
+{
+    if (T < 0 || E <= 0 || k <= 0 || k > E) return MOE_ERR_INVALID_ARG;
+    if (E > 1024 || k > 32) return MOE_ERR_UNSUPPORTED;
+    if (block_m != 16 && block_m != 32 && block_m != 64 && block_m != 128) return MOE_ERR_UNSUPPORTED;
+    if ((int64_t)T * k > (int64_t)INT32_MAX / 2) return MOE_ERR_UNSUPPORTED;
+    if (!d_counts || !d_offsets || !d_padded_offsets) return MOE_ERR_INVALID_ARG;
+    if (T > 0 && (!d_logits || !d_topk_ids || !d_topk_w || !d_row_to_pair || !d_pair_to_row)) return MOE_ERR_INVALID_ARG;
+    const void *ptrs[] = {d_logits, d_topk_ids, d_topk_w, d_bitmatrix, d_counts, d_offsets, d_padded_offsets,
+                          d_row_to_pair, d_pair_to_row, d_error};
+    for (const void *p : ptrs)
+        if (p && !aligned16(p)) return MOE_ERR_MISALIGNED;
+    const int64_t cap = moe_permute_rows_capacity(T, E, k, block_m);
+    return from_cuda(launch_route_permute(d_logits, T, E, k, block_m, d_topk_ids, d_topk_w, d_bitmatrix, d_counts,
+                                          d_offsets, d_padded_offsets, d_row_to_pair, cap, d_pair_to_row, d_error,
+                                          (cudaStream_t)stream));
+}
+
 size_t moe_mxfp4_packed_bytes(const moe_layer_desc *d)
 {
     if (!d || d->E <= 0 || d->H <= 0 || d->I <= 0 || d->H % 128 || d->I % 128) return 0;

@@ -36,6 +36,14 @@ cudaError_t launch_permute(const int32_t *ids, int T, int E, int k, int block_m,
                            int32_t *offsets, int32_t *padded, int32_t *row_to_pair, int64_t rows_cap,
                            int32_t *pair_to_row, int32_t *dev_error, cudaStream_t s);
 
+// Routing and permutation in one launch (one thread block) up to this many tokens; two launches above.
+constexpr int ROUTE_PERMUTE_FUSED_MAX_T = 128;
+
+cudaError_t launch_route_permute(const float *logits, int T, int E, int k, int block_m, int32_t *ids, float *w,
+                                 uint32_t *bitmatrix, int32_t *counts, int32_t *offsets, int32_t *padded,
+                                 int32_t *row_to_pair, int64_t rows_cap, int32_t *pair_to_row, int32_t *dev_error,
+                                 cudaStream_t s);
+
 cudaError_t launch_prepack(const uint8_t *w13_q, const uint8_t *w13_s, const uint8_t *w2_q,
                            const uint8_t *w2_s, int E, int H, int I, uint8_t *packed, cudaStream_t s);
 

@@ -18,9 +18,14 @@
 // its range again in order; a pair's row is padded[e] + warp base + (pairs of
 // e earlier in the range), so rows of one expert come out in ascending pair
 // order (stable). Phase 4 writes -1 into padding and tail rows.
+//
+// The fused routing + permutation kernel (small batches) runs the per-token
+// routing of route_token.cuh in the same thread block first, so a decode
+// step spends one launch on both.
 #include <cstdint>
 
 #include "moe_internal.h"
+#include "route_token.cuh"
 
 namespace moe {
 
@@ -53,11 +58,11 @@ __device__ __forceinline__ int block_inclusive_scan(int v, int *warp_tot)
     return r;
 }
 
-__global__ void __launch_bounds__(PERM_THREADS, 1)
-permute_kernel(const int32_t *__restrict__ ids, int T, int E, int k, int block_m,
-               int32_t *__restrict__ counts, int32_t *__restrict__ offsets, int32_t *__restrict__ padded,
-               int32_t *__restrict__ row_to_pair, int64_t rows_cap, int32_t *__restrict__ pair_to_row,
-               int32_t *__restrict__ dev_error)
+__device__ __forceinline__ void permute_block(const int32_t *__restrict__ ids, int T, int E, int k, int block_m,
+                                              int32_t *__restrict__ counts, int32_t *__restrict__ offsets,
+                                              int32_t *__restrict__ padded, int32_t *__restrict__ row_to_pair,
+                                              int64_t rows_cap, int32_t *__restrict__ pair_to_row,
+                                              int32_t *__restrict__ dev_error)
 {
     extern __shared__ int smem[];
     int *hist = smem;                                  // [PERM_WARPS][E]
@@ -146,11 +151,75 @@ permute_kernel(const int32_t *__restrict__ ids, int T, int E, int k, int block_m
     if (tid == 0 && s_err && dev_error) atomicExch(dev_error, DEV_ERR_ID_RANGE);
 }
 
+__global__ void __launch_bounds__(PERM_THREADS, 1)
+permute_kernel(const int32_t *__restrict__ ids, int T, int E, int k, int block_m,
+               int32_t *__restrict__ counts, int32_t *__restrict__ offsets, int32_t *__restrict__ padded,
+               int32_t *__restrict__ row_to_pair, int64_t rows_cap, int32_t *__restrict__ pair_to_row,
+               int32_t *__restrict__ dev_error)
+{
+    permute_block(ids, T, E, k, block_m, counts, offsets, padded, row_to_pair, rows_cap, pair_to_row, dev_error);
+}
+
+// Routing of all T tokens (warp w takes tokens w, w + 32, ...), then the
+// permutation of the ids just written, in one thread block.
+template <int VPL>
+__global__ void __launch_bounds__(PERM_THREADS, 1)
+route_permute_kernel(const float *__restrict__ logits, int T, int E, int k, int block_m, int32_t *__restrict__ ids,
+                     float *__restrict__ w, uint32_t *__restrict__ bitmatrix, int32_t *__restrict__ counts,
+                     int32_t *__restrict__ offsets, int32_t *__restrict__ padded, int32_t *__restrict__ row_to_pair,
+                     int64_t rows_cap, int32_t *__restrict__ pair_to_row, int32_t *__restrict__ dev_error)
+{
+    for (int t = threadIdx.x >> 5; t < T; t += PERM_WARPS) route_token<VPL>(logits, t, E, k, ids, w, bitmatrix);
+    __syncthreads();          // the ids written above are visible to the whole block
+    permute_block(ids, T, E, k, block_m, counts, offsets, padded, row_to_pair, rows_cap, pair_to_row, dev_error);
+}
+
+static size_t permute_smem(int E) { return sizeof(int) * ((size_t)PERM_WARPS * E + E + E + 1 + 32); }
+
+template <int VPL>
+static cudaError_t launch_fused(const float *logits, int T, int E, int k, int block_m, int32_t *ids, float *w,
+                                uint32_t *bitmatrix, int32_t *counts, int32_t *offsets, int32_t *padded,
+                                int32_t *row_to_pair, int64_t rows_cap, int32_t *pair_to_row, int32_t *dev_error,
+                                cudaStream_t s)
+{
+    const size_t smem = permute_smem(E);
+    cudaError_t err = cudaFuncSetAttribute(route_permute_kernel<VPL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (int)smem);
+    if (err != cudaSuccess) return err;
+    route_permute_kernel<VPL><<<1, PERM_THREADS, smem, s>>>(logits, T, E, k, block_m, ids, w, bitmatrix, counts,
+                                                            offsets, padded, row_to_pair, rows_cap, pair_to_row,
+                                                            dev_error);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_route_permute(const float *logits, int T, int E, int k, int block_m, int32_t *ids, float *w,
+                                 uint32_t *bitmatrix, int32_t *counts, int32_t *offsets, int32_t *padded,
+                                 int32_t *row_to_pair, int64_t rows_cap, int32_t *pair_to_row, int32_t *dev_error,
+                                 cudaStream_t s)
+{
+    if (T > ROUTE_PERMUTE_FUSED_MAX_T) {       // routing wants many blocks: two launches
+        cudaError_t err = launch_route(logits, T, E, k, ids, w, bitmatrix, s);
+        if (err != cudaSuccess) return err;
+        return launch_permute(ids, T, E, k, block_m, counts, offsets, padded, row_to_pair, rows_cap, pair_to_row,
+                              dev_error, s);
+    }
+    const int vpl = (E + 31) / 32;
+    cudaError_t err;
+    if (vpl <= 1) err = launch_fused<1>(logits, T, E, k, block_m, ids, w, bitmatrix, counts, offsets, padded, row_to_pair, rows_cap, pair_to_row, dev_error, s);
+    else if (vpl <= 2) err = launch_fused<2>(logits, T, E, k, block_m, ids, w, bitmatrix, counts, offsets, padded, row_to_pair, rows_cap, pair_to_row, dev_error, s);
+    else if (vpl <= 4) err = launch_fused<4>(logits, T, E, k, block_m, ids, w, bitmatrix, counts, offsets, padded, row_to_pair, rows_cap, pair_to_row, dev_error, s);
+    else if (vpl <= 8) err = launch_fused<8>(logits, T, E, k, block_m, ids, w, bitmatrix, counts, offsets, padded, row_to_pair, rows_cap, pair_to_row, dev_error, s);
+    else if (vpl <= 16) err = launch_fused<16>(logits, T, E, k, block_m, ids, w, bitmatrix, counts, offsets, padded, row_to_pair, rows_cap, pair_to_row, dev_error, s);
+    else err = launch_fused<32>(logits, T, E, k, block_m, ids, w, bitmatrix, counts, offsets, padded, row_to_pair, rows_cap, pair_to_row, dev_error, s);
+    note_launch(1);
+    return err;
+}
+
 cudaError_t launch_permute(const int32_t *ids, int T, int E, int k, int block_m, int32_t *counts,
                            int32_t *offsets, int32_t *padded, int32_t *row_to_pair, int64_t rows_cap,
                            int32_t *pair_to_row, int32_t *dev_error, cudaStream_t s)
 {
-    size_t smem = sizeof(int) * ((size_t)PERM_WARPS * E + E + E + 1 + 32);
+    size_t smem = permute_smem(E);
     cudaError_t err = cudaFuncSetAttribute(permute_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
     permute_kernel<<<1, PERM_THREADS, smem, s>>>(ids, T, E, k, block_m, counts, offsets, padded, row_to_pair,

@@ -1,29 +1,11 @@
-// Top-k expert routing: one warp per token.
-//
-// Method: "DeepSeek V4 Flash 单卡 MI300X" (txtmix.com) §一 — each token
-// picks k of E experts (top-6 of 256) from its router scores; §三 — the
-// routing bitmatrix (one bit per chosen expert). Selection runs on the fp32
-// logits themselves (softmax is monotone); equal logits go to the lower
-// expert index and -0.0 equals +0.0. Weights are the softmax restricted to
-// the chosen experts and renormalised, i.e. exp(l_j - l_max) / sum over the
-// chosen exp(l_i - l_max).
-//
-// Each lane owns experts lane, lane+32, ... (coalesced 128-byte loads) as
-// order-preserving 32-bit keys. Every round takes the warp maximum key with
-// redux.sync, then the lowest expert index among the lanes holding it.
+// Top-k expert routing: one warp per token (see route_token.cuh for the
+// method and its citations).
 #include <cstdint>
 
 #include "moe_internal.h"
+#include "route_token.cuh"
 
 namespace moe {
-
-// Order-preserving key of a finite float, with -0.0 folded onto +0.0.
-__device__ __forceinline__ uint32_t float_key(float f)
-{
-    uint32_t u = __float_as_uint(f);
-    if ((u << 1) == 0u) u = 0u;                 // -0.0 -> +0.0
-    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
 
 template <int VPL>
 __global__ void __launch_bounds__(256) route_kernel(const float *__restrict__ logits, int T, int E, int k,
@@ -32,59 +14,8 @@ __global__ void __launch_bounds__(256) route_kernel(const float *__restrict__ lo
 {
     const int warps = blockDim.x >> 5;
     const int t = blockIdx.x * warps + (threadIdx.x >> 5);
-    const uint32_t lane = threadIdx.x & 31u;
     if (t >= T) return;
-    const float *row = logits + (int64_t)t * E;
-
-    uint32_t key[VPL];
-#pragma unroll
-    for (int v = 0; v < VPL; ++v) {
-        int e = (int)lane + 32 * v;
-        key[v] = (e < E) ? float_key(__ldg(row + e)) : 0u;   // lanes past E never win (k <= E)
-    }
-    uint32_t taken = 0u;          // bit v: value v of this lane already chosen
-    int my_id = -1;               // lane j < k keeps the j-th choice
-    float my_logit = 0.f;
-
-    for (int j = 0; j < k; ++j) {
-        uint32_t best = 0u;
-        int best_v = -1;
-#pragma unroll
-        for (int v = 0; v < VPL; ++v) {
-            int e = (int)lane + 32 * v;
-            bool ok = e < E && !((taken >> v) & 1u);
-            if (ok && (best_v < 0 || key[v] > best)) { best = key[v]; best_v = v; }  // v ascending keeps lower index
-        }
-        uint32_t wmax = __reduce_max_sync(0xFFFFFFFFu, best_v >= 0 ? best : 0u);
-        uint32_t cand = (best_v >= 0 && best == wmax) ? (lane + 32u * (uint32_t)best_v) : 0xFFFFFFFFu;
-        uint32_t win = __reduce_min_sync(0xFFFFFFFFu, cand);
-        if ((win & 31u) == lane) taken |= 1u << (win >> 5);
-        if ((int)lane == j) {
-            my_id = (int)win;
-            my_logit = row[win];
-        }
-    }
-
-    // softmax over the chosen k, shifted by the first (largest) logit
-    float lmax = __shfl_sync(0xFFFFFFFFu, my_logit, 0);
-    float ex = ((int)lane < k) ? expf(my_logit - lmax) : 0.f;
-    float z = ex;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xFFFFFFFFu, z, o);
-    if ((int)lane < k) {
-        ids[(int64_t)t * k + lane] = my_id;
-        w[(int64_t)t * k + lane] = ex / z;
-    }
-    if (bitmatrix) {
-        // every lane takes part in the shuffles; lane q builds word q (E <= 1024: at most 32 words)
-        const int words = (E + 31) >> 5;
-        uint32_t bits = 0u;
-        for (int j = 0; j < k; ++j) {
-            const int e = __shfl_sync(0xFFFFFFFFu, my_id, j);
-            if ((e >> 5) == (int)lane) bits |= 1u << (e & 31);
-        }
-        if ((int)lane < words) bitmatrix[(int64_t)t * words + lane] = bits;
-    }
+    route_token<VPL>(logits, t, E, k, ids, w, bitmatrix);
 }
 
 cudaError_t launch_route(const float *logits, int T, int E, int k, int32_t *ids, float *w,

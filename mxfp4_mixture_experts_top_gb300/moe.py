@@ -24,7 +24,7 @@ STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
 EXPORTS = ["moe_abi_version", "moe_status_string", "moe_route", "moe_permute_rows_capacity", "moe_permute",
            "moe_mxfp4_packed_bytes", "moe_mxfp4_prepack", "moe_mxfp4_dequant_bf16", "moe_mxfp4_workspace_bytes",
            "moe_mxfp4_forward", "moe_mxfp4_forward_timed", "moe_mxfp4_workspace_layout", "moe_read_device_error", "moe_launch_count",
-           "moe_mxfp4_forward_noalloc"]
+           "moe_mxfp4_forward_noalloc", "moe_route_permute"]
 
 
 class MoeError(RuntimeError):
@@ -70,6 +70,7 @@ def load(path: str = LIB_PATH):
             "moe_read_device_error": ([P, ctypes.POINTER(ctypes.c_int), P], i32),
             "moe_launch_count": ([], ctypes.c_uint64),
             "moe_mxfp4_forward_noalloc": ([D, P, P, P, P, P, P, P, P], i32),
+            "moe_route_permute": ([P, i32, i32, i32, i32, P, P, P, P, P, P, P, P, P, P], i32),
         }
         for name, (args, res) in sigs.items():
             fn = getattr(lib, name)
@@ -150,6 +151,29 @@ def permute(topk_ids: torch.Tensor, E: int, block_m: int, out=None, error=None, 
                               _ptr(out["padded_offsets"]), _ptr(out["row_to_pair"]), _ptr(out["pair_to_row"]),
                               _ptr(error), _stream(stream)), "moe_permute")
     return out
+
+
+def route_permute(logits: torch.Tensor, k: int, block_m: int, out=None, perm_out=None, error=None, stream=None):
+    """moe_route_permute (one launch for T <= 128). Returns (topk_ids, topk_w, bitmatrix, perm dict)."""
+    _cuda(logits, torch.float32, "logits")
+    T, E = logits.shape
+    dev = logits.device
+    if out is None:
+        out = (torch.empty((T, k), dtype=torch.int32, device=dev), torch.empty((T, k), dtype=torch.float32, device=dev),
+               torch.empty((T, (E + 31) // 32), dtype=torch.int32, device=dev))
+    ids, w, bm = out
+    if perm_out is None:
+        cap = rows_capacity(T, E, k, block_m)
+        perm_out = dict(counts=torch.empty(E, dtype=torch.int32, device=dev),
+                        offsets=torch.empty(E + 1, dtype=torch.int32, device=dev),
+                        padded_offsets=torch.empty(E + 1, dtype=torch.int32, device=dev),
+                        row_to_pair=torch.empty(max(cap, 1), dtype=torch.int32, device=dev),
+                        pair_to_row=torch.empty(max(T * k, 1), dtype=torch.int32, device=dev))
+    po = perm_out
+    _check(load().moe_route_permute(_ptr(logits), T, E, k, block_m, _ptr(ids), _ptr(w), _ptr(bm), _ptr(po["counts"]),
+                                    _ptr(po["offsets"]), _ptr(po["padded_offsets"]), _ptr(po["row_to_pair"]),
+                                    _ptr(po["pair_to_row"]), _ptr(error), _stream(stream)), "moe_route_permute")
+    return ids, w, bm, po
 
 
 def make_desc(T, H, I, E, k, block_m=16, swiglu_limit=0.0) -> LayerDesc:
@@ -242,8 +266,8 @@ def read_device_error(word: torch.Tensor, stream=None) -> int:
 @dataclass
 class MoELayer:
     """One MXFP4 MoE layer on the current CUDA device: prepacked weights plus
-    persistent buffers, so a call is route -> permute -> forward with no
-    allocation (CUDA-graph capturable)."""
+    persistent buffers, so a call is route+permute (one launch for small
+    batches) -> forward with no allocation (CUDA-graph capturable)."""
 
     desc: LayerDesc
     packed: torch.Tensor
@@ -271,8 +295,8 @@ class MoELayer:
 
     def __call__(self, x: torch.Tensor, logits: torch.Tensor, stream=None) -> torch.Tensor:
         b = self.bufs
-        route(logits, self.desc.k, out=(b["ids"], b["w"], b["bm"]), stream=stream)
-        permute(b["ids"], self.desc.E, self.desc.block_m, out=b["perm"], error=b["perm_err"], stream=stream)
+        route_permute(logits, self.desc.k, self.desc.block_m, out=(b["ids"], b["w"], b["bm"]), perm_out=b["perm"],
+                      error=b["perm_err"], stream=stream)
         return forward(self.desc, x, self.packed, b["w"], b["perm"], self.workspace, y=b["y"], stream=stream)
 
     def capture_graph(self, x: torch.Tensor, logits: torch.Tensor):

@@ -140,3 +140,30 @@ def test_route_permute_deterministic(gpu_lib):
     pb = gpu_lib.permute(b[0], 256, 16)
     for n in pa:
         assert torch.equal(pa[n], pb[n])
+
+
+@pytest.mark.parametrize("T", [0, 1, 8, 37, 127, 128, 129, 512])
+@pytest.mark.parametrize("E,k,block_m", [(256, 6, 16), (32, 6, 128), (1024, 32, 16), (8, 8, 64)])
+def test_fused_route_permute_matches_oracle(gpu_lib, T, E, k, block_m):
+    """moe_route_permute (one launch up to T = 128, two above) gives the oracle's ids, weights,
+    bitmatrix and permutation, with heavy ties in half of the cases."""
+    rng = np.random.default_rng(T * 131 + E + k)
+    if T % 2:
+        pool = np.array([-1.0, -0.0, 0.0, 0.25, 0.25, 2.0], dtype=np.float32)
+        logits = pool[rng.integers(0, len(pool), size=(T, E))]
+    else:
+        logits = rng.standard_normal((T, E)).astype(np.float32)
+    err = torch.zeros(4, dtype=torch.int32, device="cuda")
+    ids, w, bm, perm = gpu_lib.route_permute(torch.from_numpy(logits).cuda(), k, block_m, error=err)
+    torch.cuda.synchronize()
+    ids_r, w_r, bm_r = oracle.route(logits, k)
+    ref = oracle.permute(ids_r, E, block_m)
+    np.testing.assert_array_equal(ids.cpu().numpy().reshape(T, k), ids_r)
+    np.testing.assert_array_equal(bm.cpu().numpy().view(np.uint32).reshape(bm_r.shape), bm_r)
+    assert np.abs(w.cpu().numpy().astype(np.float64) - w_r).max(initial=0) <= 1e-6
+    for name in ("counts", "offsets", "padded_offsets"):
+        np.testing.assert_array_equal(perm[name].cpu().numpy(), ref[name], err_msg=name)
+    cap = oracle.rows_capacity(T, E, k, block_m)
+    np.testing.assert_array_equal(perm["row_to_pair"].cpu().numpy()[:cap], ref["row_to_pair"])
+    np.testing.assert_array_equal(perm["pair_to_row"].cpu().numpy()[:T * k], ref["pair_to_row"])
+    assert gpu_lib.read_device_error(err) == 0
