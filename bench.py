@@ -52,7 +52,7 @@ NT_X, NT_H = 2, 3   # MXFP8 terms of the activations: x (bf16) and h = SiLU(gate
 
 
 def algorithmic(L, ids):
-    """Algorithmic bytes and flops of one step (roofline section).
+    """Algorithmic bytes and flops of one step.
 
     W13 kernel: touched experts' MXFP4 W13 bytes (nibbles + E8M0 scales), the P gathered
     activation rows as NT_X E4M3 terms with one scale byte per 32 elements, and the P rows of

@@ -243,7 +243,7 @@ moe_status_t moe_mxfp4_workspace_layout(const moe_layer_desc *desc, size_t out[7
  *   routine).
  *   Returns MOE_ERR_WORKSPACE when moe_mxfp4_workspace_bytes(desc) exceeds
  *   MOE_NOALLOC_SCRATCH_BYTES (e.g. H = 4096, I = 2048, E = 256, k = 6,
- *   block_m = 16 fits up to T = 20 tokens); use moe_mxfp4_forward for larger layers.
+ *   block_m = 16 fits up to T = 22 tokens); use moe_mxfp4_forward for larger layers.
  *   The first call on a device looks up the array's device address (once per
  *   device, with that device current); make that first call before any stream
  *   capture. All calls share the array, which keeps the previous call's
