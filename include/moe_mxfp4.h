@@ -223,11 +223,13 @@ moe_status_t moe_mxfp4_forward_timed(const moe_layer_desc *desc, const uint16_t 
 
 /* Byte offsets of the forward's intermediates inside the workspace, for
  * inspection: out[0] error word; out[1] gathered activation terms (E4M3
- * [2][R][H]: term, permutation row, hidden unit); out[2] their E8M0 scales
- * ([2][R][H/32]); out[3] SiLU(gate)*up terms (E4M3 [3][R][I]); out[4] their
- * scales ([3][R][I/32]); out[5] per-pair W2 outputs (fp32 [T*k, H]); out[6]
- * total bytes. R = moe_permute_rows_capacity(T, E, k, block_m). A row's value
- * is sum over terms of E4M3 value * 2^(scale byte - 127). */
+ * [H/128][2][R][128]: 128-element slab, term, permutation row, element);
+ * out[2] their E8M0 scales as 32-bit words [H/128][2][RS] (byte b of a word:
+ * 32-element block b of the slab; RS = R rounded up to 4); out[3]
+ * SiLU(gate)*up terms (E4M3 [I/128][3][R][128]); out[4] their scale words
+ * ([I/128][3][RS]); out[5] per-pair W2 outputs (fp32 [T*k, H]); out[6] total
+ * bytes. R = moe_permute_rows_capacity(T, E, k, block_m). An element's value
+ * is the sum over terms of E4M3 value * 2^(scale byte - 127). */
 moe_status_t moe_mxfp4_workspace_layout(const moe_layer_desc *desc, size_t out[7]);
 
 /*

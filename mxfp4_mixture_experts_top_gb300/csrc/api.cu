@@ -45,10 +45,10 @@ struct MapKey {
     int dev, kind;
     const void *ptr;
     uint64_t d0, d1, d2;
-    uint32_t b1;
+    uint32_t b1, b3;
     bool operator<(const MapKey &o) const
     {
-        return std::tie(dev, kind, ptr, d0, d1, d2, b1) < std::tie(o.dev, o.kind, o.ptr, o.d0, o.d1, o.d2, o.b1);
+        return std::tie(dev, kind, ptr, d0, d1, d2, b1, b3) < std::tie(o.dev, o.kind, o.ptr, o.d0, o.d1, o.d2, o.b1, o.b3);
     }
 };
 
@@ -61,15 +61,16 @@ std::map<MapKey, MapEntry> g_maps;
 
 // Cached tensor map. kind 0: prepacked weight nibbles, a 2-D tensor of d1 rows of 128 E2M1 values
 // (64 B) read as "16 x U4, 16-byte aligned" (each 8-byte group lands in 16 bytes of shared memory),
-// box 128 x b1 rows. kind 1: activation terms, a 3-D uint8 tensor [d2 terms][d1 rows][d0 K], box
-// 128 x b1 x d2. Both with the 128-byte swizzle of the MMA operands. kind 2: activation scale
-// words, a 3-D uint32 tensor [slabs][d1 terms][d0 rows], box b1 rows x d1 terms x 1, no swizzle.
+// box 128 x b1 rows. kind 1: activation terms, a 4-D uint8 tensor [d0 / 128 slabs][d2 terms]
+// [d1 rows][128], box 128 x b1 rows x d2 terms x b3 slabs. Both with the 128-byte swizzle of the
+// MMA operands. kind 2: activation scale words, a 3-D uint32 tensor [d2 slabs][d1 terms][d0 rows],
+// box b1 rows x d1 terms x b3 slabs, no swizzle.
 const CUtensorMap *get_map(int kind, const void *ptr, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t b1,
-                           moe_status_t *st)
+                           uint32_t b3, moe_status_t *st)
 {
     int dev = 0;
     cudaGetDevice(&dev);
-    MapKey key{dev, kind, ptr, d0, d1, d2, b1};
+    MapKey key{dev, kind, ptr, d0, d1, d2, b1, b3};
     std::lock_guard<std::mutex> lk(g_map_mu);
     auto it = g_maps.find(key);
     if (it != g_maps.end()) return &it->second.map;
@@ -78,7 +79,7 @@ const CUtensorMap *get_map(int kind, const void *ptr, uint64_t d0, uint64_t d1, 
     if (g_maps.size() > 4096) g_maps.clear();
     MapEntry ent;
     CUresult r;
-    cuuint32_t estr[3] = {1, 1, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
     if (kind == 0) {
         cuuint64_t dims[2] = {128, d1};
         cuuint64_t strides[1] = {64};
@@ -87,16 +88,16 @@ const CUtensorMap *get_map(int kind, const void *ptr, uint64_t d0, uint64_t d1, 
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     } else if (kind == 1) {
-        cuuint64_t dims[3] = {d0, d1, d2};
-        cuuint64_t strides[2] = {d0, d0 * d1};
-        cuuint32_t box[3] = {128, b1, (cuuint32_t)d2};
-        r = fn(&ent.map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(ptr), dims, strides, box, estr,
+        cuuint64_t dims[4] = {128, d1, d2, d0 / 128};
+        cuuint64_t strides[3] = {128, 128 * d1, 128 * d1 * d2};
+        cuuint32_t box[4] = {128, b1, (cuuint32_t)d2, b3};
+        r = fn(&ent.map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void *>(ptr), dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     } else {
         cuuint64_t dims[3] = {d0, d1, d2};
         cuuint64_t strides[2] = {d0 * 4, d0 * d1 * 4};
-        cuuint32_t box[3] = {b1, (cuuint32_t)d1, 1};
+        cuuint32_t box[3] = {b1, (cuuint32_t)d1, b3};
         r = fn(&ent.map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<void *>(ptr), dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -349,20 +350,22 @@ moe_status_t moe_mxfp4_forward_timed(const moe_layer_desc *d, const uint16_t *d_
     const uint8_t *w13 = a.packed, *w2 = a.packed + packed_w13_bytes(d->E, d->H, d->I);
     const uint64_t rows13 = (uint64_t)d->E * 2 * d->I * (d->H / KSLAB);   // 128-element rows of W13 nibbles
     const uint64_t rows2 = (uint64_t)d->E * d->H * (d->I / KSLAB);
-    if (!(a.tmap_w13 = get_map(0, w13, 128, rows13, 1, 128 * sps, &st))) return st;
-    if (!(a.tmap_w13_1 = get_map(0, w13, 128, rows13, 1, 128, &st))) return st;
-    if (!(a.tmap_w2 = get_map(0, w2, 128, rows2, 1, 128 * sps, &st))) return st;
-    if (!(a.tmap_w2_1 = get_map(0, w2, 128, rows2, 1, 128, &st))) return st;
-    if (!(a.tmap_xq = get_map(1, a.xq, (uint64_t)d->H, (uint64_t)R, NT_X, (uint32_t)regime_nmax(a.regime, 0), &st)))
-        return st;
-    if (!(a.tmap_hq = get_map(1, a.hq, (uint64_t)d->I, (uint64_t)R, NT_H, (uint32_t)regime_nmax(a.regime, 1), &st)))
-        return st;
-    if (!(a.tmap_xs = get_map(2, a.xs, (uint64_t)a.rows_sf, NT_X, (uint64_t)(d->H / KSLAB),
-                              (uint32_t)regime_nmax(a.regime, 0), &st)))
-        return st;
-    if (!(a.tmap_hs = get_map(2, a.hs, (uint64_t)a.rows_sf, NT_H, (uint64_t)(d->I / KSLAB),
-                              (uint32_t)regime_nmax(a.regime, 1), &st)))
-        return st;
+    if (!(a.tmap_w13 = get_map(0, w13, 128, rows13, 1, 128 * sps, 1, &st))) return st;
+    if (!(a.tmap_w13_1 = get_map(0, w13, 128, rows13, 1, 128, 1, &st))) return st;
+    if (!(a.tmap_w2 = get_map(0, w2, 128, rows2, 1, 128 * sps, 1, &st))) return st;
+    if (!(a.tmap_w2_1 = get_map(0, w2, 128, rows2, 1, 128, 1, &st))) return st;
+    const uint32_t n13 = (uint32_t)regime_nmax(a.regime, 0), n2 = (uint32_t)regime_nmax(a.regime, 1);
+    const uint64_t s13 = (uint64_t)(d->H / KSLAB), s2 = (uint64_t)(d->I / KSLAB);
+    // activation terms and their scale words: a whole stage (sps slabs) per box, and single-slab
+    // boxes for a stage that straddles two tiles
+    if (!(a.tmap_xq = get_map(1, a.xq, (uint64_t)d->H, (uint64_t)R, NT_X, n13, sps, &st))) return st;
+    if (!(a.tmap_xq1 = get_map(1, a.xq, (uint64_t)d->H, (uint64_t)R, NT_X, n13, 1, &st))) return st;
+    if (!(a.tmap_hq = get_map(1, a.hq, (uint64_t)d->I, (uint64_t)R, NT_H, n2, sps, &st))) return st;
+    if (!(a.tmap_hq1 = get_map(1, a.hq, (uint64_t)d->I, (uint64_t)R, NT_H, n2, 1, &st))) return st;
+    if (!(a.tmap_xs = get_map(2, a.xs, (uint64_t)a.rows_sf, NT_X, s13, n13, sps, &st))) return st;
+    if (!(a.tmap_xs1 = get_map(2, a.xs, (uint64_t)a.rows_sf, NT_X, s13, n13, 1, &st))) return st;
+    if (!(a.tmap_hs = get_map(2, a.hs, (uint64_t)a.rows_sf, NT_H, s2, n2, sps, &st))) return st;
+    if (!(a.tmap_hs1 = get_map(2, a.hs, (uint64_t)a.rows_sf, NT_H, s2, n2, 1, &st))) return st;
     if (cudaMemsetAsync(a.dev_error, 0, sizeof(int32_t), s) != cudaSuccess) return MOE_ERR_CUDA;
     return from_cuda(launch_forward(a, s));
 }

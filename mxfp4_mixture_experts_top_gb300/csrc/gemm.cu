@@ -97,8 +97,8 @@ static_assert(W13Large::NMAX == 96 && W2Large::NMAX == 64, "regime_nmax() mirror
 struct GemmParams {
     CUtensorMap tm_a;         // weight nibbles, box 128 x (128 * SPS) rows
     CUtensorMap tm_a1;        // weight nibbles, box 128 x 128 rows (a stage that straddles two tiles)
-    CUtensorMap tm_b;         // activation terms [NT][rows][K] bytes, box 128 x NMAX x NT
-    CUtensorMap tm_bs;        // activation scale words [K/128][NT][rows_sf] (uint32), box NMAX x NT x 1
+    CUtensorMap tm_b, tm_b1;  // activation terms [K/128][NT][rows][128] bytes, box 128 x NMAX x NT x (SPS | 1) slabs
+    CUtensorMap tm_bs, tm_bs1; // their scale words [K/128][NT][rows_sf] (uint32), box NMAX x NT x (SPS | 1)
     const uint8_t *wsf;       // this matrix's prepacked scale region
     const int32_t *offsets;   // [E+1]
     const int32_t *padded;    // [E+1]
@@ -107,7 +107,7 @@ struct GemmParams {
     int I, H, k;
     float swiglu_limit;
     int64_t P, rows_cap, rows_sf;
-    uint8_t *hq;              // W13 out: h terms [NT_H][rows_cap][I]
+    uint8_t *hq;              // W13 out: h terms [I/128][NT_H][rows_cap][128]
     uint8_t *hs;              // W13 out: h term scale words [I/128][NT_H][rows_sf], byte = K-block % 4
     float *staging;           // W2 out [P, H]
     int32_t *dev_error;
@@ -118,9 +118,11 @@ struct Smem {
     static constexpr int ASTAGE = C::SPS * SLAB_SMEM_BYTES;    // expanded E2M1 slabs
     static constexpr int BSLAB = C::NP * 128;                 // [term][row][128 K bytes]
     static constexpr int BSTAGE = C::SPS * BSLAB;
-    static constexpr int BSBYTES = C::NP * 4;                 // B scale words [term][row] of one slab
-    static constexpr int BSSLAB = (BSBYTES + 127) / 128 * 128; // TMA destinations stay 128-byte aligned
-    static constexpr int BSSTAGE = C::SPS * BSSLAB;
+    static constexpr int BSSLAB = C::NP * 4;                  // B scale words [term][row] of one slab
+    // a stage box writes its slabs' words back to back; a stage loaded slab by slab (across two
+    // tiles) puts slab 1 at the next 128-byte boundary (tensor-copy destinations are 128-byte aligned)
+    static constexpr int BSSLAB_PAD = (BSSLAB + 127) / 128 * 128;
+    static constexpr int BSSTAGE = ((C::SPS - 1) * BSSLAB_PAD + BSSLAB + 127) / 128 * 128;
     static constexpr int SFSTAGE = C::SPS * SLAB_SF_BYTES;
     static constexpr int A_OFF = 0;
     static constexpr int B_OFF = A_OFF + C::NA * ASTAGE;
@@ -339,6 +341,8 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_kernel(const __grid_co
         if (ptx::elect_one()) {
             ptx::prefetch_tmap(&p.tm_b);
             ptx::prefetch_tmap(&p.tm_bs);
+            ptx::prefetch_tmap(&p.tm_b1);
+            ptx::prefetch_tmap(&p.tm_bs1);
         }
         __syncwarp();
         int bi = 0;
@@ -350,17 +354,32 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_kernel(const __grid_co
         for (int i0 = 0; i0 < n_slabs; i0 += SPS) {
             if (!__all_sync(0xFFFFFFFFu, ptx::mbar_wait(&b_empty[bi], bph ^ 1u, s_abort, LIM))) { ok = false; break; }
             const int nsl = n_slabs - i0 < SPS ? n_slabs - i0 : SPS;
-            if (ptx::elect_one()) ptx::mbar_arrive_expect_tx(&b_full[bi], (uint32_t)(nsl * (S::BSLAB + S::BSBYTES)));
-            for (int pos = 0; pos < nsl; ++pos) {
+            if (ptx::elect_one()) ptx::mbar_arrive_expect_tx(&b_full[bi], (uint32_t)(nsl * (S::BSLAB + S::BSSLAB)));
+            if (nsl == SPS && ka + SPS <= slabs) {      // the stage's slabs in one box each for terms and scales
                 if (ptx::elect_one()) {
-                    ptx::tma_load_3d(bring + bi * S::BSTAGE + pos * S::BSLAB, &p.tm_b, ka * KSLAB, tl.row0, 0, &b_full[bi]);
-                    ptx::tma_load_3d(bsring + bi * S::BSSTAGE + pos * S::BSSLAB, &p.tm_bs, tl.row0, 0, ka, &b_full[bi]);
+                    ptx::tma_load_4d(bring + bi * S::BSTAGE, &p.tm_b, 0, tl.row0, 0, ka, &b_full[bi]);
+                    ptx::tma_load_3d(bsring + bi * S::BSSTAGE, &p.tm_bs, tl.row0, 0, ka, &b_full[bi]);
                 }
                 __syncwarp();
-                if (++ka == slabs) {
+                ka += SPS;
+                if (ka == slabs) {
                     ka = 0;
                     tcur += gridDim.x;
                     if (tcur < total) tl = decode_tile<C>(tcur, tile_start, E, MB, p.offsets, p.padded);
+                }
+            } else {                                    // last slab of a tile, or a stage across two tiles
+                for (int pos = 0; pos < nsl; ++pos) {
+                    if (ptx::elect_one()) {
+                        ptx::tma_load_4d(bring + bi * S::BSTAGE + pos * S::BSLAB, &p.tm_b1, 0, tl.row0, 0, ka, &b_full[bi]);
+                        ptx::tma_load_3d(bsring + bi * S::BSSTAGE + pos * S::BSSLAB_PAD, &p.tm_bs1, tl.row0, 0, ka,
+                                         &b_full[bi]);
+                    }
+                    __syncwarp();
+                    if (++ka == slabs) {
+                        ka = 0;
+                        tcur += gridDim.x;
+                        if (tcur < total) tl = decode_tile<C>(tcur, tile_start, E, MB, p.offsets, p.padded);
+                    }
                 }
             }
             ++issued;
@@ -387,9 +406,12 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_kernel(const __grid_co
                                              ptx::mbar_wait(&a_full[ai], aph, s_abort, LIM) &&
                                              ptx::mbar_wait(&b_full[bi], bph, s_abort, LIM))) { ok = false; break; }
             ptx::tc_fence_after();
+            // the activation producer's test: one box for the stage (slab words back to back) or one per slab
+            const bool whole = nsl == SPS && (i0 % slabs) + SPS <= slabs;
             for (int pos = 0; pos < nsl; ++pos) {
                 const uint4 aw = *reinterpret_cast<const uint4 *>(sfring + ai * S::SFSTAGE + pos * SLAB_SF_BYTES + lane * 16);
-                const uint32_t *bs = reinterpret_cast<const uint32_t *>(bsring + bi * S::BSSTAGE + pos * S::BSSLAB);
+                const uint32_t *bs = reinterpret_cast<const uint32_t *>(bsring + bi * S::BSSTAGE +
+                                                                        pos * (whole ? S::BSSLAB : S::BSSLAB_PAD));
                 const uint32_t cell = tmem + quarter + (uint32_t)(C::SF_BASE + sc * C::CELL_COLS + pos * C::SF_COLS);
                 ptx::tmem_st_32x32b_x4(cell, aw.x, aw.y, aw.z, aw.w);
 #pragma unroll
@@ -563,7 +585,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_kernel(const __grid_co
                             for (int term = 0; term < NT_H; ++term) {
                                 uint32_t sb;
                                 const uint32_t q = mxfp8_term1(r, e1, term, sb);
-                                p.hq[((int64_t)term * p.rows_cap + row) * p.I + f] = (uint8_t)q;
+                                p.hq[(((int64_t)(f >> 7) * NT_H + term) * p.rows_cap + row) * 128 + (f & 127)] = (uint8_t)q;
                                 if (writes_scale)
                                     p.hs[(((int64_t)(blk >> 2) * NT_H + term) * p.rows_sf + row) * 4 + (blk & 3)] = (uint8_t)sb;
                             }
@@ -598,11 +620,11 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_kernel(const __grid_co
 
 // Gathered activations as NT_X MXFP8 terms: row r of the permutation gets
 // the terms of x[token(r)], padding rows (row_to_pair == -1) get zeros. One
-// thread per (row, 32-element block). Terms are [NT_X][rows_cap][H] E4M3
-// bytes; scales are 32-bit words [H/128][NT_X][rows_sf], byte b % 4 of word
-// (b / 4, t, r) for 32-element block b (one TMA box then fetches a slab's
-// scales for all rows and terms of a tile). Rows past padded[E] are not
-// touched.
+// thread per (row, 32-element block). Terms are E4M3 bytes
+// [H/128][NT_X][rows_cap][128] (slab-major: one TMA box fetches the slabs of a
+// stage for all rows and terms of a tile); scales are 32-bit words
+// [H/128][NT_X][rows_sf], byte b % 4 of word (b / 4, t, r) for 32-element
+// block b. Rows past padded[E] are not touched.
 __global__ void gather_quant_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ row_to_pair,
                                     const int32_t *__restrict__ padded, int E, int H, int k, int64_t P,
                                     int64_t rows_cap, int64_t rows_sf, uint8_t *__restrict__ xq,
@@ -646,7 +668,7 @@ __global__ void gather_quant_kernel(const uint16_t *__restrict__ x, const int32_
                 const uint32_t hi = mxfp8_term_pair(v[4 * q + 2], v[4 * q + 3], e1, t, sbyte);
                 wq[q] = lo | (hi << 16);
             }
-            uint4 *dst = reinterpret_cast<uint4 *>(xq + ((int64_t)t * rows_cap + r) * H + b * 32);
+            uint4 *dst = reinterpret_cast<uint4 *>(xq + (((int64_t)(b >> 2) * NT_X + t) * rows_cap + r) * 128 + (b & 3) * 32);
             dst[0] = make_uint4(wq[0], wq[1], wq[2], wq[3]);
             dst[1] = make_uint4(wq[4], wq[5], wq[6], wq[7]);
             xs[(((int64_t)(b >> 2) * NT_X + t) * rows_sf + r) * 4 + (b & 3)] = (uint8_t)sbyte;
@@ -757,7 +779,9 @@ cudaError_t launch_forward(const ForwardArgs &a, cudaStream_t s)
     g.tm_a = *a.tmap_w13;
     g.tm_a1 = *a.tmap_w13_1;
     g.tm_b = *a.tmap_xq;
+    g.tm_b1 = *a.tmap_xq1;
     g.tm_bs = *a.tmap_xs;
+    g.tm_bs1 = *a.tmap_xs1;
     g.wsf = a.packed + (size_t)a.E * 2 * a.I * (a.H / 2);
     g.K = a.H;
     g.MB = a.I / 64;
@@ -773,7 +797,9 @@ cudaError_t launch_forward(const ForwardArgs &a, cudaStream_t s)
     g.tm_a = *a.tmap_w2;
     g.tm_a1 = *a.tmap_w2_1;
     g.tm_b = *a.tmap_hq;
+    g.tm_b1 = *a.tmap_hq1;
     g.tm_bs = *a.tmap_hs;
+    g.tm_bs1 = *a.tmap_hs1;
     g.wsf = a.packed + packed_w13_bytes(a.E, a.H, a.I) + (size_t)a.E * a.H * (a.I / 2);
     g.K = a.I;
     g.MB = a.H / TILE_ROWS;

@@ -64,12 +64,12 @@ struct ForwardArgs {
     const int32_t *offsets, *padded, *row_to_pair;
     float *y;
     int32_t *dev_error;
-    uint8_t *xq, *xs;      // x terms [NT_X][rows_cap][H], scale words [H/128][NT_X][rows_sf]
-    uint8_t *hq, *hs;      // h terms [NT_H][rows_cap][I], scale words [I/128][NT_H][rows_sf]
+    uint8_t *xq, *xs;      // x terms [H/128][NT_X][rows_cap][128], scale words [H/128][NT_X][rows_sf]
+    uint8_t *hq, *hs;      // h terms [I/128][NT_H][rows_cap][128], scale words [I/128][NT_H][rows_sf]
     float *staging;
     const CUtensorMap *tmap_w13, *tmap_w13_1, *tmap_w2, *tmap_w2_1;   // weight nibbles: stage / single-slab boxes
-    const CUtensorMap *tmap_xq, *tmap_hq;                            // activation terms
-    const CUtensorMap *tmap_xs, *tmap_hs;                            // their scale words
+    const CUtensorMap *tmap_xq, *tmap_xq1, *tmap_hq, *tmap_hq1;      // activation terms: stage / one-slab boxes
+    const CUtensorMap *tmap_xs, *tmap_xs1, *tmap_hs, *tmap_hs1;      // their scale words
     Regime regime;
     int num_sms;
     void *const *events;   // optional: 5 cudaEvent_t recorded between kernels

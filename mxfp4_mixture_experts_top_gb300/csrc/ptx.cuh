@@ -154,6 +154,17 @@ __device__ __forceinline__ void tma_load_3d(void *smem_dst, const void *tmap, in
         : "memory");
 }
 
+// 4-D tiled tensor load at element coords (x, y, z, w).
+__device__ __forceinline__ void tma_load_4d(void *smem_dst, const void *tmap, int32_t x, int32_t y, int32_t z, int32_t w,
+                                            uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5}], [%6];"
+        ::"r"(smem_u32(smem_dst)), "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_u32(bar))
+        : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tmap(const void *tmap)
 {
     asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");

@@ -119,10 +119,10 @@ def _e4m3_values():
 
 def _terms(ws, off_q, off_s, nt, R, K):
     """Sum of the MXFP8 terms stored at (off_q, off_s): value[row, k]. Terms are E4M3 bytes
-    [nt][R][K]; scales are 32-bit words [K/128][nt][RS] (RS = R rounded up to 4) whose byte b
-    holds the E8M0 scale of 32-element block 4 * slab + b."""
+    [K/128][nt][R][128] (slab-major); scales are 32-bit words [K/128][nt][RS] (RS = R rounded
+    up to 4) whose byte b holds the E8M0 scale of 32-element block 4 * slab + b."""
     RS = (R + 3) // 4 * 4
-    q = ws[off_q:off_q + nt * R * K].cpu().numpy().reshape(nt, R, K)
+    q = ws[off_q:off_q + nt * R * K].cpu().numpy().reshape(K // 128, nt, R, 128).transpose(1, 2, 0, 3).reshape(nt, R, K)
     sw = ws[off_s:off_s + (K // 128) * nt * RS * 4].cpu().numpy().reshape(K // 128, nt, RS, 4)
     sc = sw.transpose(1, 2, 0, 3).reshape(nt, RS, K // 32)[:, :R].astype(int)
     v = _e4m3_values()[q] * np.ldexp(1.0, np.repeat(sc, 32, axis=2) - 127)
