@@ -25,7 +25,11 @@
  *     stream). All work is enqueued on that stream only; no call
  *     synchronises the device or copies between host and device (except
  *     moe_read_device_error), so route/permute/forward can be captured in a
- *     CUDA graph.
+ *     CUDA graph. Kernels after the first of a call (and the first kernel of
+ *     moe_mxfp4_forward / moe_permute) are launched with programmatic stream
+ *     serialization: each may start while the kernel before it on the stream
+ *     finishes, and reads or writes nothing that earlier work touches before
+ *     that earlier work has completed (griddepcontrol.wait).
  *   - Argument errors are detected on the host before any launch and return
  *     MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED / MOE_ERR_MISALIGNED /
  *     MOE_ERR_WORKSPACE. A failed launch returns MOE_ERR_CUDA. Faults found on
@@ -200,7 +204,8 @@ size_t moe_mxfp4_workspace_bytes(const moe_layer_desc *desc);
  * more than 2^17), SiLU(gate)*up in 3 terms (about 12 significant bits);
  * fp32 accumulation; output fp32. Result within 2e-2 * rms of the float64
  * oracle (measured errors are about 1e-4 * rms).
- * Launches 4 kernels on `stream`; deterministic (bit-identical reruns).
+ * Launches 4 kernels on `stream`; deterministic (bit-identical reruns). The
+ * GEMMs stream their weights before the kernel ahead of them has finished.
  */
 moe_status_t moe_mxfp4_forward(const moe_layer_desc *desc, const uint16_t *d_x,
                                const void *d_packed, const float *d_topk_w,
@@ -212,7 +217,9 @@ moe_status_t moe_mxfp4_forward(const moe_layer_desc *desc, const uint16_t *d_x,
  * moe_mxfp4_forward with timing: identical work, plus cudaEventRecord of
  * events[0..4] (cudaEvent_t passed as void*, created by the caller on this
  * device) on `stream` before the gather, after the gather, after the W13 GEMM,
- * after the W2 GEMM and after the combine. NULL entries are skipped.
+ * after the W2 GEMM and after the combine. NULL entries are skipped. With any
+ * event given, the kernels run one after another without overlap, so each
+ * interval is one kernel's time.
  */
 moe_status_t moe_mxfp4_forward_timed(const moe_layer_desc *desc, const uint16_t *d_x,
                                      const void *d_packed, const float *d_topk_w,

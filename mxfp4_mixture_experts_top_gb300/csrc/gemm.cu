@@ -239,7 +239,10 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_kernel(const __grid_co
         __syncthreads();
     }
     const int total = tile_start[E];
-    if ((int)blockIdx.x >= total) return;     // uniform: this CTA has no tiles
+    if ((int)blockIdx.x >= total) {           // uniform: this CTA has no tiles
+        griddep_wait();
+        return;
+    }
 
     // ---- barriers and TMEM
     if (tid == 0) {
@@ -344,6 +347,11 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_kernel(const __grid_co
             ptx::prefetch_tmap(&p.tm_b1);
             ptx::prefetch_tmap(&p.tm_bs1);
         }
+        // The activation terms come from the kernel before (gather, or W13 for W2): under
+        // programmatic dependent launch everything above, and the weight producer's stream, may
+        // run while that kernel finishes; this warp waits for it before its first copy.
+        griddep_wait();
+        if (lane == 0) griddep_launch_dependents();
         __syncwarp();
         int bi = 0;
         uint32_t bph = 0;
@@ -630,6 +638,8 @@ __global__ void gather_quant_kernel(const uint16_t *__restrict__ x, const int32_
                                     int64_t rows_cap, int64_t rows_sf, uint8_t *__restrict__ xq,
                                     uint8_t *__restrict__ xs, int32_t *dev_error)
 {
+    griddep_wait();                  // the permutation (and x) come from earlier kernels
+    griddep_launch_dependents();
     const int64_t R = __ldg(padded + E);
     const int nblk = H / 32;
     const int64_t n = R * nblk;
@@ -680,6 +690,7 @@ __global__ void gather_quant_kernel(const uint16_t *__restrict__ x, const int32_
 __global__ void combine_kernel(const float *__restrict__ staging, const float *__restrict__ w, int T, int H,
                                int k, float *__restrict__ y)
 {
+    griddep_wait();                  // staging comes from the W2 GEMM
     const int vec = H / 4;
     const int64_t n = (int64_t)T * vec;
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
@@ -699,7 +710,7 @@ __global__ void combine_kernel(const float *__restrict__ staging, const float *_
 }
 
 template <class C>
-cudaError_t launch_gemm(const GemmParams &p, int grid, cudaStream_t s)
+cudaError_t launch_gemm(const GemmParams &p, int grid, cudaStream_t s, bool pdl)
 {
     static unsigned long long attr_set = 0;   // bit d: attribute set on device d
     const size_t smem = Smem<C>::bytes(p.E);
@@ -711,8 +722,7 @@ cudaError_t launch_gemm(const GemmParams &p, int grid, cudaStream_t s)
         if (e != cudaSuccess) return e;
         if (dev < 64) __atomic_fetch_or(&attr_set, 1ull << dev, __ATOMIC_RELAXED);
     }
-    moe_gemm_kernel<C><<<grid, C::THREADS, smem, s>>>(p);
-    return cudaGetLastError();
+    return launch_ex(moe_gemm_kernel<C>, dim3(grid), dim3(C::THREADS), smem, s, pdl, p);
 }
 
 }  // namespace
@@ -747,15 +757,20 @@ cudaError_t launch_forward(const ForwardArgs &a, cudaStream_t s)
 {
     const int64_t P = (int64_t)a.T * a.k;
     cudaError_t err;
+    // Kernels after the first overlap their start with the end of the one before (programmatic
+    // dependent launch), except when events are recorded between them to time each kernel alone.
+    bool pdl = true;
+    for (int i = 0; i < 5 && a.events; ++i)
+        if (a.events[i]) pdl = false;
     mark(a, 0, s);
     {
         const int64_t n = a.rows_cap * (a.H / 32);
         int grid = (int)((n + 255) / 256);
         if (grid > 8 * 1024) grid = 8 * 1024;
         if (grid < 1) grid = 1;
-        gather_quant_kernel<<<grid, 256, 0, s>>>(a.x, a.row_to_pair, a.padded, a.E, a.H, a.k, P, a.rows_cap,
-                                                 a.rows_sf, a.xq, a.xs, a.dev_error);
-        if ((err = cudaGetLastError()) != cudaSuccess) return err;
+        err = launch_ex(gather_quant_kernel, dim3(grid), dim3(256), 0, s, pdl, a.x, a.row_to_pair, a.padded, a.E,
+                        a.H, a.k, P, a.rows_cap, a.rows_sf, a.xq, a.xs, a.dev_error);
+        if (err != cudaSuccess) return err;
     }
     mark(a, 1, s);
     GemmParams g{};
@@ -786,10 +801,10 @@ cudaError_t launch_forward(const ForwardArgs &a, cudaStream_t s)
     g.K = a.H;
     g.MB = a.I / 64;
     const Regime rg = a.regime;
-    err = rg == Regime::Tiny  ? launch_gemm<W13Tiny>(g, a.num_sms, s)
-        : rg == Regime::Small ? launch_gemm<W13Small>(g, a.num_sms, s)
-        : rg == Regime::Mid   ? launch_gemm<W13Mid>(g, a.num_sms, s)
-                              : launch_gemm<W13Large>(g, a.num_sms, s);
+    err = rg == Regime::Tiny  ? launch_gemm<W13Tiny>(g, a.num_sms, s, pdl)
+        : rg == Regime::Small ? launch_gemm<W13Small>(g, a.num_sms, s, pdl)
+        : rg == Regime::Mid   ? launch_gemm<W13Mid>(g, a.num_sms, s, pdl)
+                              : launch_gemm<W13Large>(g, a.num_sms, s, pdl);
     if (err != cudaSuccess) return err;
     mark(a, 2, s);
 
@@ -803,10 +818,10 @@ cudaError_t launch_forward(const ForwardArgs &a, cudaStream_t s)
     g.wsf = a.packed + packed_w13_bytes(a.E, a.H, a.I) + (size_t)a.E * a.H * (a.I / 2);
     g.K = a.I;
     g.MB = a.H / TILE_ROWS;
-    err = rg == Regime::Tiny  ? launch_gemm<W2Tiny>(g, a.num_sms, s)
-        : rg == Regime::Small ? launch_gemm<W2Small>(g, a.num_sms, s)
-        : rg == Regime::Mid   ? launch_gemm<W2Mid>(g, a.num_sms, s)
-                              : launch_gemm<W2Large>(g, a.num_sms, s);
+    err = rg == Regime::Tiny  ? launch_gemm<W2Tiny>(g, a.num_sms, s, pdl)
+        : rg == Regime::Small ? launch_gemm<W2Small>(g, a.num_sms, s, pdl)
+        : rg == Regime::Mid   ? launch_gemm<W2Mid>(g, a.num_sms, s, pdl)
+                              : launch_gemm<W2Large>(g, a.num_sms, s, pdl);
     if (err != cudaSuccess) return err;
     mark(a, 3, s);
 
@@ -815,8 +830,9 @@ cudaError_t launch_forward(const ForwardArgs &a, cudaStream_t s)
         int grid = (int)((n + 255) / 256);
         if (grid > 4 * 1024) grid = 4 * 1024;
         if (grid < 1) grid = 1;
-        combine_kernel<<<grid, 256, 0, s>>>(a.staging, a.topk_w, a.T, a.H, a.k, a.y);
-        if ((err = cudaGetLastError()) != cudaSuccess) return err;
+        err = launch_ex(combine_kernel, dim3(grid), dim3(256), 0, s, pdl, (const float *)a.staging, a.topk_w, a.T,
+                        a.H, a.k, a.y);
+        if (err != cudaSuccess) return err;
     }
     mark(a, 4, s);
     note_launch(4);

@@ -24,6 +24,35 @@ Regime pick_regime(int T, int k, int E);
 int regime_nmax(Regime rg, int which);   // token rows per tile; which 0: W13, 1: W2
 int regime_sps(Regime rg);               // K-slabs per weight stage
 
+// Programmatic dependent launch. A kernel launched with `pdl` may start while
+// the previous kernel of the stream still runs. Before it reads or writes
+// anything that kernel, or any earlier work, produces or reads, it executes
+// griddep_wait(), which returns once the earlier grids have completed and
+// their memory is visible. A kernel signals griddep_launch_dependents() only
+// after its own griddep_wait(), so the part of a kernel that runs before its
+// wait overlaps the one kernel before it, never an earlier one.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_ex(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl,
+                             Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
+#ifdef __CUDACC__
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+#endif
+
 // Bounded pipeline waits give up after this much wall time.
 constexpr unsigned long long WAIT_LIMIT_NS = 2000000000ull;   // 2 s
 

@@ -157,6 +157,8 @@ permute_kernel(const int32_t *__restrict__ ids, int T, int E, int k, int block_m
                int32_t *__restrict__ row_to_pair, int64_t rows_cap, int32_t *__restrict__ pair_to_row,
                int32_t *__restrict__ dev_error)
 {
+    griddep_wait();                   // ids come from the kernel before (launched with pdl)
+    griddep_launch_dependents();
     permute_block(ids, T, E, k, block_m, counts, offsets, padded, row_to_pair, rows_cap, pair_to_row, dev_error);
 }
 
@@ -169,6 +171,8 @@ route_permute_kernel(const float *__restrict__ logits, int T, int E, int k, int 
                      int32_t *__restrict__ offsets, int32_t *__restrict__ padded, int32_t *__restrict__ row_to_pair,
                      int64_t rows_cap, int32_t *__restrict__ pair_to_row, int32_t *__restrict__ dev_error)
 {
+    // the gather launched next (with pdl) only waits on this grid, so it may start now
+    griddep_launch_dependents();
     for (int t = threadIdx.x >> 5; t < T; t += PERM_WARPS) route_token<VPL>(logits, t, E, k, ids, w, bitmatrix);
     __syncthreads();          // the ids written above are visible to the whole block
     permute_block(ids, T, E, k, block_m, counts, offsets, padded, row_to_pair, rows_cap, pair_to_row, dev_error);
@@ -222,10 +226,10 @@ cudaError_t launch_permute(const int32_t *ids, int T, int E, int k, int block_m,
     size_t smem = permute_smem(E);
     cudaError_t err = cudaFuncSetAttribute(permute_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
-    permute_kernel<<<1, PERM_THREADS, smem, s>>>(ids, T, E, k, block_m, counts, offsets, padded, row_to_pair,
-                                                 rows_cap, pair_to_row, dev_error);
+    err = launch_ex(permute_kernel, dim3(1), dim3(PERM_THREADS), smem, s, true, ids, T, E, k, block_m, counts,
+                    offsets, padded, row_to_pair, rows_cap, pair_to_row, dev_error);
     note_launch(1);
-    return cudaGetLastError();
+    return err;
 }
 
 }  // namespace moe

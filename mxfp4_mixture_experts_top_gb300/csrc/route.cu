@@ -12,6 +12,7 @@ __global__ void __launch_bounds__(256) route_kernel(const float *__restrict__ lo
                                                      int32_t *__restrict__ ids, float *__restrict__ w,
                                                      uint32_t *__restrict__ bitmatrix)
 {
+    griddep_launch_dependents();      // the permutation launched next waits for this grid's ids
     const int warps = blockDim.x >> 5;
     const int t = blockIdx.x * warps + (threadIdx.x >> 5);
     if (t >= T) return;
