@@ -73,6 +73,11 @@ struct Cfg {
     static constexpr int D_COLS = NACC * NP;                   // one accumulator set
     static constexpr int SF_BASE = 2 * MW * D_COLS;            // [MMA warp][double buffer][set]
     static constexpr int THREADS = 352 + 32 * (MW - 1);
+    // Stage s's MMAs complete -> done[s % ND]: frees the stage in the weight, activation and scale-factor
+    // rings at once. A waiter for stage s - N (N = NA, NB or NSF) cannot see the barrier a full lap
+    // ahead, since that needs stage s - N + ND >= s, which it has not filled yet.
+    static constexpr int ND = 8;
+    static_assert(NA <= ND && NB <= ND && NSF <= ND, "done ring");
     static_assert(NP % 16 == 0 && NP <= 256, "MMA N");
     static_assert(NMAX % 16 == 0, "token rows per tile");
     static_assert(SF_BASE + NSF * CELL_COLS <= TMEM_COLS, "TMEM budget");
@@ -129,7 +134,7 @@ struct Smem {
     static constexpr int SF_OFF = B_OFF + C::NB * BSTAGE;
     static constexpr int BS_OFF = SF_OFF + C::NA * SFSTAGE;
     static constexpr int BAR_OFF = BS_OFF + C::NB * BSSTAGE;
-    static constexpr int NBARS = 2 * C::NA + 2 * C::NB + 2 * C::NSF + 2 * 2 + 1;
+    static constexpr int NBARS = C::NA + C::NB + C::NSF + C::ND + 2 * 2 + 1;
     static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;
     static constexpr int PAIRMAX_OFF = MISC_OFF + 16;         // W13 epilogue: [2 buffers][4 warps][16] floats
     static constexpr int PREFIX_OFF = PAIRMAX_OFF + 2 * 4 * 16 * 4;
@@ -185,10 +190,9 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_kernel(const __grid_co
     uint8_t *sfring = smem + S::SF_OFF;
     uint8_t *bsring = smem + S::BS_OFF;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + S::BAR_OFF);
-    uint64_t *a_full = bars, *a_empty = a_full + C::NA;
-    uint64_t *b_full = a_empty + C::NA, *b_empty = b_full + C::NB;
-    uint64_t *sf_full = b_empty + C::NB, *sf_empty = sf_full + C::NSF;
-    uint64_t *d_full = sf_empty + C::NSF, *d_empty = d_full + 2;
+    uint64_t *a_full = bars, *b_full = a_full + C::NA, *sf_full = b_full + C::NB;
+    uint64_t *done = sf_full + C::NSF;
+    uint64_t *d_full = done + C::ND, *d_empty = d_full + 2;
     uint64_t *mma_done = d_empty + 2;
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(smem + S::MISC_OFF);
     volatile int *s_abort = reinterpret_cast<volatile int *>(smem + S::MISC_OFF + 4);
@@ -246,9 +250,10 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_kernel(const __grid_co
 
     // ---- barriers and TMEM
     if (tid == 0) {
-        for (int i = 0; i < C::NA; ++i) { ptx::mbar_init(&a_full[i], 1); ptx::mbar_init(&a_empty[i], 1); }
-        for (int i = 0; i < C::NB; ++i) { ptx::mbar_init(&b_full[i], 1); ptx::mbar_init(&b_empty[i], 1); }
-        for (int i = 0; i < C::NSF; ++i) { ptx::mbar_init(&sf_full[i], 4); ptx::mbar_init(&sf_empty[i], 1); }
+        for (int i = 0; i < C::NA; ++i) ptx::mbar_init(&a_full[i], 1);
+        for (int i = 0; i < C::NB; ++i) ptx::mbar_init(&b_full[i], 1);
+        for (int i = 0; i < C::NSF; ++i) ptx::mbar_init(&sf_full[i], 4);
+        for (int i = 0; i < C::ND; ++i) ptx::mbar_init(&done[i], 1);
         for (int i = 0; i < 2; ++i) {
             ptx::mbar_init(&d_full[i], C::MW);    // one commit per MMA warp and tile
             ptx::mbar_init(&d_empty[i], 4);
@@ -276,6 +281,10 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_kernel(const __grid_co
         *s_abort = 1;
         record_error(p.dev_error, DEV_ERR_TIMEOUT);
     };
+    // stage q (counted over this CTA's stages) has been consumed by its MMAs; nothing to wait for if q < 0
+    auto wait_done = [&](int q) -> bool {
+        return q < 0 || ptx::mbar_wait(&done[q % C::ND], (uint32_t)((q / C::ND) & 1), s_abort, LIM);
+    };
     // first 128-element row of (tile, slab) in the 2-D view of the nibble region
     auto a_row = [&](const Tile &tl, int ka) { return ((tl.e * MB + tl.mb) * slabs + ka) * TILE_ROWS; };
 
@@ -295,7 +304,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_kernel(const __grid_co
         int tcur = blockIdx.x, ka = 0;
         Tile tl = decode_tile<C>(tcur, tile_start, E, MB, p.offsets, p.padded);
         for (int i0 = 0; i0 < n_slabs; i0 += SPS) {
-            if (!__all_sync(0xFFFFFFFFu, ptx::mbar_wait(&a_empty[ai], aph ^ 1u, s_abort, LIM))) { ok = false; break; }
+            if (!__all_sync(0xFFFFFFFFu, wait_done(i0 / SPS - C::NA))) { ok = false; break; }
             const int nsl = n_slabs - i0 < SPS ? n_slabs - i0 : SPS;
             if (ptx::elect_one()) {
                 uint8_t *dst = aring + ai * S::ASTAGE;
@@ -360,7 +369,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_kernel(const __grid_co
         int tcur = blockIdx.x, ka = 0;
         Tile tl = decode_tile<C>(tcur, tile_start, E, MB, p.offsets, p.padded);
         for (int i0 = 0; i0 < n_slabs; i0 += SPS) {
-            if (!__all_sync(0xFFFFFFFFu, ptx::mbar_wait(&b_empty[bi], bph ^ 1u, s_abort, LIM))) { ok = false; break; }
+            if (!__all_sync(0xFFFFFFFFu, wait_done(i0 / SPS - C::NB))) { ok = false; break; }
             const int nsl = n_slabs - i0 < SPS ? n_slabs - i0 : SPS;
             if (ptx::elect_one()) ptx::mbar_arrive_expect_tx(&b_full[bi], (uint32_t)(nsl * (S::BSLAB + S::BSSLAB)));
             if (nsl == SPS && ka + SPS <= slabs) {      // the stage's slabs in one box each for terms and scales
@@ -405,12 +414,12 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_kernel(const __grid_co
         // next TMEM cell, in this warp's lane quarter; lane r of every quarter holds rows r, r + 32,
         // ... in consecutive columns.
         int ai = 0, bi = 0, sc = 0;
-        uint32_t aph = 0, bph = 0, sph = 0;
+        uint32_t aph = 0, bph = 0;
         bool ok = true;
         const uint32_t quarter = (uint32_t)((warp & 3) * 32) << 16;
         for (int i0 = 0; i0 < n_slabs; i0 += SPS) {
             const int nsl = n_slabs - i0 < SPS ? n_slabs - i0 : SPS;
-            if (!__all_sync(0xFFFFFFFFu, ptx::mbar_wait(&sf_empty[sc], sph ^ 1u, s_abort, LIM) &&
+            if (!__all_sync(0xFFFFFFFFu, wait_done(i0 / SPS - C::NSF) &&
                                              ptx::mbar_wait(&a_full[ai], aph, s_abort, LIM) &&
                                              ptx::mbar_wait(&b_full[bi], bph, s_abort, LIM))) { ok = false; break; }
             ptx::tc_fence_after();
@@ -434,75 +443,96 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_kernel(const __grid_co
             if (lane == 0) ptx::mbar_arrive(&sf_full[sc]);
             if (++ai == C::NA) { ai = 0; aph ^= 1u; }
             if (++bi == C::NB) { bi = 0; bph ^= 1u; }
-            if (++sc == C::NSF) { sc = 0; sph ^= 1u; }
+            if (++sc == C::NSF) sc = 0;
         }
         if (!ok && lane == 0) fail();
     } else if (warp == 8 || (C::MW == 2 && warp == 11)) {
-        // ===================== MMA issuers: stage s belongs to warp s % MW, which waits for it, issues
-        // its four block-scaled MMAs (K = 32 each) per slab into the warp's own accumulator set and
-        // frees it. Both warps walk every slab to follow the tiles: at each tile's start a warp waits
+        // ===================== MMA issuers: stage s belongs to warp s % MW. The warp waits for the stage's
+        // scale-factor cell only: the copiers fill it after the stage's weights and activations have
+        // landed, so that one wait covers all three. One elected lane issues the stage's block-scaled MMAs
+        // (four of K = 32 per slab) into the warp's own accumulator set and commits the stage to
+        // done[s % ND]. Both warps walk every stage to follow the tiles: at a tile's start a warp waits
         // for the tile's accumulator buffer to be free, at its end it commits the tile (with or without
         // MMAs of its own in it), so the epilogue sees one arrival per warp and tile.
         const int q = warp == 8 ? 0 : 1;
         const uint64_t adesc0 = ptx::smem_desc_sw128(ptx::smem_u32(aring));
         const uint64_t bdesc0 = ptx::smem_desc_sw128(ptx::smem_u32(bring));
         int ai = 0, bi = 0, sc = 0, di = 0, ka = 0, st = 0, mine_in_tile = 0;
-        uint32_t aph = 0, bph = 0, sph = 0, dph = 0;
-        bool ok = true, issued = false;
+        uint32_t sph = 0, dph = 0;
+        bool ok = true;
+        // the four MMAs of slab `pos` of the current stage; kk0: this warp's 32-K blocks in the tile so far
+        auto issue_slab = [&](int pos, int kk0) {
+            const uint64_t ad = adesc0 + (uint64_t)((uint32_t)(ai * S::ASTAGE + pos * SLAB_SMEM_BYTES) >> 4);
+            const uint64_t bd = bdesc0 + (uint64_t)((uint32_t)(bi * S::BSTAGE + pos * S::BSLAB) >> 4);
+            const uint32_t sfa = tmem + (uint32_t)(C::SF_BASE + sc * C::CELL_COLS + pos * C::SF_COLS);
+            const uint32_t dt0 = tmem + (uint32_t)((q * 2 + di) * C::D_COLS);
+#pragma unroll
+            for (int kb = 0; kb < 4; ++kb) {
+                const int kk = kk0 + kb;
+                // overwrite on the first use of each accumulator in the tile
+                ptx::mma_mx_ss(dt0 + (uint32_t)((kk % C::NACC) * NP), ad + (uint64_t)(kb * 2), bd + (uint64_t)(kb * 2),
+                               ptx::idesc_mx_e2m1_e4m3(128, NP, (uint32_t)kb), sfa, sfa + 4, kk >= C::NACC ? 1u : 0u);
+            }
+        };
+        auto tile_start = [&]() -> bool {     // the tile's accumulators must be free
+            if (!__all_sync(0xFFFFFFFFu, ptx::mbar_wait(&d_empty[di], dph ^ 1u, s_abort, LIM))) return false;
+            ptx::tc_fence_after();
+            mine_in_tile = 0;
+            return true;
+        };
+        auto next_tile = [&]() {
+            ka = 0;
+            if (++di == 2) { di = 0; dph ^= 1u; }
+        };
         for (int i0 = 0; i0 < n_slabs && ok; i0 += SPS, ++st) {
             const int nsl = n_slabs - i0 < SPS ? n_slabs - i0 : SPS;
             const bool mine = (st % C::MW) == q;
             if (mine) {
-                if (!__all_sync(0xFFFFFFFFu, ptx::mbar_wait(&sf_full[sc], sph, s_abort, LIM) &&
-                                                 ptx::mbar_wait(&a_full[ai], aph, s_abort, LIM) &&
-                                                 ptx::mbar_wait(&b_full[bi], bph, s_abort, LIM))) { ok = false; break; }
+                if (!__all_sync(0xFFFFFFFFu, ptx::mbar_wait(&sf_full[sc], sph, s_abort, LIM))) { ok = false; break; }
                 ptx::tc_fence_after();
             }
-            for (int pos = 0; pos < nsl; ++pos) {
-                if (ka == 0) {                        // a tile starts: its accumulators must be free
-                    if (!__all_sync(0xFFFFFFFFu, ptx::mbar_wait(&d_empty[di], dph ^ 1u, s_abort, LIM))) { ok = false; break; }
-                    ptx::tc_fence_after();
-                    mine_in_tile = 0;
-                }
-                if (mine) {
+            if (ka + nsl <= slabs) {
+                // the stage lies in one tile: one elected block for its MMAs and commits
+                if (ka == 0 && !tile_start()) { ok = false; break; }
+                const bool tile_end = ka + nsl == slabs;
+                if (mine || tile_end) {
                     if (ptx::elect_one()) {
-                        const uint64_t ad = adesc0 + (uint64_t)((uint32_t)(ai * S::ASTAGE + pos * SLAB_SMEM_BYTES) >> 4);
-                        const uint64_t bd = bdesc0 + (uint64_t)((uint32_t)(bi * S::BSTAGE + pos * S::BSLAB) >> 4);
-                        const uint32_t sfa = tmem + (uint32_t)(C::SF_BASE + sc * C::CELL_COLS + pos * C::SF_COLS);
-                        const uint32_t dt0 = tmem + (uint32_t)((q * 2 + di) * C::D_COLS);
+                        if (mine) {
 #pragma unroll
-                        for (int kb = 0; kb < 4; ++kb) {
-                            const int kk = mine_in_tile + kb;    // this warp's 32-K blocks in the tile so far
-                            // overwrite on the first use of each accumulator in the tile
-                            ptx::mma_mx_ss(dt0 + (uint32_t)((kk % C::NACC) * NP), ad + (uint64_t)(kb * 2),
-                                           bd + (uint64_t)(kb * 2), ptx::idesc_mx_e2m1_e4m3(128, NP, (uint32_t)kb),
-                                           sfa, sfa + 4, kk >= C::NACC ? 1u : 0u);
+                            for (int pos = 0; pos < SPS; ++pos)
+                                if (pos < nsl) issue_slab(pos, mine_in_tile + 4 * pos);
+                            ptx::mma_commit(&done[st % C::ND]);
                         }
+                        if (tile_end) ptx::mma_commit(&d_full[di]);
                     }
                     __syncwarp();
-                    mine_in_tile += 4;
-                    issued = true;
                 }
-                if (ka == slabs - 1) {                // the tile ends: one commit per warp
-                    if (ptx::elect_one()) ptx::mma_commit(&d_full[di]);
+                if (mine) mine_in_tile += 4 * nsl;
+                ka += nsl;
+                if (ka == slabs) next_tile();
+            } else {
+                // the stage crosses into the next tile: slab by slab
+                for (int pos = 0; pos < nsl; ++pos) {
+                    if (ka == 0 && !tile_start()) { ok = false; break; }
+                    const bool tile_end = ka == slabs - 1;
+                    if (mine || tile_end) {
+                        if (ptx::elect_one()) {
+                            if (mine) issue_slab(pos, mine_in_tile);
+                            if (tile_end) ptx::mma_commit(&d_full[di]);
+                        }
+                        __syncwarp();
+                    }
+                    if (mine) mine_in_tile += 4;
+                    if (++ka == slabs) next_tile();
+                }
+                if (!ok) break;
+                if (mine) {
+                    if (ptx::elect_one()) ptx::mma_commit(&done[st % C::ND]);
                     __syncwarp();
                 }
-                if (++ka == slabs) {
-                    ka = 0;
-                    if (++di == 2) { di = 0; dph ^= 1u; }
-                }
             }
-            if (!ok) break;
-            if (mine) {
-                if (ptx::elect_one()) {
-                    ptx::mma_commit(&sf_empty[sc]);
-                    ptx::mma_commit(&a_empty[ai]);
-                    ptx::mma_commit(&b_empty[bi]);
-                }
-                __syncwarp();
-            }
-            if (++ai == C::NA) { ai = 0; aph ^= 1u; }
-            if (++bi == C::NB) { bi = 0; bph ^= 1u; }
+            if (++ai == C::NA) ai = 0;
+            if (++bi == C::NB) bi = 0;
             if (++sc == C::NSF) { sc = 0; sph ^= 1u; }
         }
         if (!ok && lane == 0) fail();
@@ -511,7 +541,6 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_kernel(const __grid_co
         if (ptx::elect_one()) ptx::mma_commit(mma_done);
         __syncwarp();
         if (q == 0) __all_sync(0xFFFFFFFFu, ptx::mbar_wait(mma_done, 0, &never, LIM));
-        (void)issued;
     } else if (warp < 4) {
         // ===================== epilogue: TMEM -> registers -> global. The W13 epilogue pairs warps
         // at a named barrier, so no warp leaves the tile loop early: after a failed wait a warp
