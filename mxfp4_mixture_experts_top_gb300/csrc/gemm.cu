@@ -138,8 +138,10 @@ struct Smem {
     static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;
     static constexpr int PAIRMAX_OFF = MISC_OFF + 16;         // W13 epilogue: [2 buffers][4 warps][16] floats
     static constexpr int PREFIX_OFF = PAIRMAX_OFF + 2 * 4 * 16 * 4;
-    static size_t bytes(int E) { return 1024 + PREFIX_OFF + sizeof(int) * (size_t)(E + 1 + 32); }
+    // tile prefix [E + 1], scan scratch [32], then per expert its first padded row and its row count [E] each
+    static constexpr size_t bytes(int E) { return 1024 + PREFIX_OFF + sizeof(int) * (size_t)(3 * E + 1 + 32); }
     static_assert(BSLAB % 1024 == 0 && ASTAGE % 1024 == 0, "stages must keep the 1024-byte swizzle alignment");
+    static_assert(bytes(1024) <= 232448, "shared memory per CTA");
 };
 
 __device__ __forceinline__ void record_error(int32_t *dev_error, int code)
@@ -154,8 +156,8 @@ struct Tile {
 };
 
 template <class C>
-__device__ __forceinline__ Tile decode_tile(int t, const int *tile_start, int E, int MB, const int32_t *offsets,
-                                            const int32_t *padded)
+__device__ __forceinline__ Tile decode_tile(int t, const int *tile_start, int E, int MB, const int *cnt,
+                                            const int *pad0)
 {
     constexpr int NMAX = C::NMAX;
     int lo = 0, hi = E - 1;                 // largest e with tile_start[e] <= t
@@ -168,11 +170,10 @@ __device__ __forceinline__ Tile decode_tile(int t, const int *tile_start, int E,
     int local = t - tile_start[lo];
     int nb = local / MB;
     r.mb = local - nb * MB;
-    int count = __ldg(offsets + lo + 1) - __ldg(offsets + lo);
-    int rem = count - nb * NMAX;
+    int rem = cnt[lo] - nb * NMAX;
     int n = rem < NMAX ? rem : NMAX;
     r.n = (n + 15) & ~15;
-    r.row0 = __ldg(padded + lo) + nb * NMAX;
+    r.row0 = pad0[lo] + nb * NMAX;
     return r;
 }
 
@@ -199,6 +200,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_kernel(const __grid_co
     float *pairmax = reinterpret_cast<float *>(smem + S::PAIRMAX_OFF);
     int *tile_start = reinterpret_cast<int *>(smem + S::PREFIX_OFF);
     int *scan_tmp = tile_start + p.E + 1;
+    int *s_pad0 = scan_tmp + 32, *s_cnt = s_pad0 + p.E;   // per expert: first padded row, rows
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int E = p.E, MB = p.MB;
@@ -211,6 +213,10 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_kernel(const __grid_co
         for (int q = 0; q < 4; ++q) {
             const int e = tid * 4 + q;
             const int cnt = e < E ? (__ldg(p.offsets + e + 1) - __ldg(p.offsets + e)) : 0;
+            if (e < E) {
+                s_cnt[e] = cnt;
+                s_pad0[e] = __ldg(p.padded + e);
+            }
             v[q] = (cnt + NMAX - 1) / NMAX * MB;
             s += v[q];
         }
@@ -302,7 +308,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_kernel(const __grid_co
         long long issued = 0;
         bool ok = true;
         int tcur = blockIdx.x, ka = 0;
-        Tile tl = decode_tile<C>(tcur, tile_start, E, MB, p.offsets, p.padded);
+        Tile tl = decode_tile<C>(tcur, tile_start, E, MB, s_cnt, s_pad0);
         for (int i0 = 0; i0 < n_slabs; i0 += SPS) {
             if (!__all_sync(0xFFFFFFFFu, wait_done(i0 / SPS - C::NA))) { ok = false; break; }
             const int nsl = n_slabs - i0 < SPS ? n_slabs - i0 : SPS;
@@ -320,7 +326,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_kernel(const __grid_co
                     ptx::tma_load_2d(dst, &p.tm_a1, 0, r0, &a_full[ai]);
                     ptx::bulk_g2s(sdst, p.wsf + (size_t)(r0 / TILE_ROWS) * SLAB_SF_BYTES, SLAB_SF_BYTES, &a_full[ai]);
                     if (nsl == 2) {                  // the second slab opens the next tile
-                        const Tile t2 = decode_tile<C>(tcur + (int)gridDim.x, tile_start, E, MB, p.offsets, p.padded);
+                        const Tile t2 = decode_tile<C>(tcur + (int)gridDim.x, tile_start, E, MB, s_cnt, s_pad0);
                         const int r1 = a_row(t2, 0);
                         ptx::tma_load_2d(dst + SLAB_SMEM_BYTES, &p.tm_a1, 0, r1, &a_full[ai]);
                         ptx::bulk_g2s(sdst + SLAB_SF_BYTES, p.wsf + (size_t)(r1 / TILE_ROWS) * SLAB_SF_BYTES,
@@ -337,7 +343,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_kernel(const __grid_co
                 tcur += gridDim.x;
                 next_tile = true;
             }
-            if (next_tile && tcur < total) tl = decode_tile<C>(tcur, tile_start, E, MB, p.offsets, p.padded);
+            if (next_tile && tcur < total) tl = decode_tile<C>(tcur, tile_start, E, MB, s_cnt, s_pad0);
             if (++ai == C::NA) { ai = 0; aph ^= 1u; }
         }
         if (!ok && lane == 0) fail();
@@ -367,7 +373,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_kernel(const __grid_co
         long long issued = 0;
         bool ok = true;
         int tcur = blockIdx.x, ka = 0;
-        Tile tl = decode_tile<C>(tcur, tile_start, E, MB, p.offsets, p.padded);
+        Tile tl = decode_tile<C>(tcur, tile_start, E, MB, s_cnt, s_pad0);
         for (int i0 = 0; i0 < n_slabs; i0 += SPS) {
             if (!__all_sync(0xFFFFFFFFu, wait_done(i0 / SPS - C::NB))) { ok = false; break; }
             const int nsl = n_slabs - i0 < SPS ? n_slabs - i0 : SPS;
@@ -382,7 +388,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_kernel(const __grid_co
                 if (ka == slabs) {
                     ka = 0;
                     tcur += gridDim.x;
-                    if (tcur < total) tl = decode_tile<C>(tcur, tile_start, E, MB, p.offsets, p.padded);
+                    if (tcur < total) tl = decode_tile<C>(tcur, tile_start, E, MB, s_cnt, s_pad0);
                 }
             } else {                                    // last slab of a tile, or a stage across two tiles
                 for (int pos = 0; pos < nsl; ++pos) {
@@ -395,7 +401,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_kernel(const __grid_co
                     if (++ka == slabs) {
                         ka = 0;
                         tcur += gridDim.x;
-                        if (tcur < total) tl = decode_tile<C>(tcur, tile_start, E, MB, p.offsets, p.padded);
+                        if (tcur < total) tl = decode_tile<C>(tcur, tile_start, E, MB, s_cnt, s_pad0);
                     }
                 }
             }
@@ -551,7 +557,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_kernel(const __grid_co
         bool ok = true;
         int j = 0;
         for (int t = blockIdx.x; t < total; t += gridDim.x, ++j) {
-            const Tile tl = decode_tile<C>(t, tile_start, E, MB, p.offsets, p.padded);
+            const Tile tl = decode_tile<C>(t, tile_start, E, MB, s_cnt, s_pad0);
             // MMA warp q wrote into the tile iff one of the tile's stages is one of its stages
             const int s_first = (j * slabs) / SPS, s_last = (j * slabs + slabs - 1) / SPS;
             const unsigned wrote = (C::MW == 1 || s_last > s_first) ? ((1u << C::MW) - 1u) : (1u << (s_first % C::MW));
@@ -562,21 +568,28 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_kernel(const __grid_co
 #pragma unroll
                 for (int q = 0; q < 16; ++q) raw[q] = 0u;
                 if (ok) {
+                    // sum the term columns of every accumulator of every MMA warp that wrote the tile, in
+                    // (warp, accumulator, term) order; loads go out in groups of four with one wait each
+                    constexpr int NCOMB = C::MW * C::NACC * NT, G = 4;
 #pragma unroll
-                    for (int w = 0; w < C::MW; ++w) {
-                        if (!((wrote >> w) & 1u)) continue;
-                        const uint32_t dt = tmem + t_lane + (uint32_t)((w * 2 + di) * C::D_COLS);
+                    for (int g0 = 0; g0 < NCOMB; g0 += G) {
+                        uint32_t part[G][16];
 #pragma unroll
-                        for (int a = 0; a < C::NACC; ++a)
+                        for (int u = 0; u < G; ++u) {
+                            const int idx = g0 + u, w = idx / (C::NACC * NT), a = (idx / NT) % C::NACC, term = idx % NT;
+                            if (idx < NCOMB && ((wrote >> w) & 1u))
+                                ptx::tmem_ld_32x32b_x16(tmem + t_lane + (uint32_t)((w * 2 + di) * C::D_COLS + a * NP +
+                                                                                    term * NMAX + c0), part[u]);
+                        }
+                        ptx::tmem_wait_ld();
 #pragma unroll
-                            for (int term = 0; term < NT; ++term) {   // sum the accumulators and the term columns
-                                uint32_t part[16];
-                                ptx::tmem_ld_32x32b_x16(dt + (uint32_t)(a * NP + term * NMAX + c0), part);
-                                ptx::tmem_wait_ld();
+                        for (int u = 0; u < G; ++u) {
+                            const int idx = g0 + u, w = idx / (C::NACC * NT);
+                            if (idx < NCOMB && ((wrote >> w) & 1u))
 #pragma unroll
                                 for (int q = 0; q < 16; ++q)
-                                    raw[q] = __float_as_uint(__uint_as_float(raw[q]) + __uint_as_float(part[q]));
-                            }
+                                    raw[q] = __float_as_uint(__uint_as_float(raw[q]) + __uint_as_float(part[u][q]));
+                        }
                     }
                 }
                 if (MODE == 0) {
