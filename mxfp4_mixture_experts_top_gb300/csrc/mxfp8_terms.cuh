@@ -70,11 +70,23 @@ __device__ __forceinline__ uint32_t mxfp8_term_pair(float &r0, float &r1, int e1
     return q;
 }
 
-// Term t of a single value (its own block exponent e1): returns the E4M3 byte, updates the residual.
-__device__ __forceinline__ uint32_t mxfp8_term1(float &r, int e1, int t, uint32_t &sbyte)
+// Term t of two values with their own block exponents e0 and e1 (one conversion for both; the
+// conversion rounds each element on its own): returns the E4M3 byte pair (byte 0 for r0) and the two
+// E8M0 scale bytes, and updates both residuals.
+__device__ __forceinline__ uint32_t mxfp8_term_2x(float &r0, float &r1, int e0, int e1, int t, uint32_t &sb0,
+                                                  uint32_t &sb1)
 {
-    float z = 0.f;
-    return mxfp8_term_pair(r, z, e1, t, sbyte) & 0xFFu;
+    int et0 = e0 - 4 * t, et1 = e1 - 4 * t;
+    if (et0 < -127) et0 = -127;
+    if (et1 < -127) et1 = -127;
+    sb0 = (uint32_t)(et0 + 127);
+    sb1 = (uint32_t)(et1 + 127);
+    const float inv0 = pow2f(-et0 > 127 ? 127 : -et0), inv1 = pow2f(-et1 > 127 ? 127 : -et1);
+    const uint32_t q = e4m3x2_rn(r0 * inv0, r1 * inv1);
+    const float2 v = e4m3x2_value(q);
+    r0 -= v.x * pow2f(et0);
+    r1 -= v.y * pow2f(et1);
+    return q;
 }
 
 }  // namespace moe
