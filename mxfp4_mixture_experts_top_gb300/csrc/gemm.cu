@@ -438,11 +438,28 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_kernel(const __grid_co
                 const uint32_t *bs = reinterpret_cast<const uint32_t *>(bsring + bi * S::BSSTAGE +
                                                                         pos * (whole ? S::BSSLAB : S::BSSLAB_PAD));
                 const uint32_t cell = tmem + quarter + (uint32_t)(C::SF_BASE + sc * C::CELL_COLS + pos * C::SF_COLS);
-                ptx::tmem_st_32x32b_x4(cell, aw.x, aw.y, aw.z, aw.w);
+                // the slab's cell in stores of 8 columns: A's 4, then one per 32 B rows (B row j: term
+                // j / NMAX of token row j % NMAX), zeros in the columns no MMA reads
+                uint32_t wv[C::SF_COLS];
+                wv[0] = aw.x;
+                wv[1] = aw.y;
+                wv[2] = aw.z;
+                wv[3] = aw.w;
 #pragma unroll
-                for (int c = 0; c < C::SFB_COLS; ++c) {
-                    const int j = lane + 32 * c;              // B row: term j / NMAX of token row j % NMAX
-                    ptx::tmem_st_32x32b_x1(cell + 4 + (uint32_t)c, j < NP ? bs[j] : 0u);
+                for (int c = 0; c < C::SF_COLS - 4; ++c) {
+                    const int j = lane + 32 * c;
+                    wv[4 + c] = (c < C::SFB_COLS && j < NP) ? bs[j] : 0u;
+                }
+#pragma unroll
+                for (int c0 = 0; c0 < C::SF_COLS; c0 += 8) {
+                    uint32_t v8[8];
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) v8[q] = c0 + q < C::SF_COLS ? wv[c0 + q] : 0u;
+                    if (c0 + 8 <= C::SF_COLS) {
+                        ptx::tmem_st_32x32b_x8(cell + (uint32_t)c0, v8);
+                    } else {
+                        ptx::tmem_st_32x32b_x4(cell + (uint32_t)c0, v8[0], v8[1], v8[2], v8[3]);
+                    }
                 }
             }
             ptx::tmem_wait_st();
