@@ -173,9 +173,11 @@ route_permute_kernel(const float *__restrict__ logits, int T, int E, int k, int 
 {
     // the gather launched next (with pdl) only waits on this grid, so it may start now
     griddep_launch_dependents();
-    for (int t = threadIdx.x >> 5; t < T; t += PERM_WARPS) route_token<VPL>(logits, t, E, k, ids, w, bitmatrix);
+    __shared__ int32_t s_ids[ROUTE_PERMUTE_FUSED_MAX_T * 32];    // this block's ids (k <= 32), read back by the permutation
+    for (int t = threadIdx.x >> 5; t < T; t += PERM_WARPS)
+        route_token<VPL>(logits, t, E, k, ids, w, bitmatrix, s_ids);
     __syncthreads();          // the ids written above are visible to the whole block
-    permute_block(ids, T, E, k, block_m, counts, offsets, padded, row_to_pair, rows_cap, pair_to_row, dev_error);
+    permute_block(s_ids, T, E, k, block_m, counts, offsets, padded, row_to_pair, rows_cap, pair_to_row, dev_error);
 }
 
 static size_t permute_smem(int E) { return sizeof(int) * ((size_t)PERM_WARPS * E + E + E + 1 + 32); }

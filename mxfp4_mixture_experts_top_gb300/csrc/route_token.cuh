@@ -25,11 +25,12 @@ __device__ __forceinline__ uint32_t float_key(float f)
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// Route token t (whole warp, converged). VPL = ceil(E / 32) values per lane.
+// Route token t (whole warp, converged). VPL = ceil(E / 32) values per lane. ids_copy (may be null):
+// a second destination of the ids, e.g. shared memory for a permutation in the same block.
 template <int VPL>
 __device__ __forceinline__ void route_token(const float *__restrict__ logits, int t, int E, int k,
                                             int32_t *__restrict__ ids, float *__restrict__ w,
-                                            uint32_t *__restrict__ bitmatrix)
+                                            uint32_t *__restrict__ bitmatrix, int32_t *ids_copy = nullptr)
 {
     const uint32_t lane = threadIdx.x & 31u;
     const float *row = logits + (int64_t)t * E;
@@ -71,6 +72,7 @@ __device__ __forceinline__ void route_token(const float *__restrict__ logits, in
     if ((int)lane < k) {
         ids[(int64_t)t * k + lane] = my_id;
         w[(int64_t)t * k + lane] = ex / z;
+        if (ids_copy) ids_copy[t * k + (int)lane] = my_id;
     }
     if (bitmatrix) {
         // every lane takes part in the shuffles; lane q builds word q (E <= 1024: at most 32 words)
