@@ -27,12 +27,19 @@
 //   * W13's epilogue applies SiLU(gate)*up, then splits h into 3 MXFP8 terms
 //     for W2 (block maxima over 32 features span two epilogue warps, which
 //     exchange them through shared memory).
-// Warp roles (352 threads): 0-3 epilogue, 4-7 scale-factor copiers (one per
-// TMEM lane quarter: the tensor core's sub-partition q reads the scale factors
-// of its 32 A rows, and of every B row, from lane quarter q, so each quarter
-// holds a full copy), 8 MMA issuer and TMEM owner, 9 activation producer (3-D
-// TMA), 10 weight producer (2-D TMA + bulk copy), 11 second MMA issuer (decode
-// configurations).
+//   * Per stage the MMA issuer waits on one barrier (the stage's scale-factor
+//     cell, filled after its weights and activations landed) and makes one
+//     commit, to done[s % ND], which frees the stage in all rings at once.
+//   * Under programmatic dependent launch the prologue and the weight stream
+//     run while the previous kernel finishes; only the activation producer
+//     waits for it (griddepcontrol.wait).
+// Warp roles (352 threads, 384 with the second MMA issuer): 0-3 epilogue, 4-7
+// scale-factor copiers (one per TMEM lane quarter: the tensor core's
+// sub-partition q reads the scale factors of its 32 A rows, and of every B
+// row, from lane quarter q, so each quarter holds a full copy), 8 MMA issuer
+// and TMEM owner, 9 activation producer (4-D TMA of the terms, 3-D TMA of
+// their scale words), 10 weight producer (2-D TMA + bulk copy of the scales),
+// 11 second MMA issuer (decode configurations).
 // Every wait is bounded (2 s); on time-out a CTA records MOE_ERR_TIMEOUT,
 // drains its copies and MMAs, frees TMEM and exits.
 #include <cuda_bf16.h>
@@ -356,8 +363,9 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_kernel(const __grid_co
             __all_sync(0xFFFFFFFFu, ptx::mbar_wait(&a_full[n % C::NA], (uint32_t)((n / C::NA) & 1), &never, LIM));
         }
     } else if (warp == 9) {
-        // ===================== activation producer: per stage, for each of its slabs one 3-D TMA box
-        // of the term rows (128 K x NMAX rows x NT terms) and one of their scale words (NMAX x NT)
+        // ===================== activation producer: per stage one 4-D TMA box of the term rows (128 K x
+        // NMAX rows x NT terms x SPS slabs) and one 3-D box of their scale words (NMAX x NT x SPS); slab
+        // by slab for a tile's last slab or a stage that crosses into the next tile
         if (ptx::elect_one()) {
             ptx::prefetch_tmap(&p.tm_b);
             ptx::prefetch_tmap(&p.tm_bs);
