@@ -275,6 +275,22 @@ moe_status_t moe_read_device_error(void *d_error_word, int *code, void *stream);
 /* Number of kernels launched by this library since load (all entry points). */
 uint64_t moe_launch_count(void);
 
+/*
+ * Self-test of the bounded device-side wait that every GEMM pipeline wait uses
+ * (failure detection without a GPU fault). One thread waits on a
+ * shared-memory mbarrier that nothing arrives on:
+ *   abort_after_ns == 0: the wait gives up after limit_ns;
+ *   0 < abort_after_ns < limit_ns: a second warp sets the CTA's abort flag
+ *   after abort_after_ns, and the wait returns then.
+ * Either way the kernel records MOE_ERR_TIMEOUT in *d_error_word (a device
+ * int32, read and cleared with moe_read_device_error) and the wait's duration
+ * in nanoseconds in *d_elapsed_ns (a device uint64), then exits normally.
+ * limit_ns must be in (0, 1e9]; d_error_word 4-byte and d_elapsed_ns 8-byte
+ * aligned. Argument errors return before the launch.
+ */
+moe_status_t moe_selftest_bounded_wait(uint64_t limit_ns, uint64_t abort_after_ns, int32_t *d_error_word,
+                                       uint64_t *d_elapsed_ns, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

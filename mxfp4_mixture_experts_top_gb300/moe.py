@@ -24,6 +24,7 @@ STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
 EXPORTS = ["moe_abi_version", "moe_status_string", "moe_route", "moe_permute_rows_capacity", "moe_permute",
            "moe_mxfp4_packed_bytes", "moe_mxfp4_prepack", "moe_mxfp4_dequant_bf16", "moe_mxfp4_workspace_bytes",
            "moe_mxfp4_forward", "moe_mxfp4_forward_timed", "moe_mxfp4_workspace_layout", "moe_read_device_error", "moe_launch_count",
+           "moe_selftest_bounded_wait",
            "moe_mxfp4_forward_noalloc", "moe_route_permute"]
 
 
@@ -69,6 +70,7 @@ def load(path: str = LIB_PATH):
             "moe_mxfp4_workspace_layout": ([D, ctypes.POINTER(ctypes.c_size_t * 7)], i32),
             "moe_read_device_error": ([P, ctypes.POINTER(ctypes.c_int), P], i32),
             "moe_launch_count": ([], ctypes.c_uint64),
+            "moe_selftest_bounded_wait": ([ctypes.c_uint64, ctypes.c_uint64, P, P, P], i32),
             "moe_mxfp4_forward_noalloc": ([D, P, P, P, P, P, P, P, P], i32),
             "moe_route_permute": ([P, i32, i32, i32, i32, P, P, P, P, P, P, P, P, P, P], i32),
         }
@@ -254,6 +256,16 @@ def forward_timed(desc: LayerDesc, x: torch.Tensor, packed: torch.Tensor, topk_w
                                           workspace.numel() * workspace.element_size(), arr, _stream(stream)),
            "moe_mxfp4_forward_timed")
     return y
+
+
+def selftest_bounded_wait(limit_ns: int, abort_after_ns: int, error: torch.Tensor, elapsed: torch.Tensor,
+                          stream=None) -> None:
+    """moe_selftest_bounded_wait: a pipeline wait that nothing completes gives up (after limit_ns, or when
+    another warp sets the abort flag after abort_after_ns) and records MOE_ERR_TIMEOUT in `error`."""
+    _cuda(error, torch.int32, "error")
+    _cuda(elapsed, torch.int64, "elapsed")
+    _check(load().moe_selftest_bounded_wait(limit_ns, abort_after_ns, _ptr(error), _ptr(elapsed), _stream(stream)),
+           "moe_selftest_bounded_wait")
 
 
 def read_device_error(word: torch.Tensor, stream=None) -> int:

@@ -104,3 +104,13 @@ def test_entry_points_reject_bad_arguments_without_launching(lib):
     d0 = moe.make_desc(0, 512, 256, 8, 2, 16)
     assert lib.moe_mxfp4_forward(ctypes.byref(d0), null, null, null, null, null, null, null, null, 0, null) == 0
     assert moe.launch_count() == n0
+
+
+def test_selftest_bounded_wait_rejects_bad_arguments(lib):
+    """Argument checks run on the host before any launch (no GPU needed)."""
+    fake = ctypes.c_void_p(1 << 20)          # aligned, never dereferenced: every call below fails its checks
+    INVALID = 1
+    assert lib.moe_selftest_bounded_wait(0, 0, fake, fake, None) == INVALID                # no limit
+    assert lib.moe_selftest_bounded_wait(2_000_000_000, 0, fake, fake, None) == INVALID    # over 1 s
+    assert lib.moe_selftest_bounded_wait(1_000_000, 1_000_000, fake, fake, None) == INVALID  # abort not before limit
+    assert lib.moe_selftest_bounded_wait(1_000_000, 0, None, fake, None) == INVALID         # null error word
