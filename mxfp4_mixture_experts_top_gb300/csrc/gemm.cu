@@ -93,8 +93,8 @@ struct Cfg {
 };
 
 // decode, <= 2 rows per expert on average
-using W13Tiny = Cfg<0, 16, NT_X, 2, 5, 4, 6, 2, 2>;
-using W2Tiny = Cfg<1, 16, NT_H, 2, 5, 3, 6, 2, 2>;
+using W13Tiny = Cfg<0, 16, NT_X, 2, 5, 4, 6, 1, 2>;
+using W2Tiny = Cfg<1, 16, NT_H, 2, 5, 3, 6, 1, 2>;
 // decode batches: <= 16 rows per expert
 using W13Small = Cfg<0, 32, NT_X, 2, 4, 4, 6, 1, 2>;
 using W2Small = Cfg<1, 32, NT_H, 2, 4, 3, 4, 1, 2>;
