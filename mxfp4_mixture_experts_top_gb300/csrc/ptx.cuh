@@ -19,13 +19,6 @@ __device__ __forceinline__ uint64_t globaltimer_ns()
     return t;
 }
 
-__device__ __forceinline__ uint32_t lane_id()
-{
-    uint32_t l;
-    asm volatile("mov.u32 %0, %%laneid;" : "=r"(l));
-    return l;
-}
-
 // One lane of a converged warp (the same lane on every call with all lanes
 // active). Issue-once operations (TMA, tcgen05.mma, tcgen05.commit) go through
 // it from code the whole warp executes: issuing them from a lane that runs
@@ -62,13 +55,6 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t by
 {
     asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;"
                  ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
-}
-
-// Raise the transaction count of the current phase without arriving (a later
-// arrive.expect_tx of the same phase carries the arrival).
-__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes)
-{
-    asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
 }
 
 // Named barrier `id` over `nthreads` threads (whole warps).
@@ -199,18 +185,6 @@ __device__ __forceinline__ void tc_fence_after()
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// D(tmem) (+)= A(tmem) * B(smem descriptor), kind::f16 (bf16 inputs, fp32 accumulate).
-__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                            uint32_t idesc, uint32_t accumulate)
-{
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.u32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
-        ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
 // D(tmem) (+)= (A(smem) x 2^sfA) * (B(smem) x 2^sfB), kind::mxf8f6f4 with block scaling: one E8M0
 // scale per 32 K-elements of every A row and B row, read from tensor memory (K = 32 per MMA).
 __device__ __forceinline__ void mma_mx_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
@@ -231,32 +205,6 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar)
                  ::"r"(smem_u32(bar)) : "memory");
 }
 
-// Store 32 consecutive 32-bit columns of this thread's TMEM lane.
-__device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const uint32_t (&v)[32])
-{
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
-        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
-        "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};"
-        ::"r"(taddr),
-        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
-        "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]),
-        "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]),
-        "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
-        : "memory");
-}
-
-// Store 1, 2 or 4 consecutive 32-bit columns of this thread's TMEM lane.
-__device__ __forceinline__ void tmem_st_32x32b_x1(uint32_t taddr, uint32_t a)
-{
-    asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(a) : "memory");
-}
-
-__device__ __forceinline__ void tmem_st_32x32b_x2(uint32_t taddr, uint32_t a, uint32_t b)
-{
-    asm volatile("tcgen05.st.sync.aligned.32x32b.x2.b32 [%0], {%1, %2};" ::"r"(taddr), "r"(a), "r"(b) : "memory");
-}
-
 __device__ __forceinline__ void tmem_st_32x32b_x4(uint32_t taddr, uint32_t a, uint32_t b, uint32_t c, uint32_t d)
 {
     asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};"
@@ -269,18 +217,6 @@ __device__ __forceinline__ void tmem_st_32x32b_x8(uint32_t taddr, const uint32_t
     asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
                  ::"r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]),
                    "r"(v[7]) : "memory");
-}
-
-// Store 16 consecutive 32-bit columns of this thread's TMEM lane.
-__device__ __forceinline__ void tmem_st_32x32b_x16(uint32_t taddr, const uint32_t (&v)[16])
-{
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
-        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};"
-        ::"r"(taddr),
-        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
-        "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
-        : "memory");
 }
 
 __device__ __forceinline__ void tmem_wait_st()
@@ -317,16 +253,6 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr)
     d |= (uint64_t)1 << 46;                         // descriptor version (tcgen05)
     d |= (uint64_t)2 << 61;                         // layout: 128-byte swizzle
     return d;
-}
-
-// Instruction descriptor: kind::f16, A = B = bf16, D = f32, both K-major, M x N.
-__host__ __device__ __forceinline__ uint32_t idesc_bf16_f32(uint32_t M, uint32_t N)
-{
-    return (1u << 4)              // D format f32
-         | (1u << 7)              // A format bf16
-         | (1u << 10)             // B format bf16
-         | ((N >> 3) << 17)       // N / 8
-         | ((M >> 4) << 24);      // M / 16
 }
 
 // Instruction descriptor for kind::mxf8f6f4 with block scaling: A = E2M1, B = E4M3, D = f32, both
