@@ -12,6 +12,9 @@ its size) before every step, outside the per-step CUDA events; `value` is
 tokens over the summed per-step device time. `e2e` repeats the step through
 the public API with pinned host buffers: host->device copy of x and logits,
 the three calls, device->host copy of y, all inside the timed region.
+`graph` times the same step replayed from one CUDA graph (route+permute and
+the forward captured once), as a serving stack runs a decode step; `step_ms`
+gives the p10/p50/p90 of the timed steps.
 
 Under torchrun each rank runs an independent replica (weak scaling, no
 collective on the data path); rank 0 prints the JSON line with the maximum
@@ -397,6 +400,23 @@ def run_ours(args, world, rank, local):
         e1.synchronize()
         e2e_ms += e0.elapsed_time(e1)
     e2e_ms = allreduce_max(e2e_ms, world) / args.steps
+    # ---- the same step replayed from one CUDA graph (how a serving stack runs a decode step)
+    graph, _ = layer.capture_graph(x, logits)
+    g_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for _ in range(args.warmup):
+        flush_buf.zero_()
+        graph.replay()
+    for a, b in g_ev:
+        flush_buf.zero_()
+        a.record()
+        graph.replay()
+        b.record()
+    torch.cuda.synchronize()
+    assert layer.forward_error() == 0, "device error in the graph replays"
+    g_ms = allreduce_max(float(np.sum([a.elapsed_time(b) for a, b in g_ev])), world) / args.steps
+    del graph
+    graph_line = {"value": world * T / (g_ms / 1e3), "unit": UNIT, "ms_per_step": g_ms,
+                  "how": "route+permute+forward captured in one CUDA graph, replayed; L2 flushed before each replay"}
     e2e = {"value": world * T / (e2e_ms / 1e3), "unit": UNIT, "ms_per_step": e2e_ms,
            "h2d_bytes_per_step": T * H * 2 + T * E * 4, "d2h_bytes_per_step": T * H * 4}
 
@@ -460,6 +480,9 @@ def run_ours(args, world, rank, local):
             "wall_s_timed": wall,
             "clocks": clocks,
             "cpu_baseline": cpu,
+            "step_ms": {"p10": float(np.percentile(step_ms, 10)), "p50": float(np.percentile(step_ms, 50)),
+                        "p90": float(np.percentile(step_ms, 90))},
+            "graph": graph_line,
         }
         if per_config:
             line["per_config"] = per_config
