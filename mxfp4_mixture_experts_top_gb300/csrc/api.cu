@@ -65,17 +65,22 @@ std::map<MapKey, MapEntry> g_maps;
 // [d1 rows][128], box 128 x b1 rows x d2 terms x b3 slabs. Both with the 128-byte swizzle of the
 // MMA operands. kind 2: activation scale words, a 3-D uint32 tensor [d2 slabs][d1 terms][d0 rows],
 // box b1 rows x d1 terms x b3 slabs, no swizzle.
-const CUtensorMap *get_map(int kind, const void *ptr, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t b1,
-                           uint32_t b3, moe_status_t *st)
+// The map is copied out under the cache lock, so a later eviction (the cache is emptied once it
+// holds 4096 maps) or another thread cannot invalidate what the caller holds.
+bool get_map(CUtensorMap *out, int kind, const void *ptr, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t b1,
+             uint32_t b3, moe_status_t *st)
 {
     int dev = 0;
     cudaGetDevice(&dev);
     MapKey key{dev, kind, ptr, d0, d1, d2, b1, b3};
     std::lock_guard<std::mutex> lk(g_map_mu);
     auto it = g_maps.find(key);
-    if (it != g_maps.end()) return &it->second.map;
+    if (it != g_maps.end()) {
+        *out = it->second.map;
+        return true;
+    }
     EncodeTiledFn fn = encode_fn();
-    if (!fn) { *st = MOE_ERR_CUDA; return nullptr; }
+    if (!fn) { *st = MOE_ERR_CUDA; return false; }
     if (g_maps.size() > 4096) g_maps.clear();
     MapEntry ent;
     CUresult r;
@@ -102,9 +107,10 @@ const CUtensorMap *get_map(int kind, const void *ptr, uint64_t d0, uint64_t d1, 
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     }
-    if (r != CUDA_SUCCESS) { *st = MOE_ERR_CUDA; return nullptr; }
-    auto res = g_maps.emplace(key, ent);
-    return &res.first->second.map;
+    if (r != CUDA_SUCCESS) { *st = MOE_ERR_CUDA; return false; }
+    g_maps.emplace(key, ent);
+    *out = ent.map;
+    return true;
 }
 
 int sm_count()
@@ -350,22 +356,22 @@ moe_status_t moe_mxfp4_forward_timed(const moe_layer_desc *d, const uint16_t *d_
     const uint8_t *w13 = a.packed, *w2 = a.packed + packed_w13_bytes(d->E, d->H, d->I);
     const uint64_t rows13 = (uint64_t)d->E * 2 * d->I * (d->H / KSLAB);   // 128-element rows of W13 nibbles
     const uint64_t rows2 = (uint64_t)d->E * d->H * (d->I / KSLAB);
-    if (!(a.tmap_w13 = get_map(0, w13, 128, rows13, 1, 128 * sps, 1, &st))) return st;
-    if (!(a.tmap_w13_1 = get_map(0, w13, 128, rows13, 1, 128, 1, &st))) return st;
-    if (!(a.tmap_w2 = get_map(0, w2, 128, rows2, 1, 128 * sps, 1, &st))) return st;
-    if (!(a.tmap_w2_1 = get_map(0, w2, 128, rows2, 1, 128, 1, &st))) return st;
+    if (!get_map(&a.tmap_w13, 0, w13, 128, rows13, 1, 128 * sps, 1, &st)) return st;
+    if (!get_map(&a.tmap_w13_1, 0, w13, 128, rows13, 1, 128, 1, &st)) return st;
+    if (!get_map(&a.tmap_w2, 0, w2, 128, rows2, 1, 128 * sps, 1, &st)) return st;
+    if (!get_map(&a.tmap_w2_1, 0, w2, 128, rows2, 1, 128, 1, &st)) return st;
     const uint32_t n13 = (uint32_t)regime_nmax(a.regime, 0), n2 = (uint32_t)regime_nmax(a.regime, 1);
     const uint64_t s13 = (uint64_t)(d->H / KSLAB), s2 = (uint64_t)(d->I / KSLAB);
     // activation terms and their scale words: a whole stage (sps slabs) per box, and single-slab
     // boxes for a stage that straddles two tiles
-    if (!(a.tmap_xq = get_map(1, a.xq, (uint64_t)d->H, (uint64_t)R, NT_X, n13, sps, &st))) return st;
-    if (!(a.tmap_xq1 = get_map(1, a.xq, (uint64_t)d->H, (uint64_t)R, NT_X, n13, 1, &st))) return st;
-    if (!(a.tmap_hq = get_map(1, a.hq, (uint64_t)d->I, (uint64_t)R, NT_H, n2, sps, &st))) return st;
-    if (!(a.tmap_hq1 = get_map(1, a.hq, (uint64_t)d->I, (uint64_t)R, NT_H, n2, 1, &st))) return st;
-    if (!(a.tmap_xs = get_map(2, a.xs, (uint64_t)a.rows_sf, NT_X, s13, n13, sps, &st))) return st;
-    if (!(a.tmap_xs1 = get_map(2, a.xs, (uint64_t)a.rows_sf, NT_X, s13, n13, 1, &st))) return st;
-    if (!(a.tmap_hs = get_map(2, a.hs, (uint64_t)a.rows_sf, NT_H, s2, n2, sps, &st))) return st;
-    if (!(a.tmap_hs1 = get_map(2, a.hs, (uint64_t)a.rows_sf, NT_H, s2, n2, 1, &st))) return st;
+    if (!get_map(&a.tmap_xq, 1, a.xq, (uint64_t)d->H, (uint64_t)R, NT_X, n13, sps, &st)) return st;
+    if (!get_map(&a.tmap_xq1, 1, a.xq, (uint64_t)d->H, (uint64_t)R, NT_X, n13, 1, &st)) return st;
+    if (!get_map(&a.tmap_hq, 1, a.hq, (uint64_t)d->I, (uint64_t)R, NT_H, n2, sps, &st)) return st;
+    if (!get_map(&a.tmap_hq1, 1, a.hq, (uint64_t)d->I, (uint64_t)R, NT_H, n2, 1, &st)) return st;
+    if (!get_map(&a.tmap_xs, 2, a.xs, (uint64_t)a.rows_sf, NT_X, s13, n13, sps, &st)) return st;
+    if (!get_map(&a.tmap_xs1, 2, a.xs, (uint64_t)a.rows_sf, NT_X, s13, n13, 1, &st)) return st;
+    if (!get_map(&a.tmap_hs, 2, a.hs, (uint64_t)a.rows_sf, NT_H, s2, n2, sps, &st)) return st;
+    if (!get_map(&a.tmap_hs1, 2, a.hs, (uint64_t)a.rows_sf, NT_H, s2, n2, 1, &st)) return st;
     if (cudaMemsetAsync(a.dev_error, 0, sizeof(int32_t), s) != cudaSuccess) return MOE_ERR_CUDA;
     return from_cuda(launch_forward(a, s));
 }

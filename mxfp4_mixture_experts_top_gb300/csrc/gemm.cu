@@ -867,12 +867,12 @@ cudaError_t launch_forward(const ForwardArgs &a, cudaStream_t s)
     g.dev_error = a.dev_error;
 
     // W13: K = H, 64 features (128 rows) per weight tile
-    g.tm_a = *a.tmap_w13;
-    g.tm_a1 = *a.tmap_w13_1;
-    g.tm_b = *a.tmap_xq;
-    g.tm_b1 = *a.tmap_xq1;
-    g.tm_bs = *a.tmap_xs;
-    g.tm_bs1 = *a.tmap_xs1;
+    g.tm_a = a.tmap_w13;
+    g.tm_a1 = a.tmap_w13_1;
+    g.tm_b = a.tmap_xq;
+    g.tm_b1 = a.tmap_xq1;
+    g.tm_bs = a.tmap_xs;
+    g.tm_bs1 = a.tmap_xs1;
     g.wsf = a.packed + (size_t)a.E * 2 * a.I * (a.H / 2);
     g.K = a.H;
     g.MB = a.I / 64;
@@ -885,12 +885,12 @@ cudaError_t launch_forward(const ForwardArgs &a, cudaStream_t s)
     mark(a, 2, s);
 
     // W2: K = I, 128 output features per weight tile
-    g.tm_a = *a.tmap_w2;
-    g.tm_a1 = *a.tmap_w2_1;
-    g.tm_b = *a.tmap_hq;
-    g.tm_b1 = *a.tmap_hq1;
-    g.tm_bs = *a.tmap_hs;
-    g.tm_bs1 = *a.tmap_hs1;
+    g.tm_a = a.tmap_w2;
+    g.tm_a1 = a.tmap_w2_1;
+    g.tm_b = a.tmap_hq;
+    g.tm_b1 = a.tmap_hq1;
+    g.tm_bs = a.tmap_hs;
+    g.tm_bs1 = a.tmap_hs1;
     g.wsf = a.packed + packed_w13_bytes(a.E, a.H, a.I) + (size_t)a.E * a.H * (a.I / 2);
     g.K = a.I;
     g.MB = a.H / TILE_ROWS;

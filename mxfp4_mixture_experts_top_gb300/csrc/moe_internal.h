@@ -96,9 +96,9 @@ struct ForwardArgs {
     uint8_t *xq, *xs;      // x terms [H/128][NT_X][rows_cap][128], scale words [H/128][NT_X][rows_sf]
     uint8_t *hq, *hs;      // h terms [I/128][NT_H][rows_cap][128], scale words [I/128][NT_H][rows_sf]
     float *staging;
-    const CUtensorMap *tmap_w13, *tmap_w13_1, *tmap_w2, *tmap_w2_1;   // weight nibbles: stage / single-slab boxes
-    const CUtensorMap *tmap_xq, *tmap_xq1, *tmap_hq, *tmap_hq1;      // activation terms: stage / one-slab boxes
-    const CUtensorMap *tmap_xs, *tmap_xs1, *tmap_hs, *tmap_hs1;      // their scale words
+    CUtensorMap tmap_w13, tmap_w13_1, tmap_w2, tmap_w2_1;   // weight nibbles: stage / single-slab boxes
+    CUtensorMap tmap_xq, tmap_xq1, tmap_hq, tmap_hq1;      // activation terms: stage / one-slab boxes
+    CUtensorMap tmap_xs, tmap_xs1, tmap_hs, tmap_hs1;      // their scale words
     Regime regime;
     int num_sms;
     void *const *events;   // optional: 5 cudaEvent_t recorded between kernels
