@@ -68,11 +68,12 @@ constexpr int TMEM_COLS = 512;
 // NACC: accumulators per tile and MMA warp (consecutive 32-K blocks rotate
 // over them, so short MMAs do not wait on each other). MW: MMA warps; stage s
 // is issued by warp s % MW into its own accumulator sets, so while one warp
-// waits and does its bookkeeping the other keeps the tensor pipe fed.
-template <int MODE_, int NMAX_, int NT_, int SPS_, int NA_, int NB_, int NSF_, int NACC_, int MW_>
+// waits and does its bookkeeping the other keeps the tensor pipe fed. EMAX: most experts the
+// configuration takes (its shared memory holds per-expert tile prefixes, first rows and counts).
+template <int MODE_, int NMAX_, int NT_, int SPS_, int NA_, int NB_, int NSF_, int NACC_, int MW_, int EMAX_ = 1024>
 struct Cfg {
     static constexpr int MODE = MODE_, NMAX = NMAX_, NT = NT_, SPS = SPS_, NA = NA_, NB = NB_, NSF = NSF_,
-                         NACC = NACC_, MW = MW_;
+                         NACC = NACC_, MW = MW_, EMAX = EMAX_;
     static constexpr int NP = NT * NMAX;                       // MMA N: all terms of NMAX rows
     static constexpr int SFB_COLS = (NP + 31) / 32;            // B scale cells: row j in column j / 32
     static constexpr int SF_COLS = (4 + SFB_COLS + 3) / 4 * 4; // one slab's cells: A (4 columns), then B
@@ -94,7 +95,11 @@ struct Cfg {
 
 // decode, <= 2 rows per expert on average
 using W13Tiny = Cfg<0, 16, NT_X, 2, 5, 4, 6, 1, 2>;
-using W2Tiny = Cfg<1, 16, NT_H, 2, 5, 3, 6, 1, 2>;
+// W2 is bound by its activation ring as much as by its weight ring: five weight and four activation
+// stages up to 512 experts (the shared memory for more experts' prefixes does not fit), four and
+// four above
+using W2Tiny = Cfg<1, 16, NT_H, 2, 5, 4, 6, 1, 2, 512>;
+using W2TinyWideE = Cfg<1, 16, NT_H, 2, 4, 4, 6, 1, 2>;
 // decode batches: <= 16 rows per expert
 using W13Small = Cfg<0, 32, NT_X, 2, 4, 4, 6, 1, 2>;
 using W2Small = Cfg<1, 32, NT_H, 2, 4, 3, 4, 1, 2>;
@@ -148,7 +153,7 @@ struct Smem {
     // tile prefix [E + 1], scan scratch [32], then per expert its first padded row and its row count [E] each
     static constexpr size_t bytes(int E) { return 1024 + PREFIX_OFF + sizeof(int) * (size_t)(3 * E + 1 + 32); }
     static_assert(BSLAB % 1024 == 0 && ASTAGE % 1024 == 0, "stages must keep the 1024-byte swizzle alignment");
-    static_assert(bytes(1024) <= 232448, "shared memory per CTA");
+    static_assert(bytes(C::EMAX) <= 232448, "shared memory per CTA");
 };
 
 __device__ __forceinline__ void record_error(int32_t *dev_error, int code)
@@ -794,7 +799,7 @@ cudaError_t launch_gemm(const GemmParams &p, int grid, cudaStream_t s, bool pdl)
     cudaGetDevice(&dev);
     if (dev >= 64 || !((attr_set >> dev) & 1ull)) {
         cudaError_t e = cudaFuncSetAttribute(moe_gemm_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)Smem<C>::bytes(1024));
+                                             (int)Smem<C>::bytes(C::EMAX));
         if (e != cudaSuccess) return e;
         if (dev < 64) __atomic_fetch_or(&attr_set, 1ull << dev, __ATOMIC_RELAXED);
     }
@@ -894,7 +899,8 @@ cudaError_t launch_forward(const ForwardArgs &a, cudaStream_t s)
     g.wsf = a.packed + packed_w13_bytes(a.E, a.H, a.I) + (size_t)a.E * a.H * (a.I / 2);
     g.K = a.I;
     g.MB = a.H / TILE_ROWS;
-    err = rg == Regime::Tiny  ? launch_gemm<W2Tiny>(g, a.num_sms, s, pdl)
+    err = rg == Regime::Tiny  ? (a.E <= W2Tiny::EMAX ? launch_gemm<W2Tiny>(g, a.num_sms, s, pdl)
+                                                     : launch_gemm<W2TinyWideE>(g, a.num_sms, s, pdl))
         : rg == Regime::Small ? launch_gemm<W2Small>(g, a.num_sms, s, pdl)
         : rg == Regime::Mid   ? launch_gemm<W2Mid>(g, a.num_sms, s, pdl)
                               : launch_gemm<W2Large>(g, a.num_sms, s, pdl);
