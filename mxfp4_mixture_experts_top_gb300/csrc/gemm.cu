@@ -107,8 +107,12 @@ using W2Small = Cfg<1, 32, NT_H, 2, 4, 3, 4, 1, 2>;
 using W13Mid = Cfg<0, 64, NT_X, 2, 3, 3, 6, 1, 1>;
 using W2Mid = Cfg<1, 64, NT_H, 2, 3, 2, 4, 1, 1>;
 // prefill
-using W13Large = Cfg<0, 96, NT_X, 2, 3, 2, 4, 1, 1>;
-using W2Large = Cfg<1, 64, NT_H, 2, 3, 2, 4, 1, 1>;
+// (prefill weights are mostly re-read from L2, the activation rows are the bound: a third activation
+// stage up to 512 experts, two above)
+using W13Large = Cfg<0, 96, NT_X, 2, 2, 3, 4, 1, 1, 512>;
+using W2Large = Cfg<1, 64, NT_H, 2, 2, 3, 4, 1, 1, 512>;
+using W13LargeWideE = Cfg<0, 96, NT_X, 2, 3, 2, 4, 1, 1>;
+using W2LargeWideE = Cfg<1, 64, NT_H, 2, 3, 2, 4, 1, 1>;
 static_assert(W13Large::NMAX == 96 && W2Large::NMAX == 64, "regime_nmax() mirrors these");
 
 struct GemmParams {
@@ -885,7 +889,8 @@ cudaError_t launch_forward(const ForwardArgs &a, cudaStream_t s)
     err = rg == Regime::Tiny  ? launch_gemm<W13Tiny>(g, a.num_sms, s, pdl)
         : rg == Regime::Small ? launch_gemm<W13Small>(g, a.num_sms, s, pdl)
         : rg == Regime::Mid   ? launch_gemm<W13Mid>(g, a.num_sms, s, pdl)
-                              : launch_gemm<W13Large>(g, a.num_sms, s, pdl);
+                              : (a.E <= W13Large::EMAX ? launch_gemm<W13Large>(g, a.num_sms, s, pdl)
+                                                       : launch_gemm<W13LargeWideE>(g, a.num_sms, s, pdl));
     if (err != cudaSuccess) return err;
     mark(a, 2, s);
 
@@ -903,7 +908,8 @@ cudaError_t launch_forward(const ForwardArgs &a, cudaStream_t s)
                                                      : launch_gemm<W2TinyWideE>(g, a.num_sms, s, pdl))
         : rg == Regime::Small ? launch_gemm<W2Small>(g, a.num_sms, s, pdl)
         : rg == Regime::Mid   ? launch_gemm<W2Mid>(g, a.num_sms, s, pdl)
-                              : launch_gemm<W2Large>(g, a.num_sms, s, pdl);
+                              : (a.E <= W2Large::EMAX ? launch_gemm<W2Large>(g, a.num_sms, s, pdl)
+                                                      : launch_gemm<W2LargeWideE>(g, a.num_sms, s, pdl));
     if (err != cudaSuccess) return err;
     mark(a, 3, s);
 

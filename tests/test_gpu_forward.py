@@ -199,7 +199,8 @@ def test_forward_swiglu_clamp_variant(gpu_lib, gpu_layers, name):
 
 @pytest.mark.parametrize("T,H,I,E,k", [(1, 256, 128, 8, 2), (17, 128, 256, 16, 4), (200, 256, 128, 5, 3),
                                        (300, 128, 128, 64, 6),
-                                       (40, 256, 128, 1024, 6)])   # > 512 experts: the wide-E W2 tiles
+                                       (40, 256, 128, 1024, 6),     # > 512 experts: the wide-E decode W2 tiles
+                                       (11000, 128, 128, 1024, 6)])  # > 64 rows per expert, > 512 experts: wide-E prefill tiles
 def test_forward_fuzz_shapes(gpu_lib, gpu_layers, T, H, I, E, k):
     L = synth.make_layer(T=T, H=H, E=E, k=k, I=I, seed=T + E)
     r = _run_layer(gpu_lib, gpu_layers, L)
