@@ -1,0 +1,33 @@
+"""bench.py's work accounting, on the CPU: the algorithmic bytes and flops
+behind every roofline fraction it prints."""
+import numpy as np
+
+import bench
+from mxfp4_mixture_experts_top_gb300 import moe
+
+
+def test_per_expert_bytes_match_the_format_and_the_library():
+    # MXFP4: 4 bits per weight plus one E8M0 byte per 32 weights
+    w13, w2 = bench.per_expert_bytes(4096, 2048)
+    assert (w13, w2) == (2 * 2048 * 4096 // 2 + 2 * 2048 * 4096 // 32, 4096 * 2048 // 2 + 4096 * 2048 // 32)
+    assert (w13, w2) == (8_912_896, 4_456_448)
+    lib = moe.load()
+    for E, H, I in ((256, 4096, 2048), (32, 512, 256), (5, 256, 128)):
+        d = moe.make_desc(8, H, I, E, 2, 16)
+        a, b = bench.per_expert_bytes(H, I)
+        assert lib.moe_mxfp4_packed_bytes(d) == E * (a + b)
+
+
+def test_algorithmic_counts_touched_experts_and_routed_pairs():
+    T, H, I, E, k = 8, 4096, 2048, 256, 6
+    L = dict(T=T, H=H, I=I, E=E, k=k)
+    ids = np.arange(T * k).reshape(T, k) % 45          # 45 distinct experts, 48 pairs
+    a = bench.algorithmic(L, ids)
+    P = T * k
+    assert a["touched"] == 45
+    assert a["w13_kernel_bytes"] == 45 * 8_912_896 + 2 * P * (H + H // 32) + 3 * P * (I + I // 32)
+    assert a["w13_kernel_bytes"] == 401_789_952        # the decode figure quoted with the W13 roofline
+    assert a["layer_bytes"] == 45 * (8_912_896 + 4_456_448) + T * H * 2 + T * E * 4 + T * H * 4
+    assert a["flops"] == 6.0 * P * H * I
+    # executed: W13 (2I rows) against 2 x terms, W2 (H rows) against 3 h terms
+    assert a["mma_flops"] == 2.0 * P * H * I * (2 * 2 + 3)
