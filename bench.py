@@ -3,8 +3,11 @@
 
 One step = one pass of the whole layer over one batch of synthetic input:
 moe_route -> moe_permute -> moe_mxfp4_forward (gather, W13 GEMM + SiLU*up,
-W2 GEMM, combine). Default workload: one decode step with 7 draft tokens
-(T=8, H=4096, E=256, top-6, I=2048).
+W2 GEMM, combine). Default (headline) workload: the largest one, a Zipf-skewed
+8,191-token prefill (H=4096, E=256, top-6, I=2048). The other 4096-wide
+workloads (decode T=8 with 7 draft tokens, 64 decode streams T=512, a
+2,048-token prefill chunk) are timed with shorter runs in the same process
+and reported under `per_config`, each with its own roofline.
 
 Timing: W untimed warm-up steps, then exactly K steps between a barrier and
 a device synchronise on both sides. The L2 cache is flushed (a write of twice
@@ -42,7 +45,9 @@ sys.path.insert(0, ROOT)
 
 METRIC = "MoE-layer tokens/s and % of HBM / MXFP4-tensor roofline; route µs/layer"
 UNIT = "tokens/s"
-DEFAULT_WORKLOAD = "decode_t8_h4096_e256"
+DEFAULT_WORKLOAD = "prefill_t8191_zipf_h4096_e256"
+PER_CONFIG = ["decode_t8_h4096_e256", "decode_t512_h4096_e256", "prefill_t2048_h4096_e256"]
+L2_NOTE = "flushed before every timed GPU step by a write of twice the L2 size (n/a on the CPU arm)"
 
 
 def per_expert_bytes(H, I):
@@ -52,35 +57,77 @@ def per_expert_bytes(H, I):
     return w13, w2
 
 
-NT_X, NT_H = 2, 3   # MXFP8 terms of the activations: x (bf16) and h = SiLU(gate)*up
+NT_X, NT_H = 2, 3   # default MXFP8 terms of the activations: x (bf16) and h = SiLU(gate)*up
 
 
-def algorithmic(L, ids):
+def algorithmic(L, ids, nt_x=NT_X, nt_h=NT_H):
     """Algorithmic bytes and flops of one step.
 
     W13 kernel: touched experts' MXFP4 W13 bytes (nibbles + E8M0 scales), the P gathered
-    activation rows as NT_X E4M3 terms with one scale byte per 32 elements, and the P rows of
-    h written as NT_H terms with their scales. Layer: touched experts' W13 + W2 bytes, x (bf16),
-    logits (fp32), y (fp32). Useful flops: 6 P H I (2 P H 2I for W13, 2 P I H for W2);
-    executed tensor flops: NT_X (W13) and NT_H (W2) times the useful ones."""
+    activation rows as nt_x E4M3 terms with one scale byte per 32 elements, and the P rows of
+    h written as nt_h terms with their scales. W2 kernel: touched experts' W2 bytes, the h terms
+    read back, and the fp32 per-pair outputs written. Layer: touched experts' W13 + W2 bytes,
+    x (bf16), logits (fp32), y (fp32). Useful flops: 6 P H I (4 P H I for W13, 2 P I H for W2);
+    executed tensor flops: nt_x (W13) and nt_h (W2) times the useful ones."""
     T, H, I, E, k = L["T"], L["H"], L["I"], L["E"], L["k"]
     touched = int(len(np.unique(ids)))
     P = T * k
     w13, w2 = per_expert_bytes(H, I)
-    w13_kernel = touched * w13 + NT_X * P * (H + H // 32) + NT_H * P * (I + I // 32)
+    w13_kernel = touched * w13 + nt_x * P * (H + H // 32) + nt_h * P * (I + I // 32)
+    w2_kernel = touched * w2 + nt_h * P * (I + I // 32) + 4 * P * H
     layer = touched * (w13 + w2) + T * H * 2 + T * E * 4 + T * H * 4
     flops = 6.0 * P * H * I
-    mma_flops = 2.0 * P * H * I * (2 * NT_X + NT_H)
-    return dict(touched=touched, w13_kernel_bytes=w13_kernel, layer_bytes=layer, flops=flops, mma_flops=mma_flops)
+    mma_flops = 2.0 * P * H * I * (2 * nt_x + nt_h)
+    return dict(touched=touched, w13_kernel_bytes=w13_kernel, w2_kernel_bytes=w2_kernel, layer_bytes=layer,
+                flops=flops, w13_flops=4.0 * P * H * I, w2_flops=2.0 * P * H * I,
+                w13_mma_flops=4.0 * P * H * I * nt_x, w2_mma_flops=2.0 * P * H * I * nt_h, mma_flops=mma_flops)
 
 
-def w13_traffic_per_launch(alg_bytes: float):
-    """DRAM bytes per W13 launch, scaled from the committed ncu capture of a smaller case by the
-    ratio traffic / algorithmic bytes; None when the kernel sources changed since that capture."""
+def term_counts(moe, desc):
+    """(x terms, h terms) the library uses for this layer, read off its workspace layout."""
+    lay = moe.workspace_layout(desc)
+    R = moe.rows_capacity(desc.T, desc.E, desc.k, desc.block_m)
+    return (lay["xs"] - lay["xq"]) // (R * desc.H), (lay["hs"] - lay["hq"]) // (R * desc.I)
+
+
+KERNEL_NAMES = {"w13": "moe_gemm_kernel<W13*> (grouped W13 GEMM + SiLU*up + h terms)",
+                "w2": "moe_gemm_kernel<W2*> (grouped W2 GEMM)"}
+
+
+def kernel_roofline(name, key, alg, ms, peaks):
+    """Roofline of one GEMM launch (key "w13" or "w2"): bound by HBM or by the tensor pipe,
+    whichever needs more time for the work it executes (all activation terms) at the measured
+    peaks; `achieved` counts the algorithmic (useful) bytes or flops."""
+    hbm, bf16, bf16_sus, kind = peaks
+    mxf8 = MXF8_OVER_BF16 * bf16
+    kernel = KERNEL_NAMES[key]
+    nbytes, flops, mma = alg[f"{key}_kernel_bytes"], alg[f"{key}_flops"], alg[f"{key}_mma_flops"]
+    traffic, source = traffic_per_launch(name, key, nbytes)
+    if mma / (mxf8 * 1e12) > nbytes / (hbm * 1e9):
+        ach = flops / (ms / 1e3) / 1e12
+        r = {"kernel": kernel, "bound": "tensor", "achieved": ach, "peak": mxf8, "unit": "TFLOP/s",
+             "frac": ach / mxf8, "executed_frac": mma / (ms / 1e3) / 1e12 / mxf8,
+             "frac_of_sustained": ach / (MXF8_OVER_BF16 * bf16_sus),
+             "peak_source": f"{kind} bf16_tflops (burst) x {MXF8_OVER_BF16:g}: kind::mxf8f6f4 is nominally twice "
+                            "the dense bf16 rate; achieved counts useful flops, executed_frac all activation terms",
+             "flops_per_launch": flops}
+    else:
+        ach = nbytes / (ms / 1e3) / 1e9
+        r = {"kernel": kernel, "bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
+             "peak_source": f"{kind} hbm_gbs"}
+    r.update({"traffic": traffic, "traffic_source": source, "bytes_per_launch": nbytes, "avg_launch_ms": ms})
+    return r
+
+
+def traffic_per_launch(workload: str, kernel: str, alg_bytes: float):
+    """DRAM bytes per launch of `kernel` on `workload` from the committed ncu table
+    (profiles/traffic.json): measured on that workload itself, or on a smaller case and scaled by
+    the algorithmic bytes. None when the kernel sources changed since the capture or no capture
+    exists."""
     import hashlib
-    path = os.path.join(ROOT, "profiles", "w13_traffic.json")
+    path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
-        return None
+        return None, None
     with open(path) as f:
         d = json.load(f)
     h = hashlib.sha256()
@@ -88,8 +135,13 @@ def w13_traffic_per_launch(alg_bytes: float):
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     if h.hexdigest() != d["kernel_sources_sha256"]:
-        return None
-    return d["traffic_over_algorithmic"] * alg_bytes
+        return None, "kernel sources changed since the ncu capture"
+    for ent in d["entries"]:
+        if ent["workload"] == workload and ent["kernel"] == kernel:
+            if "dram_bytes_per_launch" in ent:
+                return ent["dram_bytes_per_launch"], ent["capture"]
+            return ent["traffic_over_algorithmic"] * alg_bytes, ent["capture"]
+    return None, "no ncu capture of this kernel on this workload"
 
 
 def measured_peaks():
@@ -215,12 +267,18 @@ def load_workload(name: str):
     return synth.make_config(name)
 
 
+def workload_config(name, L, touched):
+    """The `config` object of both arms' JSON lines (identical for the same workload)."""
+    return {"workload": name, "T": L["T"], "H": L["H"], "I": L["I"], "E": L["E"], "k": L["k"], "block_m": 16,
+            "touched_experts": int(touched), "l2": L2_NOTE}
+
+
 def run_reference(args, world, rank):
     if rank != 0:
         return
     import oracle
-    from mxfp4_mixture_experts_top_gb300 import synth
     L = load_workload(args.workload)
+    touched = len(np.unique(oracle.route(L["logits"], L["k"])[0]))
     n_tok = args.ref_tokens
     for _ in range(args.warmup):
         oracle_sample(L, n_tok, 0.0, 1)
@@ -236,8 +294,7 @@ def run_reference(args, world, rank):
         "metric": METRIC, "value": value, "unit": UNIT, "impl": "reference", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f64", "data": "synthetic (seeded splitmix64; sizes of the workload)",
-        "config": {"workload": args.workload, "T": L["T"], "H": L["H"], "I": L["I"], "E": L["E"], "k": L["k"],
-                   "l2": "n/a (CPU)"},
+        "config": workload_config(args.workload, L, touched),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": f"route of all {L['T']} tokens + float64 forward of {n_tok} tokens per step"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -314,16 +371,52 @@ def summarize(evsets):
     return {k: float(np.mean(v)) for k, v in out.items()}, float(np.sum(total)), [float(v) for v in total]
 
 
+def measure_config(moe, name, L, steps, warmup, flush_buf, peaks):
+    """Short run of one workload for `per_config`: step times (L2 flushed before each), the per-kernel
+    event pass, and the rooflines of the layer and of both GEMMs."""
+    import torch
+    hbm, bf16, bf16_sus, _ = peaks
+    lay, _, _, step, mk, fast = time_workload(moe, L, steps, warmup, flush_buf)
+    st = time_fast(fast, flush_buf, steps)
+    ms = float(np.mean(st))
+    evs = [mk() for _ in range(steps)]
+    for ev in evs:
+        flush_buf.zero_()
+        step(ev)
+    torch.cuda.synchronize()
+    assert lay.forward_error() == 0, f"device error in {name}"
+    pk, _, _ = summarize(evs)
+    nt_x, nt_h = term_counts(moe, lay.desc)
+    a = algorithmic(L, lay.bufs["ids"].cpu().numpy(), nt_x, nt_h)
+    mxf8 = MXF8_OVER_BF16 * bf16
+    out = {
+        "tokens_per_s": L["T"] / (ms / 1e3), "ms_per_step": ms, "touched_experts": a["touched"],
+        "activation_terms": {"x": nt_x, "h": nt_h},
+        "step_ms": {"p10": float(np.percentile(st, 10)), "p50": float(np.percentile(st, 50)),
+                    "p90": float(np.percentile(st, 90))},
+        "route_us": 1e3 * pk["route_permute"], "kernel_ms": pk,
+        "layer_roofline": {"bytes": a["layer_bytes"], "hbm_frac": a["layer_bytes"] / (ms / 1e3) / 1e9 / hbm,
+                           "flops": a["flops"],
+                           "mxf8_frac_useful": a["flops"] / (ms / 1e3) / 1e12 / mxf8,
+                           "mxf8_frac_executed": a["mma_flops"] / (ms / 1e3) / 1e12 / mxf8},
+        "w13_roofline": kernel_roofline(name, "w13", a, pk["w13"], peaks),
+        "w2_roofline": kernel_roofline(name, "w2", a, pk["w2"], peaks),
+    }
+    return out, lay, a
+
+
 def run_ours(args, world, rank, local):
     import torch
-    from mxfp4_mixture_experts_top_gb300 import moe, synth
+    from mxfp4_mixture_experts_top_gb300 import moe
     moe.load()
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     props = torch.cuda.get_device_properties(dev)
     l2 = int(getattr(props, "L2_cache_size", 0) or 128 * 1024 * 1024)
     flush_buf = torch.empty(2 * l2 // 4, dtype=torch.float32, device=dev)
-    hbm_peak, bf16_peak, bf16_sus, peak_kind = measured_peaks()
+    peaks = measured_peaks()
+    hbm_peak, bf16_peak, bf16_sus, peak_kind = peaks
+    mxf8 = MXF8_OVER_BF16 * bf16_peak
 
     L = load_workload(args.workload)
     layer, x, logits, step, mk, step_fast = time_workload(moe, L, args.steps, args.warmup, flush_buf)
@@ -334,7 +427,7 @@ def run_ours(args, world, rank, local):
     sampler = ClockSampler(smi_index)
     sampler.start()
     time.sleep(0.3)
-    for _ in range(max(args.warmup, 20)):       # keep the GPU busy while the sampler starts
+    for _ in range(max(args.warmup, 3)):       # keep the GPU busy while the sampler starts
         flush_buf.zero_()
         step_fast()
     torch.cuda.synchronize()
@@ -362,17 +455,12 @@ def run_ours(args, world, rank, local):
     value = world * T / (ms_per_step / 1e3)
 
     ids = layer.bufs["ids"].cpu().numpy()
-    alg = algorithmic(L, ids)
-    w13_ms = per_kernel["w13"]
-    achieved = alg["w13_kernel_bytes"] / (w13_ms / 1e3) / 1e9
-    roofline = {"kernel": "moe_gemm_kernel<W13> (grouped W13 GEMM + SiLU*up)", "bound": "hbm",
-                "achieved": achieved, "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
-                "peak_source": f"{peak_kind} hbm_gbs",
-                "traffic": args.w13_traffic if args.w13_traffic is not None
-                else w13_traffic_per_launch(alg["w13_kernel_bytes"]),
-                "traffic_source": "ncu capture of a 32-expert decode case scaled by algorithmic bytes "
-                                  "(profiles/w13_traffic.json); null if the kernel changed since",
-                "bytes_per_launch": alg["w13_kernel_bytes"], "avg_launch_ms": w13_ms}
+    nt_x, nt_h = term_counts(moe, layer.desc)
+    alg = algorithmic(L, ids, nt_x, nt_h)
+    dominant = "w13" if per_kernel["w13"] >= per_kernel["w2"] else "w2"
+    roofline = kernel_roofline(args.workload, dominant, alg, per_kernel[dominant], peaks)
+    other = kernel_roofline(args.workload, "w2" if dominant == "w13" else "w13", alg,
+                            per_kernel["w2" if dominant == "w13" else "w13"], peaks)
     layer_gbs = alg["layer_bytes"] / (ms_per_step / 1e3) / 1e9
     layer_tflops = alg["flops"] / (ms_per_step / 1e3) / 1e12
 
@@ -424,30 +512,18 @@ def run_ours(args, world, rank, local):
                   "how": "route+permute+forward captured in one CUDA graph, replayed; L2 flushed before each replay"}
     e2e = {"value": world * T / (e2e_ms / 1e3), "unit": UNIT, "ms_per_step": e2e_ms,
            "h2d_bytes_per_step": T * H * 2 + T * E * 4, "d2h_bytes_per_step": T * H * 4}
+    del layer, x, logits, in_dev, x_dev, lg_dev
+    torch.cuda.empty_cache()
 
-    # ---- other workloads (parity-test shapes), short runs for the per-regime picture
+    # ---- the other 4096-wide workloads: shorter runs, each with its own roofline
     per_config = {}
-    if args.all_configs and rank == 0:
-        for name in synth.CONFIG_ORDER:
-            if name == args.workload or name.startswith("tiny"):
+    if rank == 0 and not args.no_per_config:
+        for name in PER_CONFIG:
+            if name == args.workload:
                 continue
-            Lc = synth.make_config(name)
-            lay_c, _, _, step_c, mk_c, fast_c = time_workload(moe, Lc, 10, 3, flush_buf)
-            ms = float(np.mean(time_fast(fast_c, flush_buf, 10)))
-            evs = [mk_c() for _ in range(10)]
-            for i in range(10):
-                flush_buf.zero_()
-                step_c(evs[i])
-            torch.cuda.synchronize()
-            pk, _, _ = summarize(evs)
-            a = algorithmic(Lc, lay_c.bufs["ids"].cpu().numpy())
-            per_config[name] = {
-                "tokens_per_s": Lc["T"] / (ms / 1e3), "ms_per_step": ms, "touched_experts": a["touched"],
-                "layer_hbm_frac": a["layer_bytes"] / (ms / 1e3) / 1e9 / hbm_peak,
-                "layer_mxf8_frac_useful": a["flops"] / (ms / 1e3) / 1e12 / (MXF8_OVER_BF16 * bf16_sus),
-                "layer_mxf8_frac_executed": a["mma_flops"] / (ms / 1e3) / 1e12 / (MXF8_OVER_BF16 * bf16_sus),
-                "w13_hbm_frac": a["w13_kernel_bytes"] / (pk["w13"] / 1e3) / 1e9 / hbm_peak,
-                "route_us": 1e3 * pk["route_permute"], "kernel_ms": pk}
+            n = max(3, min(args.steps, 20))
+            per_config[name], lay_c, _ = measure_config(moe, name, load_workload(name), n, max(3, min(args.warmup, 5)),
+                                                        flush_buf, peaks)
             del lay_c
             torch.cuda.empty_cache()
 
@@ -464,22 +540,22 @@ def run_ours(args, world, rank, local):
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None,
-            "dtype": "mxf8f6f4 (MXFP4 weights E2M1 x E8M0 on tcgen05 block-scaled MMAs; activations as MXFP8 "
-                     "terms: x 2, h 3; fp32 accumulate)",
+            "dtype": f"mxf8f6f4 (MXFP4 weights E2M1 x E8M0 on tcgen05 block-scaled MMAs; activations as MXFP8 "
+                     f"terms: x {nt_x}, h {nt_h}; fp32 accumulate)",
             "data": "synthetic (seeded splitmix64 inputs of the workload's shapes and distributions)",
-            "config": {"workload": args.workload, "T": T, "H": H, "I": I, "E": E, "k": k, "block_m": 16,
-                       "touched_experts": alg["touched"], "l2": f"flushed before every step ({2 * l2 >> 20} MiB write)"},
+            "config": workload_config(args.workload, L, alg["touched"]),
             "route_us_per_layer": 1e3 * per_kernel["route_permute"],
             "kernel_ms": per_kernel,
             "kernel_ms_pass": "separate pass, an event between kernels (each kernel alone); the timed steps "
                               "overlap each kernel's start with the previous kernel's end",
             "layer_roofline": {"bytes": alg["layer_bytes"], "achieved_gbs": layer_gbs, "hbm_frac": layer_gbs / hbm_peak,
                                "flops": alg["flops"], "achieved_tflops": layer_tflops,
-                               "mxf8_peak_tflops": MXF8_OVER_BF16 * bf16_sus,
-                               "mxf8_frac_useful": layer_tflops / (MXF8_OVER_BF16 * bf16_sus),
-                               "mxf8_frac_executed": layer_tflops * alg["mma_flops"] / alg["flops"]
-                                                     / (MXF8_OVER_BF16 * bf16_sus)},
+                               "mxf8_peak_tflops": mxf8,
+                               "mxf8_frac_useful": layer_tflops / mxf8,
+                               "mxf8_frac_executed": layer_tflops * alg["mma_flops"] / alg["flops"] / mxf8,
+                               "mxf8_frac_useful_of_sustained": layer_tflops / (MXF8_OVER_BF16 * bf16_sus)},
             "roofline": roofline,
+            "other_gemm_roofline": other,
             "e2e": e2e,
             "gpu_launches": launches,
             "wall_s_timed": wall,
@@ -502,12 +578,11 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
                     help="a named workload, or custom:T,H,I,E,k (seed 0) for small profiling cases")
-    ap.add_argument("--all-configs", action="store_true", help="also time the other 4096-wide workloads")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the shorter runs of the other 4096-wide workloads (profiling runs)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-tokens", type=int, default=4)
-    ap.add_argument("--w13-traffic", type=float, default=None,
-                    help="DRAM bytes per W13 launch from an ncu capture of this workload (reported as-is)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

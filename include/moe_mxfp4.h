@@ -50,7 +50,7 @@
 extern "C" {
 #endif
 
-#define MOE_ABI_VERSION 2
+#define MOE_ABI_VERSION 3
 
 /* Size of the static scratch array behind moe_mxfp4_forward_noalloc. */
 #define MOE_NOALLOC_SCRATCH_BYTES (32u << 20)
@@ -105,6 +105,14 @@ moe_status_t moe_route(const float *d_logits, int T, int E, int k,
 
 /* Rows of the padded permutation: T*k + min(E, T*k) * (block_m - 1). */
 int64_t moe_permute_rows_capacity(int T, int E, int k, int block_m);
+
+/*
+ * Device workspace bytes moe_permute needs for these sizes: always 0. The
+ * permutation keeps its histograms and scans in shared memory, so the caller
+ * passes no workspace; the function exists so that callers written against a
+ * workspace-taking permutation can size one without special cases.
+ */
+size_t moe_permute_workspace_size(int T, int E, int k, int block_m);
 
 /*
  * Permutation (txtmix.com §三: the per-expert histogram whose padding lanes
@@ -257,8 +265,9 @@ moe_status_t moe_mxfp4_workspace_layout(const moe_layer_desc *desc, size_t out[7
  *   device, with that device current); make that first call before any stream
  *   capture. All calls share the array, which keeps the previous call's
  *   contents (the call clears what it needs cleared): calls whose work overlaps
- *   on the GPU, e.g. on two streams, race on it. The device error word is the
- *   array's first word and is not readable through moe_read_device_error.
+ *   on the GPU, e.g. on two streams, race on it. The forward's device error
+ *   word is the array's first word: read and clear it with
+ *   moe_mxfp4_noalloc_read_device_error.
  */
 moe_status_t moe_mxfp4_forward_noalloc(const moe_layer_desc *desc, const uint16_t *d_x,
                                        const void *d_packed, const float *d_topk_w,
@@ -266,11 +275,33 @@ moe_status_t moe_mxfp4_forward_noalloc(const moe_layer_desc *desc, const uint16_
                                        const int32_t *d_row_to_pair, float *d_y, void *stream);
 
 /*
+ * Read and clear the device error word of moe_mxfp4_forward_noalloc on the
+ * current device (the first word of its static scratch array, which host code
+ * cannot name as a device pointer). Same behaviour as moe_read_device_error:
+ * synchronises `stream`, writes the recorded moe_status_t value (MOE_OK if
+ * none) to *code and resets the word. Allocates nothing. No counterpart in
+ * the source pages.
+ */
+moe_status_t moe_mxfp4_noalloc_read_device_error(int *code, void *stream);
+
+/*
  * Read and clear a device error word (the d_error of moe_permute or the
  * first word of a forward workspace). Synchronises `stream`. Writes the
  * recorded moe_status_t value (MOE_OK if none) to *code.
  */
 moe_status_t moe_read_device_error(void *d_error_word, int *code, void *stream);
+
+/*
+ * Drop the host-side cache of TMA tensor maps (CUtensorMap, 128 bytes each).
+ * moe_mxfp4_forward encodes one map per (device, buffer address, shape, box)
+ * on first use and reuses it on later calls with the same buffers; the cache
+ * holds at most 4096 maps and never owns or touches device memory. Call this
+ * after freeing buffers that a forward used, or to return the host memory;
+ * the next forward re-encodes what it needs. Thread-safe: a forward running
+ * on another thread copies its maps out under the cache lock, so clearing
+ * never leaves it holding a released map.
+ */
+void moe_clear_cache(void);
 
 /* Number of kernels launched by this library since load (all entry points). */
 uint64_t moe_launch_count(void);

@@ -205,6 +205,21 @@ moe_status_t moe_route(const float *d_logits, int T, int E, int k, int32_t *d_to
     return from_cuda(launch_route(d_logits, T, E, k, d_topk_ids, d_topk_w, d_bitmatrix, (cudaStream_t)stream));
 }
 
+size_t moe_permute_workspace_size(int T, int E, int k, int block_m)
+{
+    (void)T;
+    (void)E;
+    (void)k;
+    (void)block_m;
+    return 0;   // the permutation keeps its scratch (histograms, scans) in shared memory
+}
+
+void moe_clear_cache(void)
+{
+    std::lock_guard<std::mutex> lk(g_map_mu);
+    g_maps.clear();
+}
+
 int64_t moe_permute_rows_capacity(int T, int E, int k, int block_m)
 {
     if (T < 0 || E <= 0 || k <= 0 || block_m <= 0) return 0;

@@ -6,8 +6,9 @@
 // plugin whose host framework owns the allocator and hands out no scratch
 // space, or code that must not call cudaMalloc/cudaFree because they can
 // synchronise the device. They still pass their inputs and outputs; only the
-// intermediates (gathered activations, the two-term SiLU product, per-pair W2
-// outputs) live in the array below.
+// intermediates (gathered activation terms, the MXFP8 terms of SiLU(gate)*up,
+// per-pair W2 outputs) and the forward's device error word live in the array
+// below.
 //
 // Cost: every GPU that loads this library holds MOE_NOALLOC_SCRATCH_BYTES of
 // device memory until the process exits. Calls share the array: two calls
@@ -62,4 +63,14 @@ extern "C" moe_status_t moe_mxfp4_forward_noalloc(const moe_layer_desc *desc, co
     // scratch byte it later reads, so stale contents from earlier calls are harmless.
     return moe_mxfp4_forward(desc, d_x, d_packed, d_topk_w, d_offsets, d_padded_offsets, d_row_to_pair, d_y,
                              scratch, (size_t)MOE_NOALLOC_SCRATCH_BYTES, stream);
+}
+
+extern "C" moe_status_t moe_mxfp4_noalloc_read_device_error(int *code, void *stream)
+{
+    if (!code) return MOE_ERR_INVALID_ARG;
+    void *scratch = nullptr;
+    const moe_status_t st = scratch_on_current_device(&scratch);
+    if (st != MOE_OK) return st;
+    // the error word sits at offset 0 of the forward's workspace layout
+    return moe_read_device_error(scratch, code, stream);
 }

@@ -182,15 +182,29 @@ route_permute_kernel(const float *__restrict__ logits, int T, int E, int k, int 
 
 static size_t permute_smem(int E) { return sizeof(int) * ((size_t)PERM_WARPS * E + E + E + 1 + 32); }
 
+// Raise a kernel's dynamic shared-memory limit to what E = 1024 needs, once per device (bit d of *mask);
+// the attribute is a per-function maximum, so smaller launches are unaffected.
+template <typename Kern>
+static cudaError_t allow_permute_smem(Kern kern, unsigned long long *mask)
+{
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if (dev < 64 && ((__atomic_load_n(mask, __ATOMIC_RELAXED) >> dev) & 1ull)) return cudaSuccess;
+    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)permute_smem(1024));
+    if (err == cudaSuccess && dev < 64) __atomic_fetch_or(mask, 1ull << dev, __ATOMIC_RELAXED);
+    return err;
+}
+
 template <int VPL>
 static cudaError_t launch_fused(const float *logits, int T, int E, int k, int block_m, int32_t *ids, float *w,
                                 uint32_t *bitmatrix, int32_t *counts, int32_t *offsets, int32_t *padded,
                                 int32_t *row_to_pair, int64_t rows_cap, int32_t *pair_to_row, int32_t *dev_error,
                                 cudaStream_t s)
 {
+    static unsigned long long attr_set = 0;
     const size_t smem = permute_smem(E);
-    cudaError_t err = cudaFuncSetAttribute(route_permute_kernel<VPL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           (int)smem);
+    cudaError_t err = allow_permute_smem(route_permute_kernel<VPL>, &attr_set);
     if (err != cudaSuccess) return err;
     route_permute_kernel<VPL><<<1, PERM_THREADS, smem, s>>>(logits, T, E, k, block_m, ids, w, bitmatrix, counts,
                                                             offsets, padded, row_to_pair, rows_cap, pair_to_row,
@@ -225,8 +239,9 @@ cudaError_t launch_permute(const int32_t *ids, int T, int E, int k, int block_m,
                            int32_t *offsets, int32_t *padded, int32_t *row_to_pair, int64_t rows_cap,
                            int32_t *pair_to_row, int32_t *dev_error, cudaStream_t s)
 {
-    size_t smem = permute_smem(E);
-    cudaError_t err = cudaFuncSetAttribute(permute_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    static unsigned long long attr_set = 0;
+    const size_t smem = permute_smem(E);
+    cudaError_t err = allow_permute_smem(permute_kernel, &attr_set);
     if (err != cudaSuccess) return err;
     err = launch_ex(permute_kernel, dim3(1), dim3(PERM_THREADS), smem, s, true, ids, T, E, k, block_m, counts,
                     offsets, padded, row_to_pair, rows_cap, pair_to_row, dev_error);

@@ -25,7 +25,8 @@ EXPORTS = ["moe_abi_version", "moe_status_string", "moe_route", "moe_permute_row
            "moe_mxfp4_packed_bytes", "moe_mxfp4_prepack", "moe_mxfp4_dequant_bf16", "moe_mxfp4_workspace_bytes",
            "moe_mxfp4_forward", "moe_mxfp4_forward_timed", "moe_mxfp4_workspace_layout", "moe_read_device_error", "moe_launch_count",
            "moe_selftest_bounded_wait",
-           "moe_mxfp4_forward_noalloc", "moe_route_permute"]
+           "moe_mxfp4_forward_noalloc", "moe_route_permute", "moe_permute_workspace_size", "moe_clear_cache",
+           "moe_mxfp4_noalloc_read_device_error"]
 
 
 class MoeError(RuntimeError):
@@ -73,6 +74,9 @@ def load(path: str = LIB_PATH):
             "moe_selftest_bounded_wait": ([ctypes.c_uint64, ctypes.c_uint64, P, P, P], i32),
             "moe_mxfp4_forward_noalloc": ([D, P, P, P, P, P, P, P, P], i32),
             "moe_route_permute": ([P, i32, i32, i32, i32, P, P, P, P, P, P, P, P, P, P], i32),
+            "moe_permute_workspace_size": ([i32, i32, i32, i32], sz),
+            "moe_clear_cache": ([], None),
+            "moe_mxfp4_noalloc_read_device_error": ([ctypes.POINTER(ctypes.c_int), P], i32),
         }
         for name, (args, res) in sigs.items():
             fn = getattr(lib, name)
@@ -266,6 +270,23 @@ def selftest_bounded_wait(limit_ns: int, abort_after_ns: int, error: torch.Tenso
     _cuda(elapsed, torch.int64, "elapsed")
     _check(load().moe_selftest_bounded_wait(limit_ns, abort_after_ns, _ptr(error), _ptr(elapsed), _stream(stream)),
            "moe_selftest_bounded_wait")
+
+
+def noalloc_read_device_error(stream=None) -> int:
+    """moe_mxfp4_noalloc_read_device_error: read and clear the error word of forward_noalloc."""
+    code = ctypes.c_int(0)
+    _check(load().moe_mxfp4_noalloc_read_device_error(ctypes.byref(code), _stream(stream)),
+           "moe_mxfp4_noalloc_read_device_error")
+    return code.value
+
+
+def clear_cache() -> None:
+    """moe_clear_cache: drop the library's host-side cache of TMA tensor maps."""
+    load().moe_clear_cache()
+
+
+def permute_workspace_size(T: int, E: int, k: int, block_m: int) -> int:
+    return int(load().moe_permute_workspace_size(T, E, k, block_m))
 
 
 def read_device_error(word: torch.Tensor, stream=None) -> int:

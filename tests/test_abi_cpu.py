@@ -35,7 +35,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert moe.abi_version() == 2
+    assert moe.abi_version() == 3
     for s in range(8):
         assert lib.moe_status_string(s)
     assert b"unknown" in lib.moe_status_string(99)
@@ -114,3 +114,18 @@ def test_selftest_bounded_wait_rejects_bad_arguments(lib):
     assert lib.moe_selftest_bounded_wait(2_000_000_000, 0, fake, fake, None) == INVALID    # over 1 s
     assert lib.moe_selftest_bounded_wait(1_000_000, 1_000_000, fake, fake, None) == INVALID  # abort not before limit
     assert lib.moe_selftest_bounded_wait(1_000_000, 0, None, fake, None) == INVALID         # null error word
+
+
+def test_permute_needs_no_workspace_and_cache_clears(lib):
+    """moe_permute_workspace_size is 0 for every shape (scratch lives in shared memory);
+    moe_clear_cache runs without a device and without launching anything."""
+    n0 = moe.launch_count()
+    for T, E, k, bm in [(0, 8, 2, 16), (8, 256, 6, 16), (8191, 256, 6, 128), (100000, 1024, 8, 64)]:
+        assert moe.permute_workspace_size(T, E, k, bm) == 0
+    moe.clear_cache()
+    moe.clear_cache()
+    assert moe.launch_count() == n0
+
+
+def test_noalloc_error_reader_rejects_a_null_code_pointer(lib):
+    assert lib.moe_mxfp4_noalloc_read_device_error(None, None) == 1

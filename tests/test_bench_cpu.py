@@ -31,3 +31,28 @@ def test_algorithmic_counts_touched_experts_and_routed_pairs():
     assert a["flops"] == 6.0 * P * H * I
     # executed: W13 (2I rows) against 2 x terms, W2 (H rows) against 3 h terms
     assert a["mma_flops"] == 2.0 * P * H * I * (2 * 2 + 3)
+
+
+def test_roofline_bound_follows_the_executed_work():
+    """Decode W13 (45 experts, 48 pairs) is HBM-bound; the skewed prefill W13 (17 experts, 49,146
+    pairs, two x terms) is tensor-bound. achieved counts the useful work only."""
+    peaks = (6800.0, 1900.0, 1700.0, "test")
+    T, H, I, E, k = 8, 4096, 2048, 256, 6
+    dec = bench.algorithmic(dict(T=T, H=H, I=I, E=E, k=k), np.arange(T * k).reshape(T, k) % 45)
+    r = bench.kernel_roofline("decode", "w13", dec, 0.1, peaks)
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s"
+    assert abs(r["achieved"] - dec["w13_kernel_bytes"] / 1e-4 / 1e9) < 1e-6 * r["achieved"]
+    T = 8191
+    ids = np.array([[(t + j) % 17 for j in range(k)] for t in range(T)])
+    pre = bench.algorithmic(dict(T=T, H=H, I=I, E=E, k=k), ids)
+    r = bench.kernel_roofline("prefill", "w13", pre, 1.4, peaks)
+    assert r["bound"] == "tensor" and r["unit"] == "TFLOP/s" and r["peak"] == 2 * 1900.0
+    assert abs(r["achieved"] - 4.0 * T * k * H * I / 1.4e-3 / 1e12) < 1e-9 * r["achieved"]
+    assert abs(r["executed_frac"] - 2 * r["frac"]) < 1e-12
+
+
+def test_both_arms_report_the_same_config():
+    L = dict(T=8191, H=4096, I=2048, E=256, k=6)
+    a = bench.workload_config("prefill_t8191_zipf_h4096_e256", L, 17)
+    assert a == bench.workload_config("prefill_t8191_zipf_h4096_e256", dict(L), 17)
+    assert a["workload"] == bench.DEFAULT_WORKLOAD and a["touched_experts"] == 17

@@ -1,11 +1,15 @@
 """GPU parity of the MXFP4 layer: decoder bit-exact, layer output within
 2e-2 * rms of the float64 oracle on every workload.
 
-Small workloads compare every output; the 4096-wide workloads compare every
-output of sampled tokens (the first and last token, random tokens, and tokens
-routed to the most and to the least loaded experts), run in the same launch
-configuration as the benchmark (block_m 16, persistent grid of one CTA per
-SM). Measured error ratios are printed.
+Small workloads compare every output. The 4096-wide workloads compare every
+output of a stratified token set chosen from the oracle's routing so that the
+GEMMs are checked on every expert the batch touches: the last token of each
+touched expert (it sits in that expert's last, partly filled, padded block),
+one token in each 64-row block of the three most loaded experts (every token
+block of the prefill tiles), and the first and last token of the batch. They
+run in the same launch configuration as the benchmark (block_m 16, persistent
+grid of one CTA per SM). Measured error ratios and expert coverage are
+printed.
 """
 import numpy as np
 import pytest
@@ -76,15 +80,48 @@ def _run_layer(moe, gpu_layers, L, block_m=16, swiglu_limit=0.0):
     return dict(y=y, ids=ids, w=w, perm=perm, ws=ws, desc=d, x=x)
 
 
-def _sample_tokens(L, ids, n_random=3, seed=0):
-    T, E = L["T"], L["E"]
-    counts = np.bincount(ids.ravel(), minlength=E)
-    hot = int(np.argmax(counts))
-    rare = int(np.argmin(np.where(counts > 0, counts, 1 << 30)))
-    tok = {0, T - 1, int(np.nonzero((ids == hot).any(1))[0][0]), int(np.nonzero((ids == rare).any(1))[0][-1])}
+def stratified_tokens(ids, block=64, seed=0):
+    """Tokens whose outputs, compared in full, reach every token block of every touched expert.
+
+    Rows of an expert are its tokens in ascending order (the permutation is
+    stable), so cell (e, b) is rows [b*block, (b+1)*block) of expert e. Every
+    cell gets a checked token: first the last token of each touched expert
+    (its last, partly filled, padded block), then, for the cells still
+    uncovered, a token at a seeded position inside the cell; each chosen token
+    covers its cell in all k of its experts. With block = 64 every token block
+    of the 16- to 96-row tiles holds a checked token. Tokens 0 and T-1 are
+    added. Returns (tokens, covered experts, touched experts, cells)."""
+    T, k = ids.shape
     rng = np.random.default_rng(seed)
-    tok.update(int(t) for t in rng.integers(0, T, size=n_random))
-    return np.array(sorted(tok), dtype=np.int32)
+    E = int(ids.max()) + 1
+    rank = np.empty_like(ids)                    # row of pair (t, j) inside its expert's segment
+    for e in range(E):
+        m = ids == e
+        rank[m] = np.arange(int(m.sum()))        # boolean indexing walks (t, j) in row-major order
+    cells = set(zip(ids.ravel().tolist(), (rank.ravel() // block).tolist()))
+    chosen, covered_cells = set(), set()
+
+    def take(t):
+        chosen.add(int(t))
+        covered_cells.update(zip(ids[t].tolist(), (rank[t] // block).tolist()))
+
+    for t in (0, T - 1):
+        take(t)
+    counts = np.bincount(ids.ravel(), minlength=E)
+    touched = np.flatnonzero(counts)
+    for e in touched:
+        take(np.flatnonzero((ids == e).any(1))[-1])
+    for e in np.argsort(-counts, kind="stable"):
+        if counts[e] == 0:
+            break
+        rows = np.flatnonzero((ids == e).any(1))
+        for b in range(-(-len(rows) // block)):
+            if (int(e), b) not in covered_cells:
+                seg = rows[b * block:(b + 1) * block]
+                take(seg[rng.integers(0, len(seg))])
+    assert covered_cells == cells
+    tok = np.array(sorted(chosen), dtype=np.int32)
+    return tok, len(np.unique(ids[tok].ravel())), len(touched), len(cells)
 
 
 def _compare(name, y_gpu, y_ref):
@@ -175,26 +212,39 @@ def test_forward_decode_t8_all_outputs(gpu_lib, gpu_layers):
     _compare("decode t8", r["y"].cpu().numpy(), oracle.forward(L, ids_r, w_r))
 
 
-@pytest.mark.parametrize("name", ["decode_t512_h4096_e256", "prefill_t2048_h4096_e256",
-                                  "prefill_t8191_zipf_h4096_e256"])
-def test_forward_large_sampled_tokens(gpu_lib, gpu_layers, name):
+LARGE = ["decode_t512_h4096_e256", "prefill_t2048_h4096_e256", "prefill_t8191_zipf_h4096_e256"]
+
+
+def _compared_tokens(L, ids_r):
+    """All tokens for the small workloads; the stratified set for the 4096-wide batches."""
+    if L["T"] <= 64:
+        return np.arange(L["T"], dtype=np.int32), None
+    tok, covered, touched, cells = stratified_tokens(ids_r)
+    assert covered == touched, f"stratified set reaches {covered} of {touched} touched experts"
+    return tok, f"{len(tok)} tokens, experts covered {covered}/{touched}, 64-row blocks covered {cells}/{cells}"
+
+
+@pytest.mark.parametrize("name", LARGE)
+def test_forward_large_stratified_tokens(gpu_lib, gpu_layers, name):
     L = synth.make_config(name)
     r = _run_layer(gpu_lib, gpu_layers, L)
     ids_r, w_r, _ = oracle.route(L["logits"], L["k"])
     assert np.array_equal(r["ids"].cpu().numpy(), ids_r)
-    tok = _sample_tokens(L, ids_r)
+    tok, what = _compared_tokens(L, ids_r)
     y = r["y"].cpu().numpy()
     assert np.isfinite(y).all()
-    _compare(f"{name} tokens {tok.tolist()}", y[tok], oracle.forward(L, ids_r, w_r, tokens=tok))
+    _compare(f"{name}: {what}", y[tok], oracle.forward(L, ids_r, w_r, tokens=tok))
 
 
-@pytest.mark.parametrize("name", ["tiny_t37_h512_e32", "decode_t8_h4096_e256"])
+@pytest.mark.parametrize("name", synth.CONFIG_ORDER)
 def test_forward_swiglu_clamp_variant(gpu_lib, gpu_layers, name):
+    """The SwiGLU clamp (limit 10) on every workload, hence on every tile configuration."""
     L = synth.make_config(name)
     r = _run_layer(gpu_lib, gpu_layers, L, swiglu_limit=10.0)
     ids_r, w_r, _ = oracle.route(L["logits"], L["k"])
-    tok = np.arange(min(L["T"], 8), dtype=np.int32)
-    _compare(f"{name} clamp10", r["y"].cpu().numpy()[tok], oracle.forward(L, ids_r, w_r, tokens=tok, swiglu_limit=10.0))
+    tok, what = _compared_tokens(L, ids_r)
+    _compare(f"{name} clamp10: {what or 'all tokens'}", r["y"].cpu().numpy()[tok],
+             oracle.forward(L, ids_r, w_r, tokens=tok, swiglu_limit=10.0))
 
 
 @pytest.mark.parametrize("T,H,I,E,k", [(1, 256, 128, 8, 2), (17, 128, 256, 16, 4), (200, 256, 128, 5, 3),

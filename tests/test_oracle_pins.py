@@ -170,6 +170,52 @@ def test_permute_matches_numpy(T, E, k, block_m):
     assert counts.sum() == T * k
 
 
+def _padded_total(ids, E, block_m):
+    """Rows the padded permutation uses, from numpy's bincount (independent of the oracle)."""
+    c = np.bincount(ids.ravel(), minlength=E)
+    return int((-(-c // block_m) * block_m).sum())
+
+
+@pytest.mark.parametrize("T,E,k,block_m", [(1, 8, 3, 16), (5, 32, 6, 16), (8, 256, 6, 16), (21, 128, 6, 128),
+                                           (37, 256, 6, 64)])
+def test_rows_capacity_attained_when_every_pair_has_its_own_expert(T, E, k, block_m):
+    """T*k <= E pairs on T*k distinct experts: every pair opens a segment padded by block_m - 1
+    rows, so the padded permutation fills the capacity exactly (no smaller bound is valid)."""
+    assert T * k <= E
+    ids = np.random.default_rng(T).permutation(E)[:T * k].reshape(T, k).astype(np.int32)
+    cap = oracle.rows_capacity(T, E, k, block_m)
+    assert _padded_total(ids, E, block_m) == cap == T * k * block_m
+    got = oracle.permute(ids, E, block_m)
+    assert got["padded_offsets"][E] == cap
+
+
+def test_rows_capacity_attained_with_more_pairs_than_experts():
+    """P = 20 pairs on E = 8 experts, block_m = 4, counts (5, 5, 5, 1, 1, 1, 1, 1): every count
+    is 1 mod 4, so all 8 segments carry 3 padding rows: 20 + 8 * 3 = 44 rows, the capacity."""
+    E, k, bm = 8, 2, 4
+    flat = [0] * 5 + [1] * 5 + [2] * 5 + [3, 4, 5, 6, 7]
+    ids = np.array([[flat[t], flat[t + 10]] for t in range(10)], np.int32)
+    assert all(len(set(r)) == k for r in ids.tolist())
+    cap = oracle.rows_capacity(10, E, k, bm)
+    assert _padded_total(ids, E, bm) == cap == 44
+    assert oracle.permute(ids, E, bm)["padded_offsets"][E] == cap
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_rows_capacity_bounds_random_and_skewed_routings(seed):
+    """No routing needs more rows than the capacity (uniform and heavily skewed draws)."""
+    rng = np.random.default_rng(seed)
+    for _ in range(20):
+        E = int(rng.integers(1, 300))
+        k = int(rng.integers(1, min(E, 8) + 1))
+        T = int(rng.integers(0, 400))
+        bm = int(rng.choice([1, 16, 32, 64, 128]))
+        p = rng.random(E) ** (1 + 6 * rng.random())
+        ids = np.stack([rng.choice(E, size=k, replace=False, p=p / p.sum()) for _ in range(T)]).astype(np.int32) \
+            if T else np.zeros((0, k), np.int32)
+        assert _padded_total(ids, E, bm) <= oracle.rows_capacity(T, E, k, bm)
+
+
 def test_permute_rejects_out_of_range_ids():
     with pytest.raises(oracle.OracleError):
         oracle.permute(np.array([[0, 4]], np.int32), 4, 16)
