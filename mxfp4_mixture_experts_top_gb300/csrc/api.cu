@@ -152,6 +152,7 @@ int64_t scale_rows(const moe_layer_desc *d)
 
 Layout workspace_layout(const moe_layer_desc *d)
 {
+    const int NT_H = regime_nt_h(pick_regime(d->T, d->k, d->E));
     const int64_t P = (int64_t)d->T * d->k;
     const int64_t R = moe_permute_rows_capacity(d->T, d->E, d->k, d->block_m);
     const int64_t RS = scale_rows(d);
@@ -376,6 +377,7 @@ moe_status_t moe_mxfp4_forward_timed(const moe_layer_desc *d, const uint16_t *d_
     if (!get_map(&a.tmap_w2, 0, w2, 128, rows2, 1, 128 * sps, 1, &st)) return st;
     if (!get_map(&a.tmap_w2_1, 0, w2, 128, rows2, 1, 128, 1, &st)) return st;
     const uint32_t n13 = (uint32_t)regime_nmax(a.regime, 0), n2 = (uint32_t)regime_nmax(a.regime, 1);
+    const uint64_t NT_H = (uint64_t)regime_nt_h(a.regime);
     const uint64_t s13 = (uint64_t)(d->H / KSLAB), s2 = (uint64_t)(d->I / KSLAB);
     // activation terms and their scale words: a whole stage (sps slabs) per box, and single-slab
     // boxes for a stage that straddles two tiles

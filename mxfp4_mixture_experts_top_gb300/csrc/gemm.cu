@@ -15,7 +15,7 @@
 //     warps copy them into a tensor-memory ring of scale-factor cells. No
 //     instruction of the SM decodes a weight: the tensor core applies the
 //     scales (block_scale, one scale per 32 K-elements, K = 32 per MMA).
-//   * B = the tile's token rows as NT MXFP8 terms (x: 2 terms, h: 3; see
+//   * B = the tile's token rows as NT MXFP8 terms (x: 2 terms, h: 3 or 2; see
 //     mxfp8_terms.cuh), stacked along N: B row t * NMAX + n is term t of token
 //     row n, so one MMA per 32-K block covers all terms and reads A once.
 //   * D = fp32 accumulators in TMEM, double-buffered so the epilogue of one
@@ -24,8 +24,9 @@
 //   * Persistent CTAs (one per SM) walk a tile list built on the device from
 //     the permutation offsets: expert-major, then token block, then weight
 //     row tile, so concurrent CTAs share B tiles in L2.
-//   * W13's epilogue applies SiLU(gate)*up, then splits h into 3 MXFP8 terms
-//     for W2 (block maxima over 32 features span two epilogue warps, which
+//   * W13's epilogue applies SiLU(gate)*up, then splits h into MXFP8 terms
+//     for W2 (3 in the decode tiles, 2 in the tiles for more than 16 rows per
+//     expert; block maxima over 32 features span two epilogue warps, which
 //     exchange them through shared memory).
 //   * Per stage the MMA issuer waits on one barrier (the stage's scale-factor
 //     cell, filled after its weights and activations landed) and makes one
@@ -70,10 +71,12 @@ constexpr int TMEM_COLS = 512;
 // is issued by warp s % MW into its own accumulator sets, so while one warp
 // waits and does its bookkeeping the other keeps the tensor pipe fed. EMAX: most experts the
 // configuration takes (its shared memory holds per-expert tile prefixes, first rows and counts).
-template <int MODE_, int NMAX_, int NT_, int SPS_, int NA_, int NB_, int NSF_, int NACC_, int MW_, int EMAX_ = 1024>
+// NTO: MXFP8 terms of h the W13 epilogue writes (MODE 0; the NT of the matching W2 configuration).
+template <int MODE_, int NMAX_, int NT_, int SPS_, int NA_, int NB_, int NSF_, int NACC_, int MW_, int EMAX_ = 1024,
+          int NTO_ = 3>
 struct Cfg {
     static constexpr int MODE = MODE_, NMAX = NMAX_, NT = NT_, SPS = SPS_, NA = NA_, NB = NB_, NSF = NSF_,
-                         NACC = NACC_, MW = MW_, EMAX = EMAX_;
+                         NACC = NACC_, MW = MW_, EMAX = EMAX_, NTO = NTO_;
     static constexpr int NP = NT * NMAX;                       // MMA N: all terms of NMAX rows
     static constexpr int SFB_COLS = (NP + 31) / 32;            // B scale cells: row j in column j / 32
     static constexpr int SF_COLS = (4 + SFB_COLS + 3) / 4 * 4; // one slab's cells: A (4 columns), then B
@@ -93,27 +96,34 @@ struct Cfg {
     static_assert(MW == 1 || MW == 2, "MMA warps");
 };
 
+// MXFP8 terms of h per regime (regime_nt_h() returns these).
+constexpr int NTH_DECODE = 3, NTH_MID = 2, NTH_LARGE = 2;
+
 // decode, <= 2 rows per expert on average
-using W13Tiny = Cfg<0, 16, NT_X, 2, 5, 4, 6, 1, 2>;
+using W13Tiny = Cfg<0, 16, NT_X, 2, 5, 4, 6, 1, 2, 1024, NTH_DECODE>;
 // W2 is bound by its activation ring as much as by its weight ring: five weight and four activation
 // stages up to 512 experts (the shared memory for more experts' prefixes does not fit), four and
 // four above
-using W2Tiny = Cfg<1, 16, NT_H, 2, 5, 4, 6, 1, 2, 512>;
-using W2TinyWideE = Cfg<1, 16, NT_H, 2, 4, 4, 6, 1, 2>;
+using W2Tiny = Cfg<1, 16, NTH_DECODE, 2, 5, 4, 6, 1, 2, 512>;
+using W2TinyWideE = Cfg<1, 16, NTH_DECODE, 2, 4, 4, 6, 1, 2, 1024>;
 // decode batches: <= 16 rows per expert
-using W13Small = Cfg<0, 32, NT_X, 2, 4, 4, 6, 1, 2>;
-using W2Small = Cfg<1, 32, NT_H, 2, 4, 3, 4, 1, 2>;
+using W13Small = Cfg<0, 32, NT_X, 2, 4, 4, 6, 1, 2, 1024, NTH_DECODE>;
+using W2Small = Cfg<1, 32, NTH_DECODE, 2, 4, 3, 4, 1, 2, 1024>;
 // <= 64 rows per expert
-using W13Mid = Cfg<0, 64, NT_X, 2, 3, 3, 6, 1, 1>;
-using W2Mid = Cfg<1, 64, NT_H, 2, 3, 2, 4, 1, 1>;
+using W13Mid = Cfg<0, 64, NT_X, 2, 3, 3, 6, 1, 1, 1024, NTH_MID>;
+using W2Mid = Cfg<1, 64, NTH_MID, 2, 3, 3, 6, 1, 1, 1024>;
 // prefill
 // (prefill weights are mostly re-read from L2, the activation rows are the bound: a third activation
-// stage up to 512 experts, two above)
-using W13Large = Cfg<0, 96, NT_X, 2, 2, 3, 4, 1, 1, 512>;
-using W2Large = Cfg<1, 64, NT_H, 2, 2, 3, 4, 1, 1, 512>;
-using W13LargeWideE = Cfg<0, 96, NT_X, 2, 3, 2, 4, 1, 1>;
-using W2LargeWideE = Cfg<1, 64, NT_H, 2, 3, 2, 4, 1, 1>;
-static_assert(W13Large::NMAX == 96 && W2Large::NMAX == 64, "regime_nmax() mirrors these");
+// stage up to 512 experts, two above; with h in two terms W2 takes 96 token rows per tile like W13)
+using W13Large = Cfg<0, 96, NT_X, 2, 2, 3, 4, 1, 1, 512, NTH_LARGE>;
+using W2Large = Cfg<1, 96, NTH_LARGE, 2, 2, 3, 4, 1, 1, 512>;
+using W13LargeWideE = Cfg<0, 96, NT_X, 2, 3, 2, 4, 1, 1, 1024, NTH_LARGE>;
+using W2LargeWideE = Cfg<1, 96, NTH_LARGE, 2, 3, 2, 4, 1, 1>;
+static_assert(W13Large::NMAX == 96 && W2Large::NMAX == 96 && W13Mid::NMAX == 64 && W2Mid::NMAX == 64,
+              "regime_nmax() mirrors these");
+static_assert(W13Tiny::NTO == W2Tiny::NT && W13Small::NTO == W2Small::NT && W13Mid::NTO == W2Mid::NT &&
+                  W13Large::NTO == W2Large::NT && W13LargeWideE::NTO == W2LargeWideE::NT,
+              "W2 reads as many h terms as W13 writes");
 
 struct GemmParams {
     CUtensorMap tm_a;         // weight nibbles, box 128 x (128 * SPS) rows
@@ -128,8 +138,8 @@ struct GemmParams {
     int I, H, k;
     float swiglu_limit;
     int64_t P, rows_cap, rows_sf;
-    uint8_t *hq;              // W13 out: h terms [I/128][NT_H][rows_cap][128]
-    uint8_t *hs;              // W13 out: h term scale words [I/128][NT_H][rows_sf], byte = K-block % 4
+    uint8_t *hq;              // W13 out: h terms [I/128][NTO][rows_cap][128]
+    uint8_t *hs;              // W13 out: h term scale words [I/128][NTO][rows_sf], byte = K-block % 4
     float *staging;           // W2 out [P, H]
     int32_t *dev_error;
 };
@@ -670,14 +680,14 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_kernel(const __grid_co
                             const int64_t row = (int64_t)tl.row0 + c0 + (lane >> 4) * 8 + j;
                             float r0 = h[j], r1 = h[j + 1];
 #pragma unroll
-                            for (int term = 0; term < NT_H; ++term) {
+                            for (int term = 0; term < C::NTO; ++term) {
                                 uint32_t sb0, sb1;
                                 const uint32_t q = mxfp8_term_2x(r0, r1, e0, e1, term, sb0, sb1);
-                                uint8_t *dq = p.hq + (((int64_t)(f >> 7) * NT_H + term) * p.rows_cap + row) * 128 + (f & 127);
+                                uint8_t *dq = p.hq + (((int64_t)(f >> 7) * C::NTO + term) * p.rows_cap + row) * 128 + (f & 127);
                                 dq[0] = (uint8_t)q;
                                 dq[128] = (uint8_t)(q >> 8);
                                 if (writes_scale) {
-                                    uint8_t *ds = p.hs + (((int64_t)(blk >> 2) * NT_H + term) * p.rows_sf + row) * 4 + (blk & 3);
+                                    uint8_t *ds = p.hs + (((int64_t)(blk >> 2) * C::NTO + term) * p.rows_sf + row) * 4 + (blk & 3);
                                     ds[0] = (uint8_t)sb0;
                                     ds[4] = (uint8_t)sb1;
                                 }
@@ -732,8 +742,21 @@ __global__ void gather_quant_kernel(const uint16_t *__restrict__ x, const int32_
         const int64_t r = idx / nblk;
         const int b = (int)(idx - r * nblk);
         const int32_t pr = __ldg(row_to_pair + r);
+        if (!(pr >= 0 && pr < P)) {
+            // padding row (or a bad entry, recorded below): an all-zero block, whose terms are zero
+            // bytes with scale byte 0 (the conversion below gives exactly these for zeros)
+            if (pr >= P && b == 0) record_error(dev_error, DEV_ERR_ID_RANGE);
+#pragma unroll
+            for (int t = 0; t < NT_X; ++t) {
+                uint4 *dst = reinterpret_cast<uint4 *>(xq + (((int64_t)(b >> 2) * NT_X + t) * rows_cap + r) * 128 + (b & 3) * 32);
+                dst[0] = make_uint4(0u, 0u, 0u, 0u);
+                dst[1] = make_uint4(0u, 0u, 0u, 0u);
+                xs[(((int64_t)(b >> 2) * NT_X + t) * rows_sf + r) * 4 + (b & 3)] = 0;
+            }
+            continue;
+        }
         float v[32];
-        if (pr >= 0 && pr < P) {
+        {
             const uint4 *src = reinterpret_cast<const uint4 *>(x + (int64_t)(pr / k) * H + b * 32);
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
@@ -745,10 +768,6 @@ __global__ void gather_quant_kernel(const uint16_t *__restrict__ x, const int32_
                     v[q * 8 + 2 * z + 1] = __uint_as_float(w[z] & 0xFFFF0000u);
                 }
             }
-        } else {
-            if (pr >= P && b == 0) record_error(dev_error, DEV_ERR_ID_RANGE);
-#pragma unroll
-            for (int q = 0; q < 32; ++q) v[q] = 0.f;
         }
         float mx = 0.f;
 #pragma unroll
@@ -823,11 +842,22 @@ Regime pick_regime(int T, int k, int E)
 
 int regime_nmax(Regime rg, int which)
 {
+    (void)which;
     switch (rg) {
     case Regime::Tiny: return 16;
     case Regime::Small: return 32;
     case Regime::Mid: return 64;
-    default: return which == 0 ? 96 : 64;
+    default: return 96;
+    }
+}
+
+int regime_nt_h(Regime rg)
+{
+    switch (rg) {
+    case Regime::Tiny:
+    case Regime::Small: return NTH_DECODE;
+    case Regime::Mid: return NTH_MID;
+    default: return NTH_LARGE;
     }
 }
 

@@ -13,9 +13,8 @@ constexpr int DEV_ERR_ID_RANGE = 6;   // MOE_ERR_DEVICE
 constexpr int DEV_ERR_TIMEOUT = 7;    // MOE_ERR_TIMEOUT
 
 // Activations enter the block-scaled GEMMs as sums of MXFP8 terms (mxfp8_terms.cuh):
-// x (bf16) in NT_X terms, h (fp32 SiLU(gate)*up) in NT_H terms.
+// x (bf16) in NT_X terms, h (fp32 SiLU(gate)*up) in regime_nt_h() terms.
 constexpr int NT_X = 2;
-constexpr int NT_H = 3;
 
 // GEMM tile shapes by the average rows per expert (T*k/E): decode batches get
 // small tiles with deep pipelines, prefill batches large tiles.
@@ -23,6 +22,11 @@ enum class Regime { Tiny, Small, Mid, Large };
 Regime pick_regime(int T, int k, int E);
 int regime_nmax(Regime rg, int which);   // token rows per tile; which 0: W13, 1: W2
 int regime_sps(Regime rg);               // K-slabs per weight stage
+// MXFP8 terms of h: 3 (about 12 significant bits) in the decode tiles (at most 16 rows per expert),
+// where the GEMMs stream weights from HBM and the extra term costs little, 2 (about 8 bits, like a
+// bf16 h) in the larger tiles, where every term is operand traffic and tensor work on every weight
+// tile.
+int regime_nt_h(Regime rg);
 
 // Programmatic dependent launch. A kernel launched with `pdl` may start while
 // the previous kernel of the stream still runs. Before it reads or writes
@@ -94,7 +98,7 @@ struct ForwardArgs {
     float *y;
     int32_t *dev_error;
     uint8_t *xq, *xs;      // x terms [H/128][NT_X][rows_cap][128], scale words [H/128][NT_X][rows_sf]
-    uint8_t *hq, *hs;      // h terms [I/128][NT_H][rows_cap][128], scale words [I/128][NT_H][rows_sf]
+    uint8_t *hq, *hs;      // h terms [I/128][nt_h][rows_cap][128], scale words [I/128][nt_h][rows_sf]
     float *staging;
     CUtensorMap tmap_w13, tmap_w13_1, tmap_w2, tmap_w2_1;   // weight nibbles: stage / single-slab boxes
     CUtensorMap tmap_xq, tmap_xq1, tmap_hq, tmap_hq1;      // activation terms: stage / one-slab boxes

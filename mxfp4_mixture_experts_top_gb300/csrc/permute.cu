@@ -1,5 +1,6 @@
 // Per-expert histogram, prefix offsets, block-padded offsets and the stable
-// token permutation, in one thread block.
+// token permutation: one thread block for small batches, many above 4096
+// (token, slot) pairs.
 //
 // Method: "DeepSeek V4 Flash 单卡 MI300X" (txtmix.com) §三 — the expert
 // histogram is built over a padded, block-aligned layout, and lanes past the
@@ -180,7 +181,183 @@ route_permute_kernel(const float *__restrict__ logits, int T, int E, int k, int 
     permute_block(s_ids, T, E, k, block_m, counts, offsets, padded, row_to_pair, rows_cap, pair_to_row, dev_error);
 }
 
+// ---------------------------------------------------------------------------------------------
+// Multi-block permutation for large batches. Block b owns experts [8b, 8b + 8). Every block builds
+// the histogram of all experts itself (the ids are a few hundred KB, read from L2), so it knows
+// every padded start without a workspace or any wait on another block; block 0 writes counts,
+// offsets and padded offsets. Then each block walks all pairs in chunks of PM_CHUNK and scatters
+// the pairs of its own experts: warp w of a chunk takes PM_SUB runs of 32 consecutive pairs and
+// ranks each pair among the earlier pairs of its expert in the warp with one ballot per owned
+// expert; a scan over the warps per expert adds the earlier warps of the chunk and the earlier
+// chunks. Rows come out in ascending pair order inside each expert segment, bit-identical to the
+// one-block kernel. The same two-sided lane mask applies: a lane counts only if it is inside its
+// run and below T*k. (__match_any_sync, whose cost grows with the number of distinct experts in a
+// warp, is avoided here: the histogram uses plain shared-memory adds, which conflict only where
+// lanes share an expert.)
+constexpr int PM_EPB = 8;                        // experts per block
+constexpr int PM_SUB = 8;                        // runs of 32 pairs per warp and chunk
+constexpr int PM_CHUNK = PERM_THREADS * PM_SUB;  // pairs per chunk
+// Above this many pairs the permutation runs on many blocks.
+constexpr int64_t PERMUTE_MULTI_MIN_PAIRS = 4096;
+
+__global__ void __launch_bounds__(PERM_THREADS, 1)
+permute_multi_kernel(const int32_t *__restrict__ ids, int T, int E, int k, int block_m,
+                     int32_t *__restrict__ counts, int32_t *__restrict__ offsets, int32_t *__restrict__ padded,
+                     int32_t *__restrict__ row_to_pair, int64_t rows_cap, int32_t *__restrict__ pair_to_row,
+                     int32_t *__restrict__ dev_error)
+{
+    griddep_wait();                   // ids come from the kernel before (launched with pdl)
+    griddep_launch_dependents();
+    extern __shared__ int smem[];
+    int *cnt = smem;                           // [E]
+    int *pad_start = cnt + E;                  // [E + 1]
+    int *warp_tot = pad_start + E + 1;         // [32]
+    __shared__ int wcnt[PERM_WARPS][PM_EPB];   // pairs of each local expert in each warp's runs
+    __shared__ int wbase[PERM_WARPS][PM_EPB];  // rows before each warp's first pair of the expert
+    __shared__ int run[PM_EPB];                // rows of the expert filled by earlier chunks
+    __shared__ int s_err;
+
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    const int64_t P = (int64_t)T * k;
+    const int e0 = blockIdx.x * PM_EPB;
+    const int ne = E - e0 < PM_EPB ? E - e0 : PM_EPB;
+    const unsigned lt_mask = (1u << lane) - 1u;
+
+    for (int i = tid; i < E; i += PERM_THREADS) cnt[i] = 0;
+    if (tid < PM_EPB) run[tid] = 0;
+    if (tid == 0) s_err = 0;
+    __syncthreads();
+
+    // Phase A: histogram of all experts. The ids of the next chunk are loaded before the current
+    // chunk is counted, so the loads of one chunk overlap the adds of the one before.
+    int nxt[PM_SUB];
+#pragma unroll
+    for (int sub = 0; sub < PM_SUB; ++sub) {
+        const int64_t p = (int64_t)sub * PERM_THREADS + tid;
+        nxt[sub] = p < P ? __ldg(ids + p) : -1;
+    }
+    for (int64_t base = 0; base < P; base += PM_CHUNK) {
+        int ev[PM_SUB];
+#pragma unroll
+        for (int sub = 0; sub < PM_SUB; ++sub) {
+            ev[sub] = nxt[sub];
+            const int64_t p = base + PM_CHUNK + (int64_t)sub * PERM_THREADS + tid;
+            nxt[sub] = p < P ? __ldg(ids + p) : -1;
+        }
+#pragma unroll
+        for (int sub = 0; sub < PM_SUB; ++sub) {
+            const int64_t p = base + (int64_t)sub * PERM_THREADS + tid;
+            const int e = ev[sub];
+            if (p < P) {
+                if (e >= 0 && e < E) {
+                    atomicAdd(&cnt[e], 1);
+                } else {
+                    s_err = 1;
+                    if (blockIdx.x == 0) pair_to_row[p] = -1;
+                }
+            }
+        }
+    }
+    __syncthreads();
+
+    // Phase B: offsets and padded offsets (E <= 1024: one expert per thread).
+    const int c = tid < E ? cnt[tid] : 0;
+    const int pc = (c + block_m - 1) / block_m * block_m;
+    const int inc_c = block_inclusive_scan(c, warp_tot);
+    const int inc_p = block_inclusive_scan(pc, warp_tot);
+    if (tid < E) {
+        pad_start[tid + 1] = inc_p;
+        if (blockIdx.x == 0) {
+            counts[tid] = c;
+            offsets[tid + 1] = inc_c;
+            padded[tid + 1] = inc_p;
+        }
+    }
+    if (tid == 0) {
+        pad_start[0] = 0;
+        if (blockIdx.x == 0) {
+            offsets[0] = 0;
+            padded[0] = 0;
+        }
+    }
+    __syncthreads();
+
+    // Phase C: stable scatter of this block's experts, chunk by chunk (the next chunk's ids are
+    // loaded while the current chunk is ranked). Lane j < PM_EPB keeps the warp's running count of
+    // local expert j in this chunk.
+#pragma unroll
+    for (int sub = 0; sub < PM_SUB; ++sub) {
+        const int64_t p = ((int64_t)wid * PM_SUB + sub) * 32 + lane;
+        nxt[sub] = p < P ? __ldg(ids + p) : -1;
+    }
+    for (int64_t base = 0; base < P; base += PM_CHUNK) {
+        int el_s[PM_SUB], rank_s[PM_SUB];
+#pragma unroll
+        for (int sub = 0; sub < PM_SUB; ++sub) {
+            el_s[sub] = nxt[sub];
+            const int64_t p = base + PM_CHUNK + ((int64_t)wid * PM_SUB + sub) * 32 + lane;
+            nxt[sub] = p < P ? __ldg(ids + p) : -1;
+        }
+        int mine = 0;                                   // lane j: pairs of local expert j so far
+#pragma unroll
+        for (int sub = 0; sub < PM_SUB; ++sub) {
+            const int e = el_s[sub];                    // -1 past T*k (the load above masks it)
+            const int el = (e >= e0 && e < e0 + ne) ? e - e0 : -1;
+            unsigned same = 0u;
+            int add = 0;
+#pragma unroll
+            for (int j = 0; j < PM_EPB; ++j) {
+                const unsigned b = __ballot_sync(0xFFFFFFFFu, el == j);
+                if (el == j) same = b;
+                if (lane == j) add = __popc(b);
+            }
+            const int before = __shfl_sync(0xFFFFFFFFu, mine, el >= 0 ? el : 0);
+            el_s[sub] = el;
+            rank_s[sub] = before + __popc(same & lt_mask);
+            mine += add;
+        }
+        if (lane < PM_EPB) wcnt[wid][lane] = mine;
+        __syncthreads();
+        if (wid < ne) {                       // warp j scans local expert j over the 32 warps
+            const int v = wcnt[lane][wid];
+            int incl = v;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int n = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+                if (lane >= o) incl += n;
+            }
+            const int r = run[wid];
+            wbase[lane][wid] = r + incl - v;
+            const int tot = __shfl_sync(0xFFFFFFFFu, incl, 31);
+            __syncwarp();
+            if (lane == 0) run[wid] = r + tot;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int sub = 0; sub < PM_SUB; ++sub) {
+            if (el_s[sub] >= 0) {
+                const int64_t p = base + ((int64_t)wid * PM_SUB + sub) * 32 + lane;
+                const int row = pad_start[e0 + el_s[sub]] + wbase[wid][el_s[sub]] + rank_s[sub];
+                row_to_pair[row] = (int32_t)p;
+                pair_to_row[p] = row;
+            }
+        }
+    }
+
+    // Phase D: padding rows of this block's experts; the tail up to rows_cap split over all blocks.
+    for (int j = 0; j < ne; ++j) {
+        const int e = e0 + j;
+        for (int r = pad_start[e] + cnt[e] + tid; r < pad_start[e + 1]; r += PERM_THREADS) row_to_pair[r] = -1;
+    }
+    for (int64_t r = pad_start[E] + (int64_t)blockIdx.x * PERM_THREADS + tid; r < rows_cap;
+         r += (int64_t)gridDim.x * PERM_THREADS)
+        row_to_pair[r] = -1;
+    __syncthreads();
+    if (blockIdx.x == 0 && tid == 0 && s_err && dev_error) atomicExch(dev_error, DEV_ERR_ID_RANGE);
+}
+
 static size_t permute_smem(int E) { return sizeof(int) * ((size_t)PERM_WARPS * E + E + E + 1 + 32); }
+static size_t permute_multi_smem(int E) { return sizeof(int) * ((size_t)E + E + 1 + 32); }
 
 // Raise a kernel's dynamic shared-memory limit to what E = 1024 needs, once per device (bit d of *mask);
 // the attribute is a per-function maximum, so smaller launches are unaffected.
@@ -239,6 +416,14 @@ cudaError_t launch_permute(const int32_t *ids, int T, int E, int k, int block_m,
                            int32_t *offsets, int32_t *padded, int32_t *row_to_pair, int64_t rows_cap,
                            int32_t *pair_to_row, int32_t *dev_error, cudaStream_t s)
 {
+    if ((int64_t)T * k > PERMUTE_MULTI_MIN_PAIRS) {
+        const int blocks = (E + PM_EPB - 1) / PM_EPB;
+        cudaError_t err = launch_ex(permute_multi_kernel, dim3(blocks), dim3(PERM_THREADS), permute_multi_smem(E), s,
+                                    true, ids, T, E, k, block_m, counts, offsets, padded, row_to_pair, rows_cap,
+                                    pair_to_row, dev_error);
+        note_launch(1);
+        return err;
+    }
     static unsigned long long attr_set = 0;
     const size_t smem = permute_smem(E);
     cudaError_t err = allow_permute_smem(permute_kernel, &attr_set);

@@ -167,3 +167,63 @@ def test_fused_route_permute_matches_oracle(gpu_lib, T, E, k, block_m):
     np.testing.assert_array_equal(perm["row_to_pair"].cpu().numpy()[:cap], ref["row_to_pair"])
     np.testing.assert_array_equal(perm["pair_to_row"].cpu().numpy()[:T * k], ref["pair_to_row"])
     assert gpu_lib.read_device_error(err) == 0
+
+
+@pytest.mark.parametrize("T,E,k,block_m,skew", [
+    (683, 256, 6, 16, 0.0),        # 4098 pairs: just past the one-block limit
+    (1366, 37, 6, 128, 8.0),       # 8196 pairs: a second chunk of 4 pairs; E not a multiple of 8
+    (1024, 8, 8, 64, 0.0),         # 8192 pairs: exactly one chunk
+    (8191, 256, 6, 16, 30.0),      # one expert takes nearly every token
+    (3000, 1024, 32, 16, 2.0),     # 96,000 pairs over 1024 experts (128 blocks)
+    (20000, 5, 5, 32, 0.0),        # every token picks every expert
+])
+def test_multi_block_permute_guards_and_skew(gpu_lib, T, E, k, block_m, skew):
+    """The many-block permutation (more than 4096 pairs) is bit-exact and writes nothing past
+    its outputs: every output carries guard words after its logical end."""
+    moe = gpu_lib
+    rng = np.random.default_rng(T + E)
+    if k == E:
+        ids = np.stack([rng.permutation(E) for _ in range(T)]).astype(np.int32)
+    else:
+        p = np.exp(skew * rng.random(E))
+        ids = np.stack([rng.choice(E, size=k, replace=False, p=p / p.sum()) for _ in range(T)]).astype(np.int32)
+    GUARD = -987654321
+    cap = oracle.rows_capacity(T, E, k, block_m)
+    out = dict(counts=torch.full((E + 16,), GUARD, dtype=torch.int32, device="cuda"),
+               offsets=torch.full((E + 17,), GUARD, dtype=torch.int32, device="cuda"),
+               padded_offsets=torch.full((E + 17,), GUARD, dtype=torch.int32, device="cuda"),
+               row_to_pair=torch.full((cap + 64,), GUARD, dtype=torch.int32, device="cuda"),
+               pair_to_row=torch.full((T * k + 64,), GUARD, dtype=torch.int32, device="cuda"))
+    err = torch.zeros(4, dtype=torch.int32, device="cuda")
+    moe.permute(torch.from_numpy(ids).cuda(), E, block_m, out=out, error=err)
+    torch.cuda.synchronize()
+    ref = oracle.permute(ids, E, block_m)
+    np.testing.assert_array_equal(out["counts"][:E].cpu().numpy(), ref["counts"])
+    np.testing.assert_array_equal(out["offsets"][:E + 1].cpu().numpy(), ref["offsets"])
+    np.testing.assert_array_equal(out["padded_offsets"][:E + 1].cpu().numpy(), ref["padded_offsets"])
+    np.testing.assert_array_equal(out["row_to_pair"][:cap].cpu().numpy(), ref["row_to_pair"])
+    np.testing.assert_array_equal(out["pair_to_row"][:T * k].cpu().numpy(), ref["pair_to_row"])
+    for name, n in (("counts", E), ("offsets", E + 1), ("padded_offsets", E + 1), ("row_to_pair", cap),
+                    ("pair_to_row", T * k)):
+        assert (out[name][n:].cpu().numpy() == GUARD).all(), name
+    assert moe.read_device_error(err) == 0
+
+
+def test_multi_block_permute_reports_out_of_range_ids(gpu_lib):
+    moe = gpu_lib
+    T, E, k = 1000, 64, 6
+    rng = np.random.default_rng(5)
+    ids = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+    ids[17, 2] = E + 3
+    ids[901, 0] = -2
+    err = torch.zeros(4, dtype=torch.int32, device="cuda")
+    out = moe.permute(torch.from_numpy(ids).cuda(), E, 16, error=err)
+    torch.cuda.synchronize()
+    assert moe.read_device_error(err) == 6
+    p2r = out["pair_to_row"].cpu().numpy()
+    assert p2r[17 * k + 2] == -1 and p2r[901 * k] == -1
+    good = ids.ravel()[(ids.ravel() >= 0) & (ids.ravel() < E)]
+    np.testing.assert_array_equal(out["counts"].cpu().numpy(), np.bincount(good, minlength=E))
+    r2p = out["row_to_pair"].cpu().numpy()
+    real = r2p[r2p >= 0]
+    assert len(real) == T * k - 2 and (p2r[real] >= 0).all()
