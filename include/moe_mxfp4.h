@@ -209,9 +209,9 @@ size_t moe_mxfp4_workspace_bytes(const moe_layer_desc *desc);
  * E2M1 weights with their E8M0 scales against the activations written as sums
  * of MXFP8 terms (E4M3 values, one E8M0 scale per 32 K-elements, term scales
  * 2^-4 apart): x in 2 terms (exact for bf16 unless a 32-element block spans
- * more than 2^17), SiLU(gate)*up in 3 terms (about 12 significant bits);
+ * more than 2^17), SiLU(gate)*up in 2 terms (about 8 significant bits, a bf16 h);
  * fp32 accumulation; output fp32. Result within 2e-2 * rms of the float64
- * oracle (measured errors are about 1e-4 * rms).
+ * oracle (measured errors are up to about 4e-3 * rms).
  * Launches 4 kernels on `stream`; deterministic (bit-identical reruns). The
  * GEMMs stream their weights before the kernel ahead of them has finished.
  */
@@ -241,8 +241,9 @@ moe_status_t moe_mxfp4_forward_timed(const moe_layer_desc *desc, const uint16_t 
  * [H/128][2][R][128]: 128-element slab, term, permutation row, element);
  * out[2] their E8M0 scales as 32-bit words [H/128][2][RS] (byte b of a word:
  * 32-element block b of the slab; RS = R rounded up to 4); out[3]
- * SiLU(gate)*up terms (E4M3 [I/128][3][R][128]); out[4] their scale words
- * ([I/128][3][RS]); out[5] per-pair W2 outputs (fp32 [T*k, H]); out[6] total
+ * SiLU(gate)*up terms (E4M3 [I/128][NH][R][128], NH = 2 in this build:
+ * (out[4] - out[3]) / (R * I) rounded down); out[4] their scale words
+ * ([I/128][NH][RS]); out[5] per-pair W2 outputs (fp32 [T*k, H]); out[6] total
  * bytes. R = moe_permute_rows_capacity(T, E, k, block_m). An element's value
  * is the sum over terms of E4M3 value * 2^(scale byte - 127). */
 moe_status_t moe_mxfp4_workspace_layout(const moe_layer_desc *desc, size_t out[7]);
@@ -260,7 +261,7 @@ moe_status_t moe_mxfp4_workspace_layout(const moe_layer_desc *desc, size_t out[7
  *   routine).
  *   Returns MOE_ERR_WORKSPACE when moe_mxfp4_workspace_bytes(desc) exceeds
  *   MOE_NOALLOC_SCRATCH_BYTES (e.g. H = 4096, I = 2048, E = 256, k = 6,
- *   block_m = 16 fits up to T = 22 tokens); use moe_mxfp4_forward for larger layers.
+ *   block_m = 16 fits up to T = 25 tokens); use moe_mxfp4_forward for larger layers.
  *   The first call on a device looks up the array's device address (once per
  *   device, with that device current); make that first call before any stream
  *   capture. All calls share the array, which keeps the previous call's
@@ -283,6 +284,40 @@ moe_status_t moe_mxfp4_forward_noalloc(const moe_layer_desc *desc, const uint16_
  * the source pages.
  */
 moe_status_t moe_mxfp4_noalloc_read_device_error(int *code, void *stream);
+
+/*
+ * Expert parallelism over G ranks (experts split in contiguous ranges of
+ * experts_per_rank = E / G; rank g owns experts [g*EPR, (g+1)*EPR)). The layer
+ * is that of txtmix.com §一 and §三; the pages run it on one GPU, so the
+ * sharding has no counterpart there: the data movement below plus two
+ * all-to-alls (the caller's collective library) distribute exactly the
+ * single-GPU computation. A rank:
+ *   1. routes and permutes its own T tokens (moe_route_permute, all E experts);
+ *   2. moe_ep_dispatch_pack: send row i (i < T*k) is the bf16 activation row of
+ *      the i-th pair in (expert, token) order, i.e. of pair
+ *      row_to_pair[padded[e] + i - offsets[e]] for the e with
+ *      offsets[e] <= i < offsets[e+1]; d_send_local_ids[i] = e % EPR. Rank g's
+ *      rows are the contiguous run offsets[g*EPR] .. offsets[(g+1)*EPR].
+ *      d_send_x bf16 bits [T*k, H]; d_send_local_ids int32 [T*k]. H % 8 == 0.
+ *   3. exchanges the runs (all-to-all), runs moe_permute + moe_mxfp4_forward on
+ *      the received rows with k = 1, E = EPR, weight 1 (the per-pair expert
+ *      outputs), and sends them back (all-to-all) in the order received;
+ *   4. moe_ep_combine: y[t] = sum_j topk_w[t,j] * returned[pos(t,j)] in slot
+ *      order, pos(p) = offsets[e] + pair_to_row[p] - padded[e]: d_returned fp32
+ *      [T*k, H] in send order, y fp32 [T, H] fully written. A pair with an id
+ *      outside [0, E) or no row adds nothing and sets *d_error (nullable) to
+ *      MOE_ERR_DEVICE. H % 4 == 0.
+ * Both take the outputs of step 1 (offsets, padded offsets, row_to_pair or
+ * pair_to_row, ids, weights) as device pointers and run on `stream`.
+ */
+moe_status_t moe_ep_dispatch_pack(const uint16_t *d_x, int T, int H, int E, int k, int experts_per_rank,
+                                  const int32_t *d_offsets, const int32_t *d_padded_offsets,
+                                  const int32_t *d_row_to_pair, uint16_t *d_send_x,
+                                  int32_t *d_send_local_ids, void *stream);
+moe_status_t moe_ep_combine(const float *d_returned, int T, int H, int E, int k,
+                            const int32_t *d_topk_ids, const float *d_topk_w,
+                            const int32_t *d_offsets, const int32_t *d_padded_offsets,
+                            const int32_t *d_pair_to_row, float *d_y, int32_t *d_error, void *stream);
 
 /*
  * Read and clear a device error word (the d_error of moe_permute or the

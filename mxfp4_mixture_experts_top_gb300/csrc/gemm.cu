@@ -15,7 +15,7 @@
 //     warps copy them into a tensor-memory ring of scale-factor cells. No
 //     instruction of the SM decodes a weight: the tensor core applies the
 //     scales (block_scale, one scale per 32 K-elements, K = 32 per MMA).
-//   * B = the tile's token rows as NT MXFP8 terms (x: 2 terms, h: 3 or 2; see
+//   * B = the tile's token rows as NT MXFP8 terms (x: 2 terms, h: 2; see
 //     mxfp8_terms.cuh), stacked along N: B row t * NMAX + n is term t of token
 //     row n, so one MMA per 32-K block covers all terms and reads A once.
 //   * D = fp32 accumulators in TMEM, double-buffered so the epilogue of one
@@ -24,9 +24,8 @@
 //   * Persistent CTAs (one per SM) walk a tile list built on the device from
 //     the permutation offsets: expert-major, then token block, then weight
 //     row tile, so concurrent CTAs share B tiles in L2.
-//   * W13's epilogue applies SiLU(gate)*up, then splits h into MXFP8 terms
-//     for W2 (3 in the decode tiles, 2 in the tiles for more than 16 rows per
-//     expert; block maxima over 32 features span two epilogue warps, which
+//   * W13's epilogue applies SiLU(gate)*up, then splits h into two MXFP8 terms
+//     for W2 (block maxima over 32 features span two epilogue warps, which
 //     exchange them through shared memory).
 //   * Per stage the MMA issuer waits on one barrier (the stage's scale-factor
 //     cell, filled after its weights and activations landed) and makes one
@@ -96,15 +95,17 @@ struct Cfg {
     static_assert(MW == 1 || MW == 2, "MMA warps");
 };
 
-// MXFP8 terms of h per regime (regime_nt_h() returns these).
-constexpr int NTH_DECODE = 3, NTH_MID = 2, NTH_LARGE = 2;
+// MXFP8 terms of h per regime (regime_nt_h() returns these): two everywhere, about 8 significant bits,
+// the precision of a bf16 h. A third term (about 12 bits) was measured at 2-3 % more decode time and
+// a third more W2 time in prefill.
+constexpr int NTH_DECODE = 2, NTH_MID = 2, NTH_LARGE = 2;
 
 // decode, <= 2 rows per expert on average
 using W13Tiny = Cfg<0, 16, NT_X, 2, 5, 4, 6, 1, 2, 1024, NTH_DECODE>;
-// W2 is bound by its activation ring as much as by its weight ring: five weight and four activation
+// W2 is bound by its activation ring as much as by its weight ring: five weight and five activation
 // stages up to 512 experts (the shared memory for more experts' prefixes does not fit), four and
 // four above
-using W2Tiny = Cfg<1, 16, NTH_DECODE, 2, 5, 4, 6, 1, 2, 512>;
+using W2Tiny = Cfg<1, 16, NTH_DECODE, 2, 5, 5, 6, 1, 2, 512>;
 using W2TinyWideE = Cfg<1, 16, NTH_DECODE, 2, 4, 4, 6, 1, 2, 1024>;
 // decode batches: <= 16 rows per expert
 using W13Small = Cfg<0, 32, NT_X, 2, 4, 4, 6, 1, 2, 1024, NTH_DECODE>;
@@ -203,8 +204,8 @@ __device__ __forceinline__ Tile decode_tile(int t, const int *tile_start, int E,
     return r;
 }
 
-// SiLU(g) = g / (1 + e^-g) with the fast exp and divide (about 1e-6 relative error; h then keeps about
-// 12 bits in its three terms). For g < -88, e^-g is +inf and the quotient is -0.
+// SiLU(g) = g / (1 + e^-g) with the fast exp and divide (about 1e-6 relative error, far below the 8
+// bits h keeps in its two terms). For g < -88, e^-g is +inf and the quotient is -0.
 __device__ __forceinline__ float silu_f(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
 
 template <class C>

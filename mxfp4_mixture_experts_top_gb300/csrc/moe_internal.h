@@ -22,10 +22,8 @@ enum class Regime { Tiny, Small, Mid, Large };
 Regime pick_regime(int T, int k, int E);
 int regime_nmax(Regime rg, int which);   // token rows per tile; which 0: W13, 1: W2
 int regime_sps(Regime rg);               // K-slabs per weight stage
-// MXFP8 terms of h: 3 (about 12 significant bits) in the decode tiles (at most 16 rows per expert),
-// where the GEMMs stream weights from HBM and the extra term costs little, 2 (about 8 bits, like a
-// bf16 h) in the larger tiles, where every term is operand traffic and tensor work on every weight
-// tile.
+// MXFP8 terms of h (gemm.cu sets them per tile regime; currently two, about 8 significant bits, the
+// precision of a bf16 h).
 int regime_nt_h(Regime rg);
 
 // Programmatic dependent launch. A kernel launched with `pdl` may start while

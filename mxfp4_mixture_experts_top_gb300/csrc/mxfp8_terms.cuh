@@ -13,7 +13,7 @@
 // the next scale, 2^-4 smaller, holds without saturation.
 // A bf16 value (8 significant bits) is represented exactly by two terms
 // unless the block's magnitudes span more than E4M3's 2^17 range; an fp32
-// value keeps about 12 bits with three terms.
+// value keeps about 8 bits with two terms and about 12 with three.
 #pragma once
 #include <cuda_fp16.h>
 

@@ -26,7 +26,7 @@ EXPORTS = ["moe_abi_version", "moe_status_string", "moe_route", "moe_permute_row
            "moe_mxfp4_forward", "moe_mxfp4_forward_timed", "moe_mxfp4_workspace_layout", "moe_read_device_error", "moe_launch_count",
            "moe_selftest_bounded_wait",
            "moe_mxfp4_forward_noalloc", "moe_route_permute", "moe_permute_workspace_size", "moe_clear_cache",
-           "moe_mxfp4_noalloc_read_device_error"]
+           "moe_mxfp4_noalloc_read_device_error", "moe_ep_dispatch_pack", "moe_ep_combine"]
 
 
 class MoeError(RuntimeError):
@@ -77,6 +77,8 @@ def load(path: str = LIB_PATH):
             "moe_permute_workspace_size": ([i32, i32, i32, i32], sz),
             "moe_clear_cache": ([], None),
             "moe_mxfp4_noalloc_read_device_error": ([ctypes.POINTER(ctypes.c_int), P], i32),
+            "moe_ep_dispatch_pack": ([P, i32, i32, i32, i32, i32, P, P, P, P, P, P], i32),
+            "moe_ep_combine": ([P, i32, i32, i32, i32, P, P, P, P, P, P, P, P], i32),
         }
         for name, (args, res) in sigs.items():
             fn = getattr(lib, name)
@@ -270,6 +272,38 @@ def selftest_bounded_wait(limit_ns: int, abort_after_ns: int, error: torch.Tenso
     _cuda(elapsed, torch.int64, "elapsed")
     _check(load().moe_selftest_bounded_wait(limit_ns, abort_after_ns, _ptr(error), _ptr(elapsed), _stream(stream)),
            "moe_selftest_bounded_wait")
+
+
+def ep_dispatch_pack(x: torch.Tensor, perm: dict, k: int, experts_per_rank: int, send_x=None, send_ids=None,
+                     stream=None):
+    """moe_ep_dispatch_pack: the activation rows of the T*k pairs in (expert, token) order, and their
+    experts as ids local to the owning rank. Returns (send_x bf16 [T*k, H], send_ids int32 [T*k])."""
+    _cuda(x, torch.bfloat16, "x")
+    T, H = x.shape
+    E = perm["counts"].numel()
+    if send_x is None:
+        send_x = torch.empty((T * k, H), dtype=torch.bfloat16, device=x.device)
+    if send_ids is None:
+        send_ids = torch.empty(max(T * k, 1), dtype=torch.int32, device=x.device)
+    _check(load().moe_ep_dispatch_pack(_ptr(x), T, H, E, k, experts_per_rank, _ptr(perm["offsets"]),
+                                       _ptr(perm["padded_offsets"]), _ptr(perm["row_to_pair"]), _ptr(send_x),
+                                       _ptr(send_ids), _stream(stream)), "moe_ep_dispatch_pack")
+    return send_x, send_ids
+
+
+def ep_combine(returned: torch.Tensor, topk_ids: torch.Tensor, topk_w: torch.Tensor, perm: dict, y=None, error=None,
+               stream=None) -> torch.Tensor:
+    """moe_ep_combine: y[t] = sum_j w[t, j] * returned[row of pair (t, j) in send order], slots ascending."""
+    _cuda(returned, torch.float32, "returned")
+    T, k = topk_ids.shape
+    H = returned.shape[1]
+    E = perm["counts"].numel()
+    if y is None:
+        y = torch.empty((T, H), dtype=torch.float32, device=returned.device)
+    _check(load().moe_ep_combine(_ptr(returned), T, H, E, k, _ptr(topk_ids), _ptr(topk_w), _ptr(perm["offsets"]),
+                                 _ptr(perm["padded_offsets"]), _ptr(perm["pair_to_row"]), _ptr(y), _ptr(error),
+                                 _stream(stream)), "moe_ep_combine")
+    return y
 
 
 def noalloc_read_device_error(stream=None) -> int:

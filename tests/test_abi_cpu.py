@@ -55,12 +55,12 @@ def test_packed_and_workspace_sizes():
                                          + 4096 * 2048 // 2 + 4096 * 2048 // 32)
     lay = moe.workspace_layout(d)
     R = moe.rows_capacity(8, 256, 6, 16)
-    # x as 2 MXFP8 terms, SiLU(gate)*up as 3 terms, each with one scale byte per 32 elements
+    # x and SiLU(gate)*up as 2 MXFP8 terms each, with one scale byte per 32 elements
     assert lay["xq"] >= 256 and lay["xs"] >= lay["xq"] + 2 * R * 4096
     RS = (R + 3) // 4 * 4                      # scale words per term and slab: rows rounded up to 4
     assert lay["hq"] >= lay["xs"] + 2 * RS * 4096 // 32
-    assert lay["hs"] >= lay["hq"] + 3 * R * 2048
-    assert lay["staging"] >= lay["hs"] + 3 * RS * 2048 // 32
+    assert lay["hs"] >= lay["hq"] + 2 * R * 2048
+    assert lay["staging"] >= lay["hs"] + 2 * RS * 2048 // 32
     assert lay["total"] >= lay["staging"] + 48 * 4096 * 4
     assert moe.workspace_bytes(d) == lay["total"]
     assert all(v % 256 == 0 for v in lay.values())

@@ -169,7 +169,8 @@ def _terms(ws, off_q, off_s, nt, R, K):
 def test_forward_tiny_intermediates(gpu_lib, gpu_layers):
     """Diagnostic: the activation terms of both GEMMs against float64. The x
     terms reproduce every bf16 input (2 terms: 4 + 4 significant bits); the h
-    terms keep SiLU(gate)*up to about 12 bits (3 terms)."""
+    terms keep SiLU(gate)*up to about 4 bits per term (the term count is read
+    off the workspace layout)."""
     moe = gpu_lib
     L = synth.make_config("tiny_t37_h512_e32")
     r = _run_layer(moe, gpu_layers, L, 16)
@@ -185,7 +186,8 @@ def test_forward_tiny_intermediates(gpu_lib, gpu_layers):
     # exact unless a 32-element block spans more than E4M3's range (then the smallest values keep
     # fewer bits): measured on these inputs about 2 in 10^4 elements, each off by < 1e-6 * max|x|
     assert np.mean(xg == want) > 0.999 and np.abs(xg - want).max() <= 1e-6 * np.abs(x).max()
-    h_gpu = _terms(ws, lay["hq"], lay["hs"], 3, R, I)[:Rv]
+    nt_h = (lay["hs"] - lay["hq"]) // (R * I)
+    h_gpu = _terms(ws, lay["hq"], lay["hs"], nt_h, R, I)[:Rv]
     ids = r["ids"].cpu().numpy()
     e2m1 = np.array([oracle.e2m1_value(c) for c in range(16)])
     worst = 0.0
@@ -200,8 +202,10 @@ def test_forward_tiny_intermediates(gpu_lib, gpu_layers):
         gu = W @ x[t]
         h = gu[:I] / (1 + np.exp(-gu[:I])) * gu[I:]
         worst = max(worst, np.abs(h_gpu[row] - h).max() / np.sqrt(np.mean(h ** 2)))
-    print(f"[tiny h] max|h_terms-h|/rms(h) = {worst:.3e}")
-    assert worst < 3e-3
+    print(f"[tiny h] {nt_h} terms: max|h_terms-h|/rms(h) = {worst:.3e}")
+    # the residual after t terms is at most half an E4M3 ulp of term t, 2^(4 - 4t) of the block's
+    # largest value (<= 448 * 2^e1), and a block's largest |h| is a few rms(h) of its row
+    assert worst < {2: 3e-2, 3: 3e-3}[nt_h]
 
 
 def test_forward_decode_t8_all_outputs(gpu_lib, gpu_layers):
@@ -250,7 +254,9 @@ def test_forward_swiglu_clamp_variant(gpu_lib, gpu_layers, name):
 @pytest.mark.parametrize("T,H,I,E,k", [(1, 256, 128, 8, 2), (17, 128, 256, 16, 4), (200, 256, 128, 5, 3),
                                        (300, 128, 128, 64, 6),
                                        (40, 256, 128, 1024, 6),     # > 512 experts: the wide-E decode W2 tiles
-                                       (11000, 128, 128, 1024, 6)])  # > 64 rows per expert, > 512 experts: wide-E prefill tiles
+                                       (11000, 128, 128, 1024, 6),  # > 64 rows per expert, > 512 experts: wide-E prefill tiles
+                                       (700, 256, 256, 8, 2),       # prefill tiles with at most 512 experts, all outputs
+                                       (600, 384, 128, 8, 2)])      # prefill tiles, an odd number of W2 output tiles
 def test_forward_fuzz_shapes(gpu_lib, gpu_layers, T, H, I, E, k):
     L = synth.make_layer(T=T, H=H, E=E, k=k, I=I, seed=T + E)
     r = _run_layer(gpu_lib, gpu_layers, L)

@@ -71,13 +71,14 @@ def _largest_T(moe, H, I, E, k, block_m=16):
 
 
 def test_noalloc_at_its_size_limit_after_larger_and_smaller_calls(gpu_lib, gpu_layers):
-    """The 256-expert layer at the largest token count the array holds (22 tokens), then a smaller
-    call with another routing, then the largest again on new activations: every call bit-exact
-    against moe_mxfp4_forward, so nothing depends on what an earlier call left in the array."""
+    """The 256-expert layer at the largest token count the array holds (25 tokens, as the header
+    documents), then a smaller call with another routing, then the largest again on new activations:
+    every call bit-exact against moe_mxfp4_forward, so nothing depends on what an earlier call left in
+    the array."""
     moe = gpu_lib
     H, I, E, k = 4096, 2048, 256, 6
     Tmax = _largest_T(moe, H, I, E, k)
-    assert Tmax == 22
+    assert Tmax == 25
     big = synth.make_layer(T=Tmax, H=H, E=E, k=k, I=I, seed=0)
     small = synth.make_config("decode_t8_h4096_e256")            # same weights (seed 0), other tokens
     seq = [(big, 1.0), (small, 1.0), (big, -0.75)]
@@ -94,7 +95,7 @@ def test_noalloc_rejects_layers_larger_than_its_scratch(gpu_lib):
     moe = gpu_lib
     lib = moe.load()
     fake = ctypes.c_void_p(1 << 20)     # never dereferenced: the size check fails first
-    for T in (23, 2048):
+    for T in (26, 2048):                # one token past the documented limit, and a prefill chunk
         desc = moe.make_desc(T, 4096, 2048, 256, 6, 16)
         assert moe.workspace_bytes(desc) > moe.NOALLOC_SCRATCH_BYTES
         rc = lib.moe_mxfp4_forward_noalloc(ctypes.byref(desc), fake, fake, fake, fake, fake, fake, fake, None)
