@@ -182,182 +182,226 @@ route_permute_kernel(const float *__restrict__ logits, int T, int E, int k, int 
 }
 
 // ---------------------------------------------------------------------------------------------
-// Multi-block permutation for large batches. Block b owns experts [8b, 8b + 8). Every block builds
-// the histogram of all experts itself (the ids are a few hundred KB, read from L2), so it knows
-// every padded start without a workspace or any wait on another block; block 0 writes counts,
-// offsets and padded offsets. Then each block walks all pairs in chunks of PM_CHUNK and scatters
-// the pairs of its own experts: warp w of a chunk takes PM_SUB runs of 32 consecutive pairs and
-// ranks each pair among the earlier pairs of its expert in the warp with one ballot per owned
-// expert; a scan over the warps per expert adds the earlier warps of the chunk and the earlier
-// chunks. Rows come out in ascending pair order inside each expert segment, bit-identical to the
-// one-block kernel. The same two-sided lane mask applies: a lane counts only if it is inside its
-// run and below T*k. (__match_any_sync, whose cost grows with the number of distinct experts in a
-// warp, is avoided here: the histogram uses plain shared-memory adds, which conflict only where
-// lanes share an expert.)
-constexpr int PM_EPB = 8;                        // experts per block
-constexpr int PM_SUB = 8;                        // runs of 32 pairs per warp and chunk
-constexpr int PM_CHUNK = PERM_THREADS * PM_SUB;  // pairs per chunk
-// Above this many pairs the permutation runs on many blocks.
+// Chunked permutation for large batches, in three launches. The pairs are cut into nc chunks of C
+// consecutive pairs (the last chunk also takes the remainder), with C a multiple of PC_THREADS and
+// C >= E. Until the last launch overwrites it, chunk b's own slice of pair_to_row, entries
+// [b*C, b*C + E), holds the chunk's per-expert numbers, so no workspace is needed:
+//   1. chunk histograms (one block per chunk): slice[e] = pairs of expert e in the chunk;
+//   2. per expert (one warp each), an exclusive scan over the chunks: slice[e] = pairs of e in the
+//      earlier chunks; counts[e] = the total;
+//   3. per chunk (one block each): offsets and padded offsets from the counts (block 0 writes them),
+//      then the chunk's pairs in order, 256 at a time: a pair's row is padded[e] + (pairs of e in
+//      earlier chunks) + (in earlier rounds of this chunk) + (in earlier warps of this round) +
+//      (in earlier lanes of its warp). Rows of one expert come out in ascending pair order, the
+//      same rows as the one-block kernel. Padding rows of experts b, b + nc, ... and a 1/nc share
+//      of the tail get -1.
+// The two-sided lane mask applies in launches 1 and 3: a lane counts only inside its chunk, which
+// never extends past T*k.
+constexpr int PC_THREADS = 256;
+constexpr int PC_WARPS = PC_THREADS / 32;
+constexpr int PC_TARGET_CHUNKS = 256;            // chunks are at least P / 256 pairs
+// Above this many pairs the permutation runs chunked on many blocks.
 constexpr int64_t PERMUTE_MULTI_MIN_PAIRS = 4096;
 
-__global__ void __launch_bounds__(PERM_THREADS, 1)
-permute_multi_kernel(const int32_t *__restrict__ ids, int T, int E, int k, int block_m,
-                     int32_t *__restrict__ counts, int32_t *__restrict__ offsets, int32_t *__restrict__ padded,
-                     int32_t *__restrict__ row_to_pair, int64_t rows_cap, int32_t *__restrict__ pair_to_row,
-                     int32_t *__restrict__ dev_error)
+struct ChunkPlan {
+    int64_t C;     // pairs per chunk (the last chunk: P - (nc - 1) * C)
+    int nc;        // chunks
+};
+
+static ChunkPlan chunk_plan(int64_t P, int E)
+{
+    int64_t c = (P + PC_TARGET_CHUNKS - 1) / PC_TARGET_CHUNKS;
+    if (c < E) c = E;
+    c = (c + PC_THREADS - 1) / PC_THREADS * PC_THREADS;
+    ChunkPlan pl;
+    pl.C = c;
+    pl.nc = (int)(P / c);          // 1 .. 256: P > 4096 and C <= max(1024, P / 256 + 256) < P; C >= P / 256
+    return pl;
+}
+
+__device__ __forceinline__ void chunk_range(int64_t P, int64_t C, int nc, int b, int64_t &lo, int64_t &hi)
+{
+    lo = (int64_t)b * C;
+    hi = b == nc - 1 ? P : lo + C;
+}
+
+__global__ void __launch_bounds__(PC_THREADS)
+permute_chunk_hist_kernel(const int32_t *__restrict__ ids, int64_t P, int E, int64_t C, int nc,
+                          int32_t *__restrict__ pair_to_row)
 {
     griddep_wait();                   // ids come from the kernel before (launched with pdl)
     griddep_launch_dependents();
     extern __shared__ int smem[];
-    int *cnt = smem;                           // [E]
-    int *pad_start = cnt + E;                  // [E + 1]
-    int *warp_tot = pad_start + E + 1;         // [32]
-    __shared__ int wcnt[PERM_WARPS][PM_EPB];   // pairs of each local expert in each warp's runs
-    __shared__ int wbase[PERM_WARPS][PM_EPB];  // rows before each warp's first pair of the expert
-    __shared__ int run[PM_EPB];                // rows of the expert filled by earlier chunks
+    int *hist = smem;                 // [E]
+    int64_t lo, hi;
+    chunk_range(P, C, nc, blockIdx.x, lo, hi);
+    for (int e = threadIdx.x; e < E; e += PC_THREADS) hist[e] = 0;
+    __syncthreads();
+    for (int64_t p = lo + threadIdx.x; p < hi; p += PC_THREADS) {    // lanes past the chunk are masked
+        const int e = __ldg(ids + p);
+        if (e >= 0 && e < E) atomicAdd(&hist[e], 1);
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += PC_THREADS) pair_to_row[lo + e] = hist[e];
+}
+
+__global__ void __launch_bounds__(PC_THREADS)
+permute_chunk_scan_kernel(int E, int64_t C, int nc, int32_t *__restrict__ counts, int32_t *__restrict__ pair_to_row)
+{
+    griddep_wait();                   // the chunk histograms come from the kernel before
+    griddep_launch_dependents();
+    const int lane = threadIdx.x & 31;
+    const int e = blockIdx.x * PC_WARPS + (threadIdx.x >> 5);
+    if (e >= E) return;                                   // uniform per warp
+    constexpr int MAXC = (PC_TARGET_CHUNKS + 31) / 32;     // chunks per lane (nc <= 256)
+    const int c0 = lane * nc / 32, c1 = (lane + 1) * nc / 32;
+    int v[MAXC];
+    int sum = 0;
+#pragma unroll
+    for (int i = 0; i < MAXC; ++i) {
+        v[i] = c0 + i < c1 ? pair_to_row[(int64_t)(c0 + i) * C + e] : 0;
+        sum += v[i];
+    }
+    int incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += n;
+    }
+    int run = incl - sum;
+#pragma unroll
+    for (int i = 0; i < MAXC; ++i) {
+        if (c0 + i < c1) pair_to_row[(int64_t)(c0 + i) * C + e] = run;
+        run += v[i];
+    }
+    if (lane == 31) counts[e] = incl;
+}
+
+// Inclusive scan of one int per thread over a PC_THREADS block.
+__device__ __forceinline__ int chunk_block_scan(int v, int *warp_tot)
+{
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xFFFFFFFFu, v, o);
+        if (lane >= o) v += n;
+    }
+    if (lane == 31) warp_tot[wid] = v;
+    __syncthreads();
+    if (wid == 0) {
+        int t = lane < PC_WARPS ? warp_tot[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < PC_WARPS; o <<= 1) {
+            const int n = __shfl_up_sync(0xFFFFFFFFu, t, o);
+            if (lane >= o) t += n;
+        }
+        if (lane < PC_WARPS) warp_tot[lane] = t;
+    }
+    __syncthreads();
+    const int r = v + (wid > 0 ? warp_tot[wid - 1] : 0);
+    __syncthreads();
+    return r;
+}
+
+__global__ void __launch_bounds__(PC_THREADS)
+permute_chunk_scatter_kernel(const int32_t *__restrict__ ids, int64_t P, int E, int block_m, int64_t C, int nc,
+                             const int32_t *__restrict__ counts, int32_t *__restrict__ offsets,
+                             int32_t *__restrict__ padded, int32_t *__restrict__ row_to_pair, int64_t rows_cap,
+                             int32_t *__restrict__ pair_to_row, int32_t *__restrict__ dev_error)
+{
+    griddep_wait();                   // counts and the per-chunk bases come from the kernel before
+    griddep_launch_dependents();
+    extern __shared__ int smem[];
+    int *pad_start = smem;                       // [E + 1]
+    int *cnt = pad_start + E + 1;                // [E]
+    int *base = cnt + E;                         // [E]: next row of expert e for this chunk
+    int *wc = base + E;                          // [PC_WARPS][E]: pairs of e in each warp's 32 lanes
+    __shared__ int warp_tot[32];
     __shared__ int s_err;
 
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-    const int64_t P = (int64_t)T * k;
-    const int e0 = blockIdx.x * PM_EPB;
-    const int ne = E - e0 < PM_EPB ? E - e0 : PM_EPB;
     const unsigned lt_mask = (1u << lane) - 1u;
+    int64_t lo, hi;
+    chunk_range(P, C, nc, blockIdx.x, lo, hi);
 
-    for (int i = tid; i < E; i += PERM_THREADS) cnt[i] = 0;
-    if (tid < PM_EPB) run[tid] = 0;
-    if (tid == 0) s_err = 0;
-    __syncthreads();
-
-    // Phase A: histogram of all experts. The ids of the next chunk are loaded before the current
-    // chunk is counted, so the loads of one chunk overlap the adds of the one before.
-    int nxt[PM_SUB];
+    // offsets and padded offsets: thread i scans experts 4i .. 4i+3 (E <= 1024)
+    int c4[4], s_c = 0, s_p = 0;
 #pragma unroll
-    for (int sub = 0; sub < PM_SUB; ++sub) {
-        const int64_t p = (int64_t)sub * PERM_THREADS + tid;
-        nxt[sub] = p < P ? __ldg(ids + p) : -1;
+    for (int q = 0; q < 4; ++q) {
+        const int e = tid * 4 + q;
+        c4[q] = e < E ? __ldg(counts + e) : 0;
+        s_c += c4[q];
+        s_p += (c4[q] + block_m - 1) / block_m * block_m;
     }
-    for (int64_t base = 0; base < P; base += PM_CHUNK) {
-        int ev[PM_SUB];
+    if (tid == 0) s_err = 0;
+    const int inc_c = chunk_block_scan(s_c, warp_tot);
+    const int inc_p = chunk_block_scan(s_p, warp_tot);
+    {
+        int rc = inc_c - s_c, rp = inc_p - s_p;
 #pragma unroll
-        for (int sub = 0; sub < PM_SUB; ++sub) {
-            ev[sub] = nxt[sub];
-            const int64_t p = base + PM_CHUNK + (int64_t)sub * PERM_THREADS + tid;
-            nxt[sub] = p < P ? __ldg(ids + p) : -1;
-        }
-#pragma unroll
-        for (int sub = 0; sub < PM_SUB; ++sub) {
-            const int64_t p = base + (int64_t)sub * PERM_THREADS + tid;
-            const int e = ev[sub];
-            if (p < P) {
-                if (e >= 0 && e < E) {
-                    atomicAdd(&cnt[e], 1);
-                } else {
-                    s_err = 1;
-                    if (blockIdx.x == 0) pair_to_row[p] = -1;
+        for (int q = 0; q < 4; ++q) {
+            const int e = tid * 4 + q;
+            if (e < E) {
+                pad_start[e] = rp;
+                cnt[e] = c4[q];
+                base[e] = rp + pair_to_row[lo + e];            // this chunk's slice: rows of e in earlier chunks
+                if (blockIdx.x == 0) {
+                    offsets[e] = rc;
+                    padded[e] = rp;
                 }
             }
+            rc += c4[q];
+            rp += (c4[q] + block_m - 1) / block_m * block_m;
         }
-    }
-    __syncthreads();
-
-    // Phase B: offsets and padded offsets (E <= 1024: one expert per thread).
-    const int c = tid < E ? cnt[tid] : 0;
-    const int pc = (c + block_m - 1) / block_m * block_m;
-    const int inc_c = block_inclusive_scan(c, warp_tot);
-    const int inc_p = block_inclusive_scan(pc, warp_tot);
-    if (tid < E) {
-        pad_start[tid + 1] = inc_p;
-        if (blockIdx.x == 0) {
-            counts[tid] = c;
-            offsets[tid + 1] = inc_c;
-            padded[tid + 1] = inc_p;
-        }
-    }
-    if (tid == 0) {
-        pad_start[0] = 0;
-        if (blockIdx.x == 0) {
-            offsets[0] = 0;
-            padded[0] = 0;
-        }
-    }
-    __syncthreads();
-
-    // Phase C: stable scatter of this block's experts, chunk by chunk (the next chunk's ids are
-    // loaded while the current chunk is ranked). Lane j < PM_EPB keeps the warp's running count of
-    // local expert j in this chunk.
-#pragma unroll
-    for (int sub = 0; sub < PM_SUB; ++sub) {
-        const int64_t p = ((int64_t)wid * PM_SUB + sub) * 32 + lane;
-        nxt[sub] = p < P ? __ldg(ids + p) : -1;
-    }
-    for (int64_t base = 0; base < P; base += PM_CHUNK) {
-        int el_s[PM_SUB], rank_s[PM_SUB];
-#pragma unroll
-        for (int sub = 0; sub < PM_SUB; ++sub) {
-            el_s[sub] = nxt[sub];
-            const int64_t p = base + PM_CHUNK + ((int64_t)wid * PM_SUB + sub) * 32 + lane;
-            nxt[sub] = p < P ? __ldg(ids + p) : -1;
-        }
-        int mine = 0;                                   // lane j: pairs of local expert j so far
-#pragma unroll
-        for (int sub = 0; sub < PM_SUB; ++sub) {
-            const int e = el_s[sub];                    // -1 past T*k (the load above masks it)
-            const int el = (e >= e0 && e < e0 + ne) ? e - e0 : -1;
-            unsigned same = 0u;
-            int add = 0;
-#pragma unroll
-            for (int j = 0; j < PM_EPB; ++j) {
-                const unsigned b = __ballot_sync(0xFFFFFFFFu, el == j);
-                if (el == j) same = b;
-                if (lane == j) add = __popc(b);
+        if (tid == PC_THREADS - 1) {
+            pad_start[E] = rp;
+            if (blockIdx.x == 0) {
+                offsets[E] = rc;
+                padded[E] = rp;
             }
-            const int before = __shfl_sync(0xFFFFFFFFu, mine, el >= 0 ? el : 0);
-            el_s[sub] = el;
-            rank_s[sub] = before + __popc(same & lt_mask);
-            mine += add;
         }
-        if (lane < PM_EPB) wcnt[wid][lane] = mine;
+    }
+    for (int i = tid; i < PC_WARPS * E; i += PC_THREADS) wc[i] = 0;
+    __syncthreads();                  // the slice has been read: its entries may now be overwritten
+
+    for (int64_t r0 = lo; r0 < hi; r0 += PC_THREADS) {
+        const int64_t p = r0 + tid;
+        const bool valid = p < hi;                          // logical-block mask (never past T*k)
+        int e = valid ? __ldg(ids + p) : -1;
+        if (valid && (e < 0 || e >= E)) { e = -1; s_err = 1; }
+        const unsigned m = __match_any_sync(0xFFFFFFFFu, e);
+        const bool leader = (m & lt_mask) == 0u;
+        if (e >= 0 && leader) wc[wid * E + e] = __popc(m);
         __syncthreads();
-        if (wid < ne) {                       // warp j scans local expert j over the 32 warps
-            const int v = wcnt[lane][wid];
-            int incl = v;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int n = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-                if (lane >= o) incl += n;
-            }
-            const int r = run[wid];
-            wbase[lane][wid] = r + incl - v;
-            const int tot = __shfl_sync(0xFFFFFFFFu, incl, 31);
-            __syncwarp();
-            if (lane == 0) run[wid] = r + tot;
+        if (e >= 0) {
+            int row = base[e] + __popc(m & lt_mask);
+            for (int w = 0; w < wid; ++w) row += wc[w * E + e];
+            row_to_pair[row] = (int32_t)p;
+            pair_to_row[p] = row;
+        } else if (valid) {
+            pair_to_row[p] = -1;
         }
         __syncthreads();
-#pragma unroll
-        for (int sub = 0; sub < PM_SUB; ++sub) {
-            if (el_s[sub] >= 0) {
-                const int64_t p = base + ((int64_t)wid * PM_SUB + sub) * 32 + lane;
-                const int row = pad_start[e0 + el_s[sub]] + wbase[wid][el_s[sub]] + rank_s[sub];
-                row_to_pair[row] = (int32_t)p;
-                pair_to_row[p] = row;
-            }
+        if (e >= 0 && leader) {
+            atomicAdd(&base[e], __popc(m));
+            wc[wid * E + e] = 0;
         }
+        __syncthreads();
     }
 
-    // Phase D: padding rows of this block's experts; the tail up to rows_cap split over all blocks.
-    for (int j = 0; j < ne; ++j) {
-        const int e = e0 + j;
-        for (int r = pad_start[e] + cnt[e] + tid; r < pad_start[e + 1]; r += PERM_THREADS) row_to_pair[r] = -1;
-    }
-    for (int64_t r = pad_start[E] + (int64_t)blockIdx.x * PERM_THREADS + tid; r < rows_cap;
-         r += (int64_t)gridDim.x * PERM_THREADS)
+    // padding rows of experts b, b + nc, ...; the tail up to rows_cap split over the blocks
+    for (int e = blockIdx.x; e < E; e += nc)
+        for (int r = pad_start[e] + cnt[e] + tid; r < pad_start[e + 1]; r += PC_THREADS) row_to_pair[r] = -1;
+    for (int64_t r = pad_start[E] + (int64_t)blockIdx.x * PC_THREADS + tid; r < rows_cap;
+         r += (int64_t)nc * PC_THREADS)
         row_to_pair[r] = -1;
     __syncthreads();
-    if (blockIdx.x == 0 && tid == 0 && s_err && dev_error) atomicExch(dev_error, DEV_ERR_ID_RANGE);
+    if (tid == 0 && s_err && dev_error) atomicExch(dev_error, DEV_ERR_ID_RANGE);
 }
 
+static size_t chunk_scatter_smem(int E) { return sizeof(int) * ((size_t)E + 1 + E + E + (size_t)PC_WARPS * E); }
+
 static size_t permute_smem(int E) { return sizeof(int) * ((size_t)PERM_WARPS * E + E + E + 1 + 32); }
-static size_t permute_multi_smem(int E) { return sizeof(int) * ((size_t)E + E + 1 + 32); }
 
 // Raise a kernel's dynamic shared-memory limit to what E = 1024 needs, once per device (bit d of *mask);
 // the attribute is a per-function maximum, so smaller launches are unaffected.
@@ -416,12 +460,19 @@ cudaError_t launch_permute(const int32_t *ids, int T, int E, int k, int block_m,
                            int32_t *offsets, int32_t *padded, int32_t *row_to_pair, int64_t rows_cap,
                            int32_t *pair_to_row, int32_t *dev_error, cudaStream_t s)
 {
-    if ((int64_t)T * k > PERMUTE_MULTI_MIN_PAIRS) {
-        const int blocks = (E + PM_EPB - 1) / PM_EPB;
-        cudaError_t err = launch_ex(permute_multi_kernel, dim3(blocks), dim3(PERM_THREADS), permute_multi_smem(E), s,
-                                    true, ids, T, E, k, block_m, counts, offsets, padded, row_to_pair, rows_cap,
-                                    pair_to_row, dev_error);
-        note_launch(1);
+    const int64_t P = (int64_t)T * k;
+    if (P > PERMUTE_MULTI_MIN_PAIRS) {
+        const ChunkPlan pl = chunk_plan(P, E);
+        cudaError_t err = launch_ex(permute_chunk_hist_kernel, dim3(pl.nc), dim3(PC_THREADS), sizeof(int) * (size_t)E,
+                                    s, true, ids, P, E, pl.C, pl.nc, pair_to_row);
+        if (err != cudaSuccess) return err;
+        err = launch_ex(permute_chunk_scan_kernel, dim3((E + PC_WARPS - 1) / PC_WARPS), dim3(PC_THREADS), 0, s, true,
+                        E, pl.C, pl.nc, counts, pair_to_row);
+        if (err != cudaSuccess) return err;
+        err = launch_ex(permute_chunk_scatter_kernel, dim3(pl.nc), dim3(PC_THREADS), chunk_scatter_smem(E), s, true,
+                        (const int32_t *)ids, P, E, block_m, pl.C, pl.nc, (const int32_t *)counts, offsets, padded,
+                        row_to_pair, rows_cap, pair_to_row, dev_error);
+        note_launch(3);
         return err;
     }
     static unsigned long long attr_set = 0;

@@ -11,7 +11,9 @@
 //
 // Each lane owns experts lane, lane+32, ... (coalesced 128-byte loads) as
 // order-preserving 32-bit keys. Every round takes the warp maximum key with
-// redux.sync, then the lowest expert index among the lanes holding it.
+// redux.sync; a ballot finds the lanes holding it (one lane: its lowest value
+// index with that key wins; several: the lowest expert index among them, by a
+// second redux.sync).
 #pragma once
 #include <cstdint>
 
@@ -38,27 +40,36 @@ __device__ __forceinline__ void route_token(const float *__restrict__ logits, in
 #pragma unroll
     for (int v = 0; v < VPL; ++v) {
         int e = (int)lane + 32 * v;
-        key[v] = (e < E) ? float_key(__ldg(row + e)) : 0u;   // lanes past E never win (k <= E)
+        key[v] = (e < E) ? float_key(__ldg(row + e)) : 0u;   // values past E never win (k <= E)
     }
-    uint32_t taken = 0u;          // bit v: value v of this lane already chosen
+    // Chosen values get key 0, below every finite logit's key (>= 0x00800000), like lanes past E.
     int my_id = -1;               // lane j < k keeps the j-th choice
     float my_logit = 0.f;
 
     for (int j = 0; j < k; ++j) {
-        uint32_t best = 0u;
-        int best_v = -1;
+        uint32_t best = key[0];   // this lane's largest remaining key, at its lowest value index
+        int best_v = 0;
 #pragma unroll
-        for (int v = 0; v < VPL; ++v) {
-            int e = (int)lane + 32 * v;
-            bool ok = e < E && !((taken >> v) & 1u);
-            if (ok && (best_v < 0 || key[v] > best)) { best = key[v]; best_v = v; }  // v ascending keeps lower index
+        for (int v = 1; v < VPL; ++v) {
+            const bool gt = key[v] > best;
+            best = gt ? key[v] : best;
+            best_v = gt ? v : best_v;
         }
-        uint32_t wmax = __reduce_max_sync(0xFFFFFFFFu, best_v >= 0 ? best : 0u);
-        uint32_t cand = (best_v >= 0 && best == wmax) ? (lane + 32u * (uint32_t)best_v) : 0xFFFFFFFFu;
-        uint32_t win = __reduce_min_sync(0xFFFFFFFFu, cand);
-        if ((win & 31u) == lane) taken |= 1u << (win >> 5);
+        const uint32_t wmax = __reduce_max_sync(0xFFFFFFFFu, best);
+        const unsigned holders = __ballot_sync(0xFFFFFFFFu, best == wmax);
+        int win;
+        if (__popc(holders) == 1) {                  // warp-uniform: the common case, no tie across lanes
+            const int wl = __ffs(holders) - 1;
+            win = wl + 32 * __shfl_sync(0xFFFFFFFFu, best_v, wl);
+        } else {                                     // equal keys in several lanes: lowest expert index
+            const uint32_t cand = best == wmax ? lane + 32u * (uint32_t)best_v : 0xFFFFFFFFu;
+            win = (int)__reduce_min_sync(0xFFFFFFFFu, cand);
+        }
+        const bool mine = (win & 31) == (int)lane;
+#pragma unroll
+        for (int v = 0; v < VPL; ++v) key[v] = (mine && v == best_v) ? 0u : key[v];
         if ((int)lane == j) {
-            my_id = (int)win;
+            my_id = win;
             my_logit = row[win];
         }
     }
