@@ -152,7 +152,7 @@ int64_t scale_rows(const moe_layer_desc *d)
 
 Layout workspace_layout(const moe_layer_desc *d)
 {
-    const int NT_H = regime_nt_h(pick_regime(d->T, d->k, d->E));
+    const int NT_H = regime_nt_h(pick_regime(d->T, d->k, d->E, d->H));
     const int64_t P = (int64_t)d->T * d->k;
     const int64_t R = moe_permute_rows_capacity(d->T, d->E, d->k, d->block_m);
     const int64_t RS = scale_rows(d);
@@ -367,7 +367,7 @@ moe_status_t moe_mxfp4_forward_timed(const moe_layer_desc *d, const uint16_t *d_
     a.staging = reinterpret_cast<float *>(ws + L.staging);
     a.num_sms = sm_count();
     a.events = events;
-    a.regime = pick_regime(d->T, d->k, d->E);
+    a.regime = pick_regime(d->T, d->k, d->E, d->H);
     const uint32_t sps = (uint32_t)regime_sps(a.regime);
     const uint8_t *w13 = a.packed, *w2 = a.packed + packed_w13_bytes(d->E, d->H, d->I);
     const uint64_t rows13 = (uint64_t)d->E * 2 * d->I * (d->H / KSLAB);   // 128-element rows of W13 nibbles

@@ -46,6 +46,7 @@
 
 #include <cstdint>
 
+#include "gemm_common.cuh"
 #include "moe_internal.h"
 #include "mxfp4_tile.cuh"
 #include "mxfp8_terms.cuh"
@@ -54,8 +55,6 @@
 namespace moe {
 
 namespace {
-
-constexpr int TMEM_COLS = 512;
 
 // Kernel configuration. MODE 0: W13 (x terms -> SiLU(gate)*up -> h terms),
 // MODE 1: W2 (h terms -> per-pair outputs). NMAX: most token rows per tile
@@ -126,24 +125,6 @@ static_assert(W13Tiny::NTO == W2Tiny::NT && W13Small::NTO == W2Small::NT && W13M
                   W13Large::NTO == W2Large::NT && W13LargeWideE::NTO == W2LargeWideE::NT,
               "W2 reads as many h terms as W13 writes");
 
-struct GemmParams {
-    CUtensorMap tm_a;         // weight nibbles, box 128 x (128 * SPS) rows
-    CUtensorMap tm_a1;        // weight nibbles, box 128 x 128 rows (a stage that straddles two tiles)
-    CUtensorMap tm_b, tm_b1;  // activation terms [K/128][NT][rows][128] bytes, box 128 x NMAX x NT x (SPS | 1) slabs
-    CUtensorMap tm_bs, tm_bs1; // their scale words [K/128][NT][rows_sf] (uint32), box NMAX x NT x (SPS | 1)
-    const uint8_t *wsf;       // this matrix's prepacked scale region
-    const int32_t *offsets;   // [E+1]
-    const int32_t *padded;    // [E+1]
-    const int32_t *row_to_pair;
-    int E, K, MB;             // MB: 128-row weight tiles per expert
-    int I, H, k;
-    float swiglu_limit;
-    int64_t P, rows_cap, rows_sf;
-    uint8_t *hq;              // W13 out: h terms [I/128][NTO][rows_cap][128]
-    uint8_t *hs;              // W13 out: h term scale words [I/128][NTO][rows_sf], byte = K-block % 4
-    float *staging;           // W2 out [P, H]
-    int32_t *dev_error;
-};
 
 template <class C>
 struct Smem {
@@ -171,42 +152,8 @@ struct Smem {
     static_assert(bytes(C::EMAX) <= 232448, "shared memory per CTA");
 };
 
-__device__ __forceinline__ void record_error(int32_t *dev_error, int code)
-{
-    if (dev_error) atomicCAS(dev_error, 0, code);
-}
 
-// Tile t -> (expert, token block, weight row tile); tile_start is the
-// exclusive prefix over experts of ceil(count / NMAX) * MB.
-struct Tile {
-    int e, mb, row0, n;
-};
 
-template <class C>
-__device__ __forceinline__ Tile decode_tile(int t, const int *tile_start, int E, int MB, const int *cnt,
-                                            const int *pad0)
-{
-    constexpr int NMAX = C::NMAX;
-    int lo = 0, hi = E - 1;                 // largest e with tile_start[e] <= t
-    while (lo < hi) {
-        int mid = (lo + hi + 1) >> 1;
-        if (tile_start[mid] <= t) lo = mid; else hi = mid - 1;
-    }
-    Tile r;
-    r.e = lo;
-    int local = t - tile_start[lo];
-    int nb = local / MB;
-    r.mb = local - nb * MB;
-    int rem = cnt[lo] - nb * NMAX;
-    int n = rem < NMAX ? rem : NMAX;
-    r.n = (n + 15) & ~15;
-    r.row0 = pad0[lo] + nb * NMAX;
-    return r;
-}
-
-// SiLU(g) = g / (1 + e^-g) with the fast exp and divide (about 1e-6 relative error, far below the 8
-// bits h keeps in its two terms). For g < -88, e^-g is +inf and the quotient is -0.
-__device__ __forceinline__ float silu_f(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
 
 template <class C>
 __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_kernel(const __grid_constant__ GemmParams p)
@@ -337,7 +284,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_kernel(const __grid_co
         long long issued = 0;
         bool ok = true;
         int tcur = blockIdx.x, ka = 0;
-        Tile tl = decode_tile<C>(tcur, tile_start, E, MB, s_cnt, s_pad0);
+        Tile tl = decode_tile<C::NMAX>(tcur, tile_start, E, MB, s_cnt, s_pad0);
         for (int i0 = 0; i0 < n_slabs; i0 += SPS) {
             if (!__all_sync(0xFFFFFFFFu, wait_done(i0 / SPS - C::NA))) { ok = false; break; }
             const int nsl = n_slabs - i0 < SPS ? n_slabs - i0 : SPS;
@@ -355,7 +302,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_kernel(const __grid_co
                     ptx::tma_load_2d(dst, &p.tm_a1, 0, r0, &a_full[ai]);
                     ptx::bulk_g2s(sdst, p.wsf + (size_t)(r0 / TILE_ROWS) * SLAB_SF_BYTES, SLAB_SF_BYTES, &a_full[ai]);
                     if (nsl == 2) {                  // the second slab opens the next tile
-                        const Tile t2 = decode_tile<C>(tcur + (int)gridDim.x, tile_start, E, MB, s_cnt, s_pad0);
+                        const Tile t2 = decode_tile<C::NMAX>(tcur + (int)gridDim.x, tile_start, E, MB, s_cnt, s_pad0);
                         const int r1 = a_row(t2, 0);
                         ptx::tma_load_2d(dst + SLAB_SMEM_BYTES, &p.tm_a1, 0, r1, &a_full[ai]);
                         ptx::bulk_g2s(sdst + SLAB_SF_BYTES, p.wsf + (size_t)(r1 / TILE_ROWS) * SLAB_SF_BYTES,
@@ -372,7 +319,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_kernel(const __grid_co
                 tcur += gridDim.x;
                 next_tile = true;
             }
-            if (next_tile && tcur < total) tl = decode_tile<C>(tcur, tile_start, E, MB, s_cnt, s_pad0);
+            if (next_tile && tcur < total) tl = decode_tile<C::NMAX>(tcur, tile_start, E, MB, s_cnt, s_pad0);
             if (++ai == C::NA) { ai = 0; aph ^= 1u; }
         }
         if (!ok && lane == 0) fail();
@@ -403,7 +350,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_kernel(const __grid_co
         long long issued = 0;
         bool ok = true;
         int tcur = blockIdx.x, ka = 0;
-        Tile tl = decode_tile<C>(tcur, tile_start, E, MB, s_cnt, s_pad0);
+        Tile tl = decode_tile<C::NMAX>(tcur, tile_start, E, MB, s_cnt, s_pad0);
         for (int i0 = 0; i0 < n_slabs; i0 += SPS) {
             if (!__all_sync(0xFFFFFFFFu, wait_done(i0 / SPS - C::NB))) { ok = false; break; }
             const int nsl = n_slabs - i0 < SPS ? n_slabs - i0 : SPS;
@@ -418,7 +365,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_kernel(const __grid_co
                 if (ka == slabs) {
                     ka = 0;
                     tcur += gridDim.x;
-                    if (tcur < total) tl = decode_tile<C>(tcur, tile_start, E, MB, s_cnt, s_pad0);
+                    if (tcur < total) tl = decode_tile<C::NMAX>(tcur, tile_start, E, MB, s_cnt, s_pad0);
                 }
             } else {                                    // last slab of a tile, or a stage across two tiles
                 for (int pos = 0; pos < nsl; ++pos) {
@@ -431,7 +378,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_kernel(const __grid_co
                     if (++ka == slabs) {
                         ka = 0;
                         tcur += gridDim.x;
-                        if (tcur < total) tl = decode_tile<C>(tcur, tile_start, E, MB, s_cnt, s_pad0);
+                        if (tcur < total) tl = decode_tile<C::NMAX>(tcur, tile_start, E, MB, s_cnt, s_pad0);
                     }
                 }
             }
@@ -604,7 +551,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_kernel(const __grid_co
         bool ok = true;
         int j = 0;
         for (int t = blockIdx.x; t < total; t += gridDim.x, ++j) {
-            const Tile tl = decode_tile<C>(t, tile_start, E, MB, s_cnt, s_pad0);
+            const Tile tl = decode_tile<C::NMAX>(t, tile_start, E, MB, s_cnt, s_pad0);
             // MMA warp q wrote into the tile iff one of the tile's stages is one of its stages
             const int s_first = (j * slabs) / SPS, s_last = (j * slabs + slabs - 1) / SPS;
             const unsigned wrote = (C::MW == 1 || s_last > s_first) ? ((1u << C::MW) - 1u) : (1u << (s_first % C::MW));
@@ -832,13 +779,14 @@ cudaError_t launch_gemm(const GemmParams &p, int grid, cudaStream_t s, bool pdl)
 
 }  // namespace
 
-Regime pick_regime(int T, int k, int E)
+Regime pick_regime(int T, int k, int E, int H)
 {
     const double avg = (double)T * k / E;
     if (avg <= 2.0) return Regime::Tiny;
     if (avg <= 16.0) return Regime::Small;
     if (avg <= 64.0) return Regime::Mid;
-    return Regime::Large;
+    if (avg <= 128.0 || H % 256 != 0) return Regime::Large;
+    return Regime::Huge;       // token-major tiles (gemm_rows.cu): 256 W2 output rows per tile
 }
 
 int regime_nmax(Regime rg, int which)
@@ -848,7 +796,8 @@ int regime_nmax(Regime rg, int which)
     case Regime::Tiny: return 16;
     case Regime::Small: return 32;
     case Regime::Mid: return 64;
-    default: return 96;
+    case Regime::Large: return 96;
+    default: return 128;
     }
 }
 
@@ -862,7 +811,7 @@ int regime_nt_h(Regime rg)
     }
 }
 
-int regime_sps(Regime) { return 2; }
+int regime_sps(Regime rg) { return rg == Regime::Huge ? 1 : 2; }
 
 static void mark(const ForwardArgs &a, int i, cudaStream_t s)
 {
@@ -917,7 +866,8 @@ cudaError_t launch_forward(const ForwardArgs &a, cudaStream_t s)
     g.K = a.H;
     g.MB = a.I / 64;
     const Regime rg = a.regime;
-    err = rg == Regime::Tiny  ? launch_gemm<W13Tiny>(g, a.num_sms, s, pdl)
+    err = rg == Regime::Huge  ? launch_gemm_rows(g, 0, a.num_sms, s, pdl)
+        : rg == Regime::Tiny  ? launch_gemm<W13Tiny>(g, a.num_sms, s, pdl)
         : rg == Regime::Small ? launch_gemm<W13Small>(g, a.num_sms, s, pdl)
         : rg == Regime::Mid   ? launch_gemm<W13Mid>(g, a.num_sms, s, pdl)
                               : (a.E <= W13Large::EMAX ? launch_gemm<W13Large>(g, a.num_sms, s, pdl)
@@ -935,7 +885,8 @@ cudaError_t launch_forward(const ForwardArgs &a, cudaStream_t s)
     g.wsf = a.packed + packed_w13_bytes(a.E, a.H, a.I) + (size_t)a.E * a.H * (a.I / 2);
     g.K = a.I;
     g.MB = a.H / TILE_ROWS;
-    err = rg == Regime::Tiny  ? (a.E <= W2Tiny::EMAX ? launch_gemm<W2Tiny>(g, a.num_sms, s, pdl)
+    err = rg == Regime::Huge  ? launch_gemm_rows(g, 1, a.num_sms, s, pdl)
+        : rg == Regime::Tiny  ? (a.E <= W2Tiny::EMAX ? launch_gemm<W2Tiny>(g, a.num_sms, s, pdl)
                                                      : launch_gemm<W2TinyWideE>(g, a.num_sms, s, pdl))
         : rg == Regime::Small ? launch_gemm<W2Small>(g, a.num_sms, s, pdl)
         : rg == Regime::Mid   ? launch_gemm<W2Mid>(g, a.num_sms, s, pdl)

@@ -18,8 +18,8 @@ constexpr int NT_X = 2;
 
 // GEMM tile shapes by the average rows per expert (T*k/E): decode batches get
 // small tiles with deep pipelines, prefill batches large tiles.
-enum class Regime { Tiny, Small, Mid, Large };
-Regime pick_regime(int T, int k, int E);
+enum class Regime { Tiny, Small, Mid, Large, Huge };
+Regime pick_regime(int T, int k, int E, int H);
 int regime_nmax(Regime rg, int which);   // token rows per tile; which 0: W13, 1: W2
 int regime_sps(Regime rg);               // K-slabs per weight stage
 // MXFP8 terms of h (gemm.cu sets them per tile regime; currently two, about 8 significant bits, the

@@ -264,6 +264,23 @@ def test_forward_fuzz_shapes(gpu_lib, gpu_layers, T, H, I, E, k):
     _compare(f"fuzz {T}x{H}x{I} E{E} k{k}", r["y"].cpu().numpy(), oracle.forward(L, ids_r, w_r))
 
 
+@pytest.mark.parametrize("block_m", [16, 128])
+@pytest.mark.parametrize("T,H,I,E,k,limit", [(1200, 512, 256, 16, 4, 0.0),   # 300 rows per expert: 3 token blocks
+                                             (1000, 256, 384, 5, 3, 10.0),   # 600 rows per expert, clamp, I/128 odd
+                                             (520, 768, 128, 2, 1, 0.0)])    # 260 rows per expert, three W2 blocks
+def test_forward_token_major_tiles(gpu_lib, gpu_layers, T, H, I, E, k, limit, block_m):
+    """More than 128 rows per expert on average selects the token-major tiles (128 token rows x 256
+    weight rows, terms summed by the tensor core): every output against the oracle, with small and
+    large row padding, partial last token blocks and rows of the next expert inside a tile."""
+    L = synth.make_layer(T=T, H=H, E=E, k=k, I=I, seed=T + H)
+    r = _run_layer(gpu_lib, gpu_layers, L, block_m=block_m, swiglu_limit=limit)
+    ids_r, w_r, _ = oracle.route(L["logits"], k)
+    y = r["y"].cpu().numpy()
+    assert np.isfinite(y).all()
+    _compare(f"token-major {T}x{H}x{I} E{E} k{k} bm{block_m} L{limit}", y,
+             oracle.forward(L, ids_r, w_r, swiglu_limit=limit))
+
+
 def test_forward_deterministic(gpu_lib, gpu_layers):
     L = synth.make_config("decode_t512_h4096_e256")
     a = _run_layer(gpu_lib, gpu_layers, L)["y"].clone()
