@@ -92,15 +92,25 @@ def term_counts(moe, desc):
 
 KERNEL_NAMES = {"w13": "moe_gemm_kernel<W13*> (grouped W13 GEMM + SiLU*up + h terms)",
                 "w2": "moe_gemm_kernel<W2*> (grouped W2 GEMM)"}
+ROWS_KERNEL_NAMES = {"w13": "moe_gemm_rows_kernel<W13Rows> (token-major grouped W13 GEMM + SiLU*up + h terms)",
+                     "w2": "moe_gemm_rows_kernel<W2Rows> (token-major grouped W2 GEMM)"}
 
 
-def kernel_roofline(name, key, alg, ms, peaks):
+def kernel_names(L):
+    """Names of the two GEMM kernels the library launches for this layer: the token-major tiles above
+    128 rows per expert on average when H is a multiple of 256, the weight-major tiles otherwise (the
+    library's tile choice, restated here only to label the JSON line)."""
+    rows = L["T"] * L["k"] / L["E"] > 128 and L["H"] % 256 == 0
+    return ROWS_KERNEL_NAMES if rows else KERNEL_NAMES
+
+
+def kernel_roofline(name, key, alg, ms, peaks, names=KERNEL_NAMES):
     """Roofline of one GEMM launch (key "w13" or "w2"): bound by HBM or by the tensor pipe,
     whichever needs more time for the work it executes (all activation terms) at the measured
     peaks; `achieved` counts the algorithmic (useful) bytes or flops."""
     hbm, bf16, bf16_sus, kind = peaks
     mxf8 = MXF8_OVER_BF16 * bf16
-    kernel = KERNEL_NAMES[key]
+    kernel = names[key]
     nbytes, flops, mma = alg[f"{key}_kernel_bytes"], alg[f"{key}_flops"], alg[f"{key}_mma_flops"]
     traffic, source = traffic_per_launch(name, key, nbytes)
     if mma / (mxf8 * 1e12) > nbytes / (hbm * 1e9):
@@ -440,8 +450,8 @@ def measure_config(moe, name, L, steps, warmup, flush_buf, peaks):
                            "flops": a["flops"],
                            "mxf8_frac_useful": a["flops"] / (ms / 1e3) / 1e12 / mxf8,
                            "mxf8_frac_executed": a["mma_flops"] / (ms / 1e3) / 1e12 / mxf8},
-        "w13_roofline": kernel_roofline(name, "w13", a, pk["w13"], peaks),
-        "w2_roofline": kernel_roofline(name, "w2", a, pk["w2"], peaks),
+        "w13_roofline": kernel_roofline(name, "w13", a, pk["w13"], peaks, kernel_names(L)),
+        "w2_roofline": kernel_roofline(name, "w2", a, pk["w2"], peaks, kernel_names(L)),
     }
     return out, lay, a
 
@@ -500,9 +510,9 @@ def run_ours(args, world, rank, local):
     nt_x, nt_h = term_counts(moe, layer.desc)
     alg = algorithmic(L, ids, nt_x, nt_h)
     dominant = "w13" if per_kernel["w13"] >= per_kernel["w2"] else "w2"
-    roofline = kernel_roofline(args.workload, dominant, alg, per_kernel[dominant], peaks)
+    roofline = kernel_roofline(args.workload, dominant, alg, per_kernel[dominant], peaks, kernel_names(L))
     other = kernel_roofline(args.workload, "w2" if dominant == "w13" else "w13", alg,
-                            per_kernel["w2" if dominant == "w13" else "w13"], peaks)
+                            per_kernel["w2" if dominant == "w13" else "w13"], peaks, kernel_names(L))
     layer_gbs = alg["layer_bytes"] / (ms_per_step / 1e3) / 1e9
     layer_tflops = alg["flops"] / (ms_per_step / 1e3) / 1e12
 

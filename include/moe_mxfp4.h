@@ -20,7 +20,8 @@
  *   - Pointers named d_* are DEVICE pointers (cudaMalloc'd or equivalent) on
  *     the current device; the caller allocates and owns all of them. The
  *     library never allocates, frees or keeps device memory between calls.
- *     Every device pointer must be 16-byte aligned.
+ *     Every device pointer must be 16-byte aligned; the forward's workspace
+ *     256-byte aligned (as cudaMalloc returns it).
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *     stream). All work is enqueued on that stream only; no call
  *     synchronises the device or copies between host and device (except
@@ -208,8 +209,9 @@ size_t moe_mxfp4_workspace_bytes(const moe_layer_desc *desc);
  *   d_offsets, d_padded_offsets, d_row_to_pair   from moe_permute.
  * Output:
  *   d_y              fp32 [T, H], fully overwritten.
- * d_workspace: moe_mxfp4_workspace_bytes(desc) bytes, contents need not be
- * initialised; the call resets its device error word.
+ * d_workspace: moe_mxfp4_workspace_bytes(desc) bytes, 256-byte aligned
+ * (MOE_ERR_MISALIGNED otherwise), contents need not be initialised; the call
+ * resets its device error word.
  * Numerics: block-scaled tensor-core MMAs (tcgen05 kind::mxf8f6f4) of the
  * E2M1 weights with their E8M0 scales against the activations written as sums
  * of MXFP8 terms (E4M3 values, one E8M0 scale per 32 K-elements, term scales

@@ -182,7 +182,7 @@ const char *moe_status_string(moe_status_t s)
     case MOE_OK: return "ok";
     case MOE_ERR_INVALID_ARG: return "invalid argument";
     case MOE_ERR_UNSUPPORTED: return "unsupported shape";
-    case MOE_ERR_MISALIGNED: return "pointer not 16-byte aligned";
+    case MOE_ERR_MISALIGNED: return "pointer not 16-byte aligned (the forward workspace: 256-byte)";
     case MOE_ERR_WORKSPACE: return "workspace or packed buffer too small";
     case MOE_ERR_CUDA: return "CUDA error";
     case MOE_ERR_DEVICE: return "device-detected invalid input (expert id out of range)";
@@ -336,6 +336,7 @@ moe_status_t moe_mxfp4_forward_timed(const moe_layer_desc *d, const uint16_t *d_
         if (!p) return MOE_ERR_INVALID_ARG;
     for (const void *p : ptrs)
         if (!aligned16(p)) return MOE_ERR_MISALIGNED;
+    if (reinterpret_cast<uintptr_t>(d_workspace) & 255u) return MOE_ERR_MISALIGNED;   // 32-byte stores inside
     Layout L = workspace_layout(d);
     if (workspace_bytes < L.total) return MOE_ERR_WORKSPACE;
     cudaStream_t s = (cudaStream_t)stream;

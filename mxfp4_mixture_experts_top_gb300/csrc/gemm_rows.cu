@@ -426,22 +426,27 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_rows_kernel(const __gr
                             const uint32_t hi = mxfp8_term_pair(h[4 * z + 2], h[4 * z + 3], e1, t, sb);
                             w[z] = lo | (hi << 16);
                         }
-                        uint4 *dq = reinterpret_cast<uint4 *>(p.hq + (((int64_t)tl.mb * NT + t) * p.rows_cap + row) * 128 +
-                                                              blk * 32);
-                        dq[0] = make_uint4(w[0], w[1], w[2], w[3]);
-                        dq[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                        ptx::st_global_v8(p.hq + (((int64_t)tl.mb * NT + t) * p.rows_cap + row) * 128 + blk * 32, w);
                         sbytes[t] |= sb << (8 * ch);
                     }
                 } else if (pair >= 0) {
-                    float4 *dst = reinterpret_cast<float4 *>(p.staging + (int64_t)pair * p.H + (int64_t)tl.mb * C::TN + c0);
+                    // 256 contiguous bytes of the pair's staging row per chunk, in 32-byte stores (the
+                    // combine reads them back once, after the whole launch)
+                    float *dst = p.staging + (int64_t)pair * p.H + (int64_t)tl.mb * C::TN + c0;
 #pragma unroll
-                    for (int z = 0; z < 8; ++z)
-                        dst[z] = make_float4(__uint_as_float(a0[4 * z]), __uint_as_float(a0[4 * z + 1]),
-                                             __uint_as_float(a0[4 * z + 2]), __uint_as_float(a0[4 * z + 3]));
+                    for (int z = 0; z < 4; ++z) {
+                        uint32_t v[8];
 #pragma unroll
-                    for (int z = 0; z < 8; ++z)
-                        dst[8 + z] = make_float4(__uint_as_float(a1[4 * z]), __uint_as_float(a1[4 * z + 1]),
-                                                 __uint_as_float(a1[4 * z + 2]), __uint_as_float(a1[4 * z + 3]));
+                        for (int u = 0; u < 8; ++u) v[u] = a0[8 * z + u];
+                        ptx::st_global_v8_stream(dst + 8 * z, v);
+                    }
+#pragma unroll
+                    for (int z = 0; z < 4; ++z) {
+                        uint32_t v[8];
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) v[u] = a1[8 * z + u];
+                        ptx::st_global_v8_stream(dst + 32 + 8 * z, v);
+                    }
                 }
             }
             if (MODE == 0 && ok && row_ok) {

@@ -156,6 +156,24 @@ __device__ __forceinline__ void prefetch_tmap(const void *tmap)
     asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }
 
+// 32-byte global stores (256-bit vectors, sm_100 and later; the address must be 32-byte aligned).
+// A warp whose lanes write 32 bytes each to different rows fills whole 32-byte sectors, where two
+// 16-byte stores would move two partly written sectors each.
+__device__ __forceinline__ void st_global_v8(void *p, const uint32_t (&v)[8])
+{
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
+                 ::"l"(p), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+                 : "memory");
+}
+
+// The same, for data read once much later by another kernel: not kept in L1, first out of L2.
+__device__ __forceinline__ void st_global_v8_stream(void *p, const uint32_t (&v)[8])
+{
+    asm volatile("st.global.L1::no_allocate.L2::evict_first.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
+                 ::"l"(p), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+                 : "memory");
+}
+
 // ----------------------------------------------------------------- tcgen05
 // Allocate `ncols` TMEM columns (power of two >= 32); whole warp executes.
 // The TMEM base address is written to shared memory at `dst`.

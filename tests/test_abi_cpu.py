@@ -98,6 +98,8 @@ def test_entry_points_reject_bad_arguments_without_launching(lib):
     assert lib.moe_mxfp4_forward(ctypes.byref(d), fake, fake, fake, fake, fake, fake, fake, fake, 16, null) == 4
     assert lib.moe_mxfp4_forward(ctypes.byref(d), odd, fake, fake, fake, fake, fake, fake, fake, 1 << 40, null) == 3
     assert lib.moe_mxfp4_forward(ctypes.byref(d), null, fake, fake, fake, fake, fake, fake, fake, 1 << 40, null) == 1
+    ws16 = ctypes.c_void_p(0x10010)        # 16-byte aligned, not 256: the forward workspace needs 256
+    assert lib.moe_mxfp4_forward(ctypes.byref(d), fake, fake, fake, fake, fake, fake, fake, ws16, 1 << 40, null) == 3
     assert lib.moe_mxfp4_prepack(ctypes.byref(d), fake, fake, fake, fake, fake, 16, null) == 4
     assert lib.moe_mxfp4_dequant_bf16(ctypes.byref(d), fake, 2, 0, fake, null) == 1
     assert lib.moe_mxfp4_dequant_bf16(ctypes.byref(d), fake, 0, 8, fake, null) == 1
