@@ -676,6 +676,11 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_kernel(const __grid_co
 // stage for all rows and terms of a tile); scales are 32-bit words
 // [H/128][NT_X][rows_sf], byte b % 4 of word (b / 4, t, r) for 32-element
 // block b. Rows past padded[E] are not touched.
+// A thread stores its block's 32 term bytes with one 32-byte store per term
+// (whole sectors); the four threads of a scale word (consecutive blocks of one
+// row: H / 32 is a multiple of 4) hand their bytes to the first, which stores
+// the word. Every warp runs the same number of iterations (lanes past the end
+// only skip the stores), so the shuffles always see the whole warp.
 __global__ void gather_quant_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ row_to_pair,
                                     const int32_t *__restrict__ padded, int E, int H, int k, int64_t P,
                                     int64_t rows_cap, int64_t rows_sf, uint8_t *__restrict__ xq,
@@ -686,25 +691,19 @@ __global__ void gather_quant_kernel(const uint16_t *__restrict__ x, const int32_
     const int64_t R = __ldg(padded + E);
     const int nblk = H / 32;
     const int64_t n = R * nblk;
-    for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < n; idx += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t r = idx / nblk;
-        const int b = (int)(idx - r * nblk);
-        const int32_t pr = __ldg(row_to_pair + r);
-        if (!(pr >= 0 && pr < P)) {
-            // padding row (or a bad entry, recorded below): an all-zero block, whose terms are zero
-            // bytes with scale byte 0 (the conversion below gives exactly these for zeros)
-            if (pr >= P && b == 0) record_error(dev_error, DEV_ERR_ID_RANGE);
-#pragma unroll
-            for (int t = 0; t < NT_X; ++t) {
-                uint4 *dst = reinterpret_cast<uint4 *>(xq + (((int64_t)(b >> 2) * NT_X + t) * rows_cap + r) * 128 + (b & 3) * 32);
-                dst[0] = make_uint4(0u, 0u, 0u, 0u);
-                dst[1] = make_uint4(0u, 0u, 0u, 0u);
-                xs[(((int64_t)(b >> 2) * NT_X + t) * rows_sf + r) * 4 + (b & 3)] = 0;
-            }
-            continue;
-        }
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    const int64_t warp0 = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) & ~(int64_t)31;
+    const int lane = threadIdx.x & 31;
+    for (int64_t wbase = warp0; wbase < n; wbase += stride) {
+        const int64_t idx = wbase + lane;
+        const bool live = idx < n;
+        const int64_t r = live ? idx / nblk : 0;
+        const int b = live ? (int)(idx - r * nblk) : 0;
+        const int32_t pr = live ? __ldg(row_to_pair + r) : -1;
+        const bool real = live && pr >= 0 && pr < P;
+        if (live && pr >= P && b == 0) record_error(dev_error, DEV_ERR_ID_RANGE);
         float v[32];
-        {
+        if (real) {
             const uint4 *src = reinterpret_cast<const uint4 *>(x + (int64_t)(pr / k) * H + b * 32);
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
@@ -718,22 +717,142 @@ __global__ void gather_quant_kernel(const uint16_t *__restrict__ x, const int32_
             }
         }
         float mx = 0.f;
+        if (real) {
 #pragma unroll
-        for (int q = 0; q < 32; ++q) mx = fmaxf(mx, fabsf(v[q]));
+            for (int q = 0; q < 32; ++q) mx = fmaxf(mx, fabsf(v[q]));
+        }
         const int e1 = mxfp8_block_exp(mx);
 #pragma unroll
         for (int t = 0; t < NT_X; ++t) {
-            uint32_t wq[8], sbyte = 0;
+            // a padding row (or a bad entry, recorded above) is an all-zero block: zero term bytes and
+            // scale byte 0, what the conversion gives for zeros, written without converting
+            uint32_t wq[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u}, sbyte = 0;
+            if (real) {
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const uint32_t lo = mxfp8_term_pair(v[4 * q], v[4 * q + 1], e1, t, sbyte);
+                    const uint32_t hi = mxfp8_term_pair(v[4 * q + 2], v[4 * q + 3], e1, t, sbyte);
+                    wq[q] = lo | (hi << 16);
+                }
+            }
+            // the scale word of blocks 4j .. 4j+3: lane (b % 4 == 0) collects its three neighbours' bytes
+            uint32_t word = sbyte;
+            word |= __shfl_down_sync(0xFFFFFFFFu, sbyte, 1) << 8;
+            word |= __shfl_down_sync(0xFFFFFFFFu, sbyte, 2) << 16;
+            word |= __shfl_down_sync(0xFFFFFFFFu, sbyte, 3) << 24;
+            if (live) {
+                ptx::st_global_v8(xq + (((int64_t)(b >> 2) * NT_X + t) * rows_cap + r) * 128 + (b & 3) * 32, wq);
+                if ((b & 3) == 0)
+                    *reinterpret_cast<uint32_t *>(xs + (((int64_t)(b >> 2) * NT_X + t) * rows_sf + r) * 4) = word;
+            }
+        }
+    }
+}
+
+// Gather in two passes for batches with many rows per expert, where the one-pass gather above would
+// convert every token's x k times (once per row). Pass 1, one warp per row: a real row records itself
+// in the inverse map p2r[pair] = row; a padding row gets its zero terms and scale words. Pass 2, one
+// thread per (token, 32-element block) as above: the block's terms are computed once and stored to
+// each of the token's k rows. p2r lives in the fp32 staging region, which only the W2 GEMM writes
+// later; an entry is trusted only if row_to_pair sends its row back to the pair (a pair without a row,
+// i.e. with an expert id the permutation skipped, keeps whatever the region held).
+__global__ void gather_rows_kernel(const int32_t *__restrict__ row_to_pair, const int32_t *__restrict__ padded,
+                                   int E, int H, int64_t P, int64_t rows_cap, int64_t rows_sf,
+                                   uint8_t *__restrict__ xq, uint8_t *__restrict__ xs, int32_t *__restrict__ p2r,
+                                   int32_t *dev_error)
+{
+    griddep_wait();                  // the permutation comes from an earlier kernel
+    griddep_launch_dependents();
+    const int64_t R = __ldg(padded + E);
+    const int lane = threadIdx.x & 31;
+    const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    const int slabs = H / 128;
+    const uint32_t zero[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+    for (int64_t r = blockIdx.x * (int64_t)(blockDim.x >> 5) + (threadIdx.x >> 5); r < R; r += warps) {
+        const int32_t pr = __ldg(row_to_pair + r);
+        if (pr >= 0 && pr < P) {
+            if (lane == 0) p2r[pr] = (int32_t)r;
+            continue;
+        }
+        if (pr >= P && lane == 0) record_error(dev_error, DEV_ERR_ID_RANGE);
+        // zero terms: 4 lanes per 128-byte slab row, 8 slabs per pass of the warp
+        for (int i = lane; i < slabs * 4; i += 32) {
+            const int sl = i >> 2;
+#pragma unroll
+            for (int t = 0; t < NT_X; ++t) {
+                ptx::st_global_v8(xq + (((int64_t)sl * NT_X + t) * rows_cap + r) * 128 + (i & 3) * 32, zero);
+                if ((i & 3) == 0) *reinterpret_cast<uint32_t *>(xs + (((int64_t)sl * NT_X + t) * rows_sf + r) * 4) = 0u;
+            }
+        }
+    }
+}
+
+__global__ void gather_tokens_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ row_to_pair,
+                                     const int32_t *__restrict__ padded, const int32_t *__restrict__ p2r, int E,
+                                     int T, int H, int k, int64_t rows_cap, int64_t rows_sf,
+                                     uint8_t *__restrict__ xq, uint8_t *__restrict__ xs)
+{
+    griddep_wait();                  // the inverse map and the padding rows come from the kernel before
+    griddep_launch_dependents();
+    const int64_t R = __ldg(padded + E);
+    const int nblk = H / 32;
+    const int64_t n = (int64_t)T * nblk;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    const int64_t warp0 = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) & ~(int64_t)31;
+    const int lane = threadIdx.x & 31;
+    for (int64_t wbase = warp0; wbase < n; wbase += stride) {
+        const int64_t idx = wbase + lane;
+        const bool live = idx < n;
+        const int64_t t = live ? idx / nblk : 0;
+        const int b = live ? (int)(idx - t * nblk) : 0;
+        float v[32];
+        float mx = 0.f;
+        if (live) {
+            const uint4 *src = reinterpret_cast<const uint4 *>(x + t * H + b * 32);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const uint4 u = __ldg(src + q);
+                const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                for (int z = 0; z < 4; ++z) {
+                    v[q * 8 + 2 * z] = __uint_as_float(w[z] << 16);
+                    v[q * 8 + 2 * z + 1] = __uint_as_float(w[z] & 0xFFFF0000u);
+                }
+            }
+#pragma unroll
+            for (int q = 0; q < 32; ++q) mx = fmaxf(mx, fabsf(v[q]));
+        }
+        const int e1 = mxfp8_block_exp(mx);
+        uint32_t wq[NT_X][8], word[NT_X];
+#pragma unroll
+        for (int tt = 0; tt < NT_X; ++tt) {
+            uint32_t sbyte = 0;
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
-                const uint32_t lo = mxfp8_term_pair(v[4 * q], v[4 * q + 1], e1, t, sbyte);
-                const uint32_t hi = mxfp8_term_pair(v[4 * q + 2], v[4 * q + 3], e1, t, sbyte);
-                wq[q] = lo | (hi << 16);
+                if (live) {
+                    const uint32_t lo = mxfp8_term_pair(v[4 * q], v[4 * q + 1], e1, tt, sbyte);
+                    const uint32_t hi = mxfp8_term_pair(v[4 * q + 2], v[4 * q + 3], e1, tt, sbyte);
+                    wq[tt][q] = lo | (hi << 16);
+                } else {
+                    wq[tt][q] = 0u;
+                }
             }
-            uint4 *dst = reinterpret_cast<uint4 *>(xq + (((int64_t)(b >> 2) * NT_X + t) * rows_cap + r) * 128 + (b & 3) * 32);
-            dst[0] = make_uint4(wq[0], wq[1], wq[2], wq[3]);
-            dst[1] = make_uint4(wq[4], wq[5], wq[6], wq[7]);
-            xs[(((int64_t)(b >> 2) * NT_X + t) * rows_sf + r) * 4 + (b & 3)] = (uint8_t)sbyte;
+            word[tt] = sbyte;
+            word[tt] |= __shfl_down_sync(0xFFFFFFFFu, sbyte, 1) << 8;
+            word[tt] |= __shfl_down_sync(0xFFFFFFFFu, sbyte, 2) << 16;
+            word[tt] |= __shfl_down_sync(0xFFFFFFFFu, sbyte, 3) << 24;
+        }
+        if (!live) continue;
+        for (int j = 0; j < k; ++j) {
+            const int64_t p = t * k + j;
+            const int32_t r = __ldg(p2r + p);
+            if (!(r >= 0 && r < R) || __ldg(row_to_pair + r) != (int32_t)p) continue;   // no row for this pair
+#pragma unroll
+            for (int tt = 0; tt < NT_X; ++tt) {
+                ptx::st_global_v8(xq + (((int64_t)(b >> 2) * NT_X + tt) * rows_cap + r) * 128 + (b & 3) * 32, wq[tt]);
+                if ((b & 3) == 0)
+                    *reinterpret_cast<uint32_t *>(xs + (((int64_t)(b >> 2) * NT_X + tt) * rows_sf + r) * 4) = word[tt];
+            }
         }
     }
 }
@@ -828,7 +947,22 @@ cudaError_t launch_forward(const ForwardArgs &a, cudaStream_t s)
     for (int i = 0; i < 5 && a.events; ++i)
         if (a.events[i]) pdl = false;
     mark(a, 0, s);
-    {
+    const bool two_pass = a.regime == Regime::Mid || a.regime == Regime::Large || a.regime == Regime::Huge;
+    if (two_pass) {
+        int32_t *p2r = reinterpret_cast<int32_t *>(a.staging);     // P entries; W2 overwrites them later
+        int grid = (int)((a.rows_cap + 7) / 8);                      // 8 warps (rows) per block
+        if (grid > 8 * 1024) grid = 8 * 1024;
+        err = launch_ex(gather_rows_kernel, dim3(grid), dim3(256), 0, s, pdl, a.row_to_pair, a.padded, a.E, a.H, P,
+                        a.rows_cap, a.rows_sf, a.xq, a.xs, p2r, a.dev_error);
+        if (err != cudaSuccess) return err;
+        const int64_t n = (int64_t)a.T * (a.H / 32);
+        grid = (int)((n + 255) / 256);
+        if (grid > 8 * 1024) grid = 8 * 1024;
+        if (grid < 1) grid = 1;
+        err = launch_ex(gather_tokens_kernel, dim3(grid), dim3(256), 0, s, pdl, a.x, a.row_to_pair, a.padded,
+                        (const int32_t *)p2r, a.E, a.T, a.H, a.k, a.rows_cap, a.rows_sf, a.xq, a.xs);
+        if (err != cudaSuccess) return err;
+    } else {
         const int64_t n = a.rows_cap * (a.H / 32);
         int grid = (int)((n + 255) / 256);
         if (grid > 8 * 1024) grid = 8 * 1024;
@@ -905,7 +1039,7 @@ cudaError_t launch_forward(const ForwardArgs &a, cudaStream_t s)
         if (err != cudaSuccess) return err;
     }
     mark(a, 4, s);
-    note_launch(4);
+    note_launch(two_pass ? 5 : 4);
     return cudaSuccess;
 }
 

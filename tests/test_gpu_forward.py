@@ -208,6 +208,27 @@ def test_forward_tiny_intermediates(gpu_lib, gpu_layers):
     assert worst < {2: 3e-2, 3: 3e-3}[nt_h]
 
 
+@pytest.mark.parametrize("T,H,I,E,k,block_m", [(300, 256, 128, 64, 6, 64),     # 28 rows per expert
+                                                 (700, 256, 256, 8, 2, 128)])   # 175: token-major tiles
+def test_gather_two_pass_terms(gpu_lib, gpu_layers, T, H, I, E, k, block_m):
+    """Above 16 rows per expert on average the gather converts each token once and stores its terms
+    to all k of its rows (through an inverse of row_to_pair); padding rows get zero terms. Every
+    gathered row against the token's bf16 values."""
+    moe = gpu_lib
+    L = synth.make_layer(T=T, H=H, E=E, k=k, I=I, seed=T * 3 + E)
+    r = _run_layer(moe, gpu_layers, L, block_m)
+    lay = moe.workspace_layout(r["desc"])
+    R = moe.rows_capacity(T, E, k, block_m)
+    Rv = int(r["perm"]["padded_offsets"][-1].item())
+    x = synth.bf16_bits_to_f64(L["x_bits"])
+    r2p = r["perm"]["row_to_pair"].cpu().numpy()[:Rv]
+    assert (r2p < 0).any(), "the case should hold padding rows"
+    xg = _terms(r["ws"], lay["xq"], lay["xs"], 2, R, H)[:Rv]
+    want = np.where(r2p[:, None] >= 0, x[np.maximum(r2p, 0) // k], 0.0)
+    assert np.all(xg[r2p < 0] == 0)
+    assert np.mean(xg == want) > 0.999 and np.abs(xg - want).max() <= 1e-6 * np.abs(x).max()
+
+
 def test_forward_decode_t8_all_outputs(gpu_lib, gpu_layers):
     L = synth.make_config("decode_t8_h4096_e256")
     r = _run_layer(gpu_lib, gpu_layers, L)
