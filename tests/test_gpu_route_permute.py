@@ -142,11 +142,12 @@ def test_route_permute_deterministic(gpu_lib):
         assert torch.equal(pa[n], pb[n])
 
 
-@pytest.mark.parametrize("T", [0, 1, 8, 37, 127, 128, 129, 512])
+@pytest.mark.parametrize("T", [0, 1, 8, 37, 127, 128, 129, 512, 1501, 8191])
 @pytest.mark.parametrize("E,k,block_m", [(256, 6, 16), (32, 6, 128), (1024, 32, 16), (8, 8, 64)])
 def test_fused_route_permute_matches_oracle(gpu_lib, T, E, k, block_m):
-    """moe_route_permute (one launch up to T = 128, two above) gives the oracle's ids, weights,
-    bitmatrix and permutation, with heavy ties in half of the cases."""
+    """moe_route_permute (one launch up to T = 128; above, routing, then the one-block permutation up
+    to 4,096 pairs and the chunked one beyond) gives the oracle's ids, weights, bitmatrix and
+    permutation, with heavy ties in half of the cases."""
     rng = np.random.default_rng(T * 131 + E + k)
     if T % 2:
         pool = np.array([-1.0, -0.0, 0.0, 0.25, 0.25, 2.0], dtype=np.float32)
