@@ -98,9 +98,9 @@ ROWS_KERNEL_NAMES = {"w13": "moe_gemm_rows_kernel<W13Rows> (token-major grouped 
 
 def kernel_names(L):
     """Names of the two GEMM kernels the library launches for this layer: the token-major tiles above
-    128 rows per expert on average when H is a multiple of 256, the weight-major tiles otherwise (the
+    64 rows per expert on average when H is a multiple of 256, the weight-major tiles otherwise (the
     library's tile choice, restated here only to label the JSON line)."""
-    rows = L["T"] * L["k"] / L["E"] > 128 and L["H"] % 256 == 0
+    rows = L["T"] * L["k"] / L["E"] > 64 and L["H"] % 256 == 0
     return ROWS_KERNEL_NAMES if rows else KERNEL_NAMES
 
 

@@ -904,7 +904,7 @@ Regime pick_regime(int T, int k, int E, int H)
     if (avg <= 2.0) return Regime::Tiny;
     if (avg <= 16.0) return Regime::Small;
     if (avg <= 64.0) return Regime::Mid;
-    if (avg <= 128.0 || H % 256 != 0) return Regime::Large;
+    if (H % 256 != 0) return Regime::Large;   // weight-major 96-row tiles
     return Regime::Huge;       // token-major tiles (gemm_rows.cu): 256 W2 output rows per tile
 }
 

@@ -275,9 +275,10 @@ def test_forward_swiglu_clamp_variant(gpu_lib, gpu_layers, name):
 @pytest.mark.parametrize("T,H,I,E,k", [(1, 256, 128, 8, 2), (17, 128, 256, 16, 4), (200, 256, 128, 5, 3),
                                        (300, 128, 128, 64, 6),
                                        (40, 256, 128, 1024, 6),     # > 512 experts: the wide-E decode W2 tiles
-                                       (11000, 128, 128, 1024, 6),  # > 64 rows per expert, > 512 experts: wide-E prefill tiles
-                                       (700, 256, 256, 8, 2),       # prefill tiles with at most 512 experts, all outputs
-                                       (600, 384, 128, 8, 2)])      # prefill tiles, an odd number of W2 output tiles
+                                       (11000, 128, 128, 1024, 6),  # > 64 rows per expert, H % 256 != 0, > 512 experts: wide-E 96-row tiles
+                                       (700, 256, 256, 8, 2),       # token-major tiles, all outputs
+                                       (600, 384, 128, 8, 2),       # H % 256 != 0: 96-row tiles, an odd number of W2 output tiles
+                                       (600, 384, 256, 32, 6)])     # 112 rows per expert, H % 256 != 0: 96-row tiles, <= 512 experts
 def test_forward_fuzz_shapes(gpu_lib, gpu_layers, T, H, I, E, k):
     L = synth.make_layer(T=T, H=H, E=E, k=k, I=I, seed=T + E)
     r = _run_layer(gpu_lib, gpu_layers, L)
@@ -290,7 +291,7 @@ def test_forward_fuzz_shapes(gpu_lib, gpu_layers, T, H, I, E, k):
                                              (1000, 256, 384, 5, 3, 10.0),   # 600 rows per expert, clamp, I/128 odd
                                              (520, 768, 128, 2, 1, 0.0)])    # 260 rows per expert, three W2 blocks
 def test_forward_token_major_tiles(gpu_lib, gpu_layers, T, H, I, E, k, limit, block_m):
-    """More than 128 rows per expert on average selects the token-major tiles (128 token rows x 256
+    """More than 64 rows per expert on average selects the token-major tiles (128 token rows x 256
     weight rows, terms summed by the tensor core): every output against the oracle, with small and
     large row padding, partial last token blocks and rows of the next expert inside a tile."""
     L = synth.make_layer(T=T, H=H, E=E, k=k, I=I, seed=T + H)
