@@ -400,6 +400,30 @@ def time_fast(step_fast, flush_buf, steps):
     return [a.elapsed_time(b) for a, b in ev]
 
 
+def time_fast_combine(moe, layer, x, logits, flush_buf, steps):
+    """Device time (ms) of each of `steps` steps with MOE_FLAG_FAST_COMBINE (up to 16 rows per expert
+    W2 adds w * o into y with reduction atomics: no per-pair rows, no combine kernel), L2 flushed
+    before each. Not bit-reproducible where taken, so not the headline; reported beside it."""
+    import copy
+    import torch
+    d = copy.copy(layer.desc)
+    d.flags = moe.FLAG_FAST_COMBINE
+    b = layer.bufs
+    k = d.k
+
+    def step():
+        moe.route_permute(logits, k, d.block_m, out=(b["ids"], b["w"], b["bm"]), perm_out=b["perm"],
+                          error=b["perm_err"])
+        moe.forward(d, x, layer.packed, b["w"], b["perm"], layer.workspace, b["y"])
+    for _ in range(3):
+        flush_buf.zero_()
+        step()
+    st = time_fast(step, flush_buf, steps)
+    torch.cuda.synchronize()
+    assert layer.forward_error() == 0, "device error in the fast-combine steps"
+    return st
+
+
 def summarize(evsets):
     # events: 0 start, 1 after route+permute, 2 before gather, 3 after gather, 4 after W13, 5 after W2, 6 after combine
     keys = ["route_permute", "gather", "w13", "w2", "combine"]
@@ -426,9 +450,10 @@ def measure_config(moe, name, L, steps, warmup, flush_buf, peaks):
     event pass, and the rooflines of the layer and of both GEMMs."""
     import torch
     hbm, bf16, bf16_sus, _ = peaks
-    lay, _, _, step, mk, fast = time_workload(moe, L, steps, warmup, flush_buf)
+    lay, x, logits, step, mk, fast = time_workload(moe, L, steps, warmup, flush_buf)
     st = time_fast(fast, flush_buf, steps)
     ms = float(np.mean(st))
+    fc_ms = float(np.mean(time_fast_combine(moe, lay, x, logits, flush_buf, steps)))
     evs = [mk() for _ in range(steps)]
     for ev in evs:
         flush_buf.zero_()
@@ -442,6 +467,7 @@ def measure_config(moe, name, L, steps, warmup, flush_buf, peaks):
     mxf8 = MXF8_OVER_BF16 * bf16
     out = {
         "tokens_per_s": L["T"] / (ms / 1e3), "ms_per_step": ms, "touched_experts": a["touched"],
+        "fast_combine": {"tokens_per_s": L["T"] / (fc_ms / 1e3), "ms_per_step": fc_ms},
         "activation_terms": {"x": nt_x, "h": nt_h},
         "step_ms": {"p10": float(np.percentile(st, 10)), "p50": float(np.percentile(st, 50)),
                     "p90": float(np.percentile(st, 90))},
@@ -585,6 +611,13 @@ def run_ours(args, world, rank, local):
     del graph
     graph_line = {"value": world * T / (g_ms / 1e3), "unit": UNIT, "ms_per_step": g_ms,
                   "how": "route+permute+forward captured in one CUDA graph, replayed; L2 flushed before each replay"}
+    fc = time_fast_combine(moe, layer, x, logits, flush_buf, args.steps)
+    fc_ms = float(np.mean(fc))
+    fast_line = {"value": world * T / (fc_ms / 1e3), "unit": UNIT, "ms_per_step": fc_ms,
+                 "how": "the same step with MOE_FLAG_FAST_COMBINE, which lets the library add w * o into y "
+                        "with fp32 reduction atomics from W2 (no per-pair rows, no combine kernel) where that is "
+                        "faster, up to 16 rows per expert; larger batches keep the slot-ordered combine. Not "
+                        "bit-reproducible where taken, so not the headline"}
     e2e = {"value": world * T / (e2e_ms / 1e3), "unit": UNIT, "ms_per_step": e2e_ms,
            "h2d_bytes_per_step": T * H * 2 + T * E * 4, "d2h_bytes_per_step": T * H * 4,
            "how": "public API (moe_route_permute + moe_mxfp4_forward) with pinned host buffers: per step one "
@@ -647,6 +680,7 @@ def run_ours(args, world, rank, local):
             "step_ms": {"p10": float(np.percentile(step_ms, 10)), "p50": float(np.percentile(step_ms, 50)),
                         "p90": float(np.percentile(step_ms, 90))},
             "graph": graph_line,
+            "fast_combine": fast_line,
         }
         if per_config:
             line["per_config"] = per_config

@@ -73,8 +73,23 @@ typedef enum {
  *   the permutation (16, 32, 64 or 128).
  *   swiglu_limit > 0 enables the clamp gate = min(gate, L),
  *   up = clamp(up, -L, L) before SiLU(gate) * up; <= 0 disables it.
- *   flags: reserved, must be 0.
+ *   flags: 0 or MOE_FLAG_FAST_COMBINE.
  * Supported: 1 <= k <= min(E, 32), E <= 1024, H and I multiples of 128. */
+
+/*
+ * MOE_FLAG_FAST_COMBINE: permits the W2 GEMM to add w[t,j] * o_j straight
+ * into y with fp32 reduction atomics (red.global.add) instead of writing
+ * per-pair rows that a separate kernel sums in slot order; y is then zeroed by
+ * the forward first. This saves the per-pair rows' round trip and one launch.
+ * The library takes it where it is faster: batches of up to 16 rows per
+ * expert on average (T*k/E <= 16, the decode shapes); larger batches keep the
+ * slot-ordered combine with or without the flag. With the atomic combine the
+ * sum order depends on the order the GPU retires the adds: results match the
+ * default path up to fp32 rounding (a few ulp of y) and are not
+ * bit-reproducible from run to run. The default (flags 0) is always the
+ * deterministic slot-ordered combine.
+ */
+#define MOE_FLAG_FAST_COMBINE 1u
 typedef struct moe_layer_desc {
     int T, H, I, E, k, block_m;
     float swiglu_limit;

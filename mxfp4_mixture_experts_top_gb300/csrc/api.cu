@@ -129,7 +129,7 @@ moe_status_t check_desc(const moe_layer_desc *d)
 {
     if (!d) return MOE_ERR_INVALID_ARG;
     if (d->T < 0 || d->H <= 0 || d->I <= 0 || d->E <= 0 || d->k <= 0 || d->k > d->E) return MOE_ERR_INVALID_ARG;
-    if (d->flags != 0) return MOE_ERR_INVALID_ARG;
+    if (d->flags & ~MOE_FLAG_FAST_COMBINE) return MOE_ERR_INVALID_ARG;
     if (d->E > 1024 || d->k > 32) return MOE_ERR_UNSUPPORTED;
     if (d->H % 128 || d->I % 128) return MOE_ERR_UNSUPPORTED;
     if (d->block_m != 16 && d->block_m != 32 && d->block_m != 64 && d->block_m != 128) return MOE_ERR_UNSUPPORTED;
@@ -351,6 +351,7 @@ moe_status_t moe_mxfp4_forward_timed(const moe_layer_desc *d, const uint16_t *d_
     a.k = d->k;
     a.block_m = d->block_m;
     a.swiglu_limit = d->swiglu_limit;
+    a.fast_combine = false;      // set below, once the regime is known
     a.rows_cap = R;
     a.rows_sf = scale_rows(d);
     a.x = d_x;
@@ -369,6 +370,11 @@ moe_status_t moe_mxfp4_forward_timed(const moe_layer_desc *d, const uint16_t *d_
     a.num_sms = sm_count();
     a.events = events;
     a.regime = pick_regime(d->T, d->k, d->E, d->H);
+    // The flag permits the atomic combine; it is used where it measured faster (up to 16 rows per
+    // expert on average). Larger batches keep the slot-ordered combine: their W2 epilogues would
+    // issue T*k*H reductions, which cost more in L2 than the per-pair rows' round trip.
+    a.fast_combine = (d->flags & MOE_FLAG_FAST_COMBINE) != 0 &&
+                     (a.regime == Regime::Tiny || a.regime == Regime::Small);
     const uint32_t sps = (uint32_t)regime_sps(a.regime);
     const uint8_t *w13 = a.packed, *w2 = a.packed + packed_w13_bytes(d->E, d->H, d->I);
     const uint64_t rows13 = (uint64_t)d->E * 2 * d->I * (d->H / KSLAB);   // 128-element rows of W13 nibbles

@@ -645,13 +645,27 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_kernel(const __grid_co
                 } else if (ok) {
                     const int c = tl.mb * TILE_ROWS + warp * 32 + lane;
                     const int my_pair = (lane < 16) ? __ldg(p.row_to_pair + tl.row0 + c0 + lane) : -1;
+                    if (p.y) {
+                        // fast combine: w * o added into the token's row of y; lane j < 16 holds row j's weight
+                        const float my_w = (my_pair >= 0 && my_pair < p.P) ? __ldg(p.topk_w + my_pair) : 0.f;
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const int pr = __shfl_sync(0xFFFFFFFFu, my_pair, j);
-                        if (pr >= 0 && pr < p.P)
-                            p.staging[(int64_t)pr * p.H + c] = __uint_as_float(raw[j]);
-                        else if (pr >= p.P && lane == 0)
-                            record_error(p.dev_error, DEV_ERR_ID_RANGE);
+                        for (int j = 0; j < 16; ++j) {
+                            const int pr = __shfl_sync(0xFFFFFFFFu, my_pair, j);
+                            const float wj = __shfl_sync(0xFFFFFFFFu, my_w, j);
+                            if (pr >= 0 && pr < p.P)
+                                ptx::red_add_f32(p.y + (int64_t)(pr / p.k) * p.H + c, wj * __uint_as_float(raw[j]));
+                            else if (pr >= p.P && lane == 0)
+                                record_error(p.dev_error, DEV_ERR_ID_RANGE);
+                        }
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            const int pr = __shfl_sync(0xFFFFFFFFu, my_pair, j);
+                            if (pr >= 0 && pr < p.P)
+                                p.staging[(int64_t)pr * p.H + c] = __uint_as_float(raw[j]);
+                            else if (pr >= p.P && lane == 0)
+                                record_error(p.dev_error, DEV_ERR_ID_RANGE);
+                        }
                     }
                 }
             }
@@ -669,6 +683,16 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_kernel(const __grid_co
     if (warp == 8) ptx::tmem_dealloc(tmem, TMEM_COLS);
 }
 
+// The fast combine adds into y: the gather kernel that runs first zeroes it (n4 float4 words; y is
+// 16-byte aligned), which the W2 GEMM, two launches later, sees complete.
+__device__ __forceinline__ void zero_y(float *y, int64_t n4)
+{
+    if (!y) return;
+    const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n4; i += (int64_t)gridDim.x * blockDim.x)
+        reinterpret_cast<float4 *>(y)[i] = z;
+}
+
 // Gathered activations as NT_X MXFP8 terms: row r of the permutation gets
 // the terms of x[token(r)], padding rows (row_to_pair == -1) get zeros. One
 // thread per (row, 32-element block). Terms are E4M3 bytes
@@ -684,10 +708,11 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_kernel(const __grid_co
 __global__ void gather_quant_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ row_to_pair,
                                     const int32_t *__restrict__ padded, int E, int H, int k, int64_t P,
                                     int64_t rows_cap, int64_t rows_sf, uint8_t *__restrict__ xq,
-                                    uint8_t *__restrict__ xs, int32_t *dev_error)
+                                    uint8_t *__restrict__ xs, int32_t *dev_error, float *y_zero, int64_t y_n4)
 {
     griddep_wait();                  // the permutation (and x) come from earlier kernels
     griddep_launch_dependents();
+    zero_y(y_zero, y_n4);
     const int64_t R = __ldg(padded + E);
     const int nblk = H / 32;
     const int64_t n = R * nblk;
@@ -759,10 +784,11 @@ __global__ void gather_quant_kernel(const uint16_t *__restrict__ x, const int32_
 __global__ void gather_rows_kernel(const int32_t *__restrict__ row_to_pair, const int32_t *__restrict__ padded,
                                    int E, int H, int64_t P, int64_t rows_cap, int64_t rows_sf,
                                    uint8_t *__restrict__ xq, uint8_t *__restrict__ xs, int32_t *__restrict__ p2r,
-                                   int32_t *dev_error)
+                                   int32_t *dev_error, float *y_zero, int64_t y_n4)
 {
     griddep_wait();                  // the permutation comes from an earlier kernel
     griddep_launch_dependents();
+    zero_y(y_zero, y_n4);
     const int64_t R = __ldg(padded + E);
     const int lane = threadIdx.x & 31;
     const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
@@ -947,13 +973,15 @@ cudaError_t launch_forward(const ForwardArgs &a, cudaStream_t s)
     for (int i = 0; i < 5 && a.events; ++i)
         if (a.events[i]) pdl = false;
     mark(a, 0, s);
+    float *y_zero = a.fast_combine ? a.y : nullptr;
+    const int64_t y_n4 = (int64_t)a.T * a.H / 4;
     const bool two_pass = a.regime == Regime::Mid || a.regime == Regime::Large || a.regime == Regime::Huge;
     if (two_pass) {
         int32_t *p2r = reinterpret_cast<int32_t *>(a.staging);     // P entries; W2 overwrites them later
         int grid = (int)((a.rows_cap + 7) / 8);                      // 8 warps (rows) per block
         if (grid > 8 * 1024) grid = 8 * 1024;
         err = launch_ex(gather_rows_kernel, dim3(grid), dim3(256), 0, s, pdl, a.row_to_pair, a.padded, a.E, a.H, P,
-                        a.rows_cap, a.rows_sf, a.xq, a.xs, p2r, a.dev_error);
+                        a.rows_cap, a.rows_sf, a.xq, a.xs, p2r, a.dev_error, y_zero, y_n4);
         if (err != cudaSuccess) return err;
         const int64_t n = (int64_t)a.T * (a.H / 32);
         grid = (int)((n + 255) / 256);
@@ -968,7 +996,7 @@ cudaError_t launch_forward(const ForwardArgs &a, cudaStream_t s)
         if (grid > 8 * 1024) grid = 8 * 1024;
         if (grid < 1) grid = 1;
         err = launch_ex(gather_quant_kernel, dim3(grid), dim3(256), 0, s, pdl, a.x, a.row_to_pair, a.padded, a.E,
-                        a.H, a.k, P, a.rows_cap, a.rows_sf, a.xq, a.xs, a.dev_error);
+                        a.H, a.k, P, a.rows_cap, a.rows_sf, a.xq, a.xs, a.dev_error, y_zero, y_n4);
         if (err != cudaSuccess) return err;
     }
     mark(a, 1, s);
@@ -987,6 +1015,8 @@ cudaError_t launch_forward(const ForwardArgs &a, cudaStream_t s)
     g.hq = a.hq;
     g.hs = a.hs;
     g.staging = a.staging;
+    g.y = nullptr;                    // W13 writes h; only W2 may add into y
+    g.topk_w = a.topk_w;
     g.dev_error = a.dev_error;
 
     // W13: K = H, 64 features (128 rows) per weight tile
@@ -1010,6 +1040,7 @@ cudaError_t launch_forward(const ForwardArgs &a, cudaStream_t s)
     mark(a, 2, s);
 
     // W2: K = I, 128 output features per weight tile
+    g.y = a.fast_combine ? a.y : nullptr;
     g.tm_a = a.tmap_w2;
     g.tm_a1 = a.tmap_w2_1;
     g.tm_b = a.tmap_hq;
@@ -1028,8 +1059,7 @@ cudaError_t launch_forward(const ForwardArgs &a, cudaStream_t s)
                                                       : launch_gemm<W2LargeWideE>(g, a.num_sms, s, pdl));
     if (err != cudaSuccess) return err;
     mark(a, 3, s);
-
-    {
+    if (!a.fast_combine) {           // the fast combine has already added every pair into y
         const int64_t n = (int64_t)a.T * (a.H / 4);
         int grid = (int)((n + 255) / 256);
         if (grid > 4 * 1024) grid = 4 * 1024;
@@ -1039,7 +1069,7 @@ cudaError_t launch_forward(const ForwardArgs &a, cudaStream_t s)
         if (err != cudaSuccess) return err;
     }
     mark(a, 4, s);
-    note_launch(two_pass ? 5 : 4);
+    note_launch((two_pass ? 5 : 4) - (a.fast_combine ? 1 : 0));
     return cudaSuccess;
 }
 

@@ -184,8 +184,11 @@ def route_permute(logits: torch.Tensor, k: int, block_m: int, out=None, perm_out
     return ids, w, bm, po
 
 
-def make_desc(T, H, I, E, k, block_m=16, swiglu_limit=0.0) -> LayerDesc:
-    return LayerDesc(T, H, I, E, k, block_m, float(swiglu_limit), 0)
+FLAG_FAST_COMBINE = 1   # MOE_FLAG_FAST_COMBINE
+
+
+def make_desc(T, H, I, E, k, block_m=16, swiglu_limit=0.0, flags=0) -> LayerDesc:
+    return LayerDesc(T, H, I, E, k, block_m, float(swiglu_limit), int(flags))
 
 
 def packed_bytes(desc: LayerDesc) -> int:
@@ -342,8 +345,9 @@ class MoELayer:
     bufs: dict
 
     @classmethod
-    def create(cls, T, H, I, E, k, w13_q, w13_s, w2_q, w2_s, block_m=16, swiglu_limit=0.0, device="cuda"):
-        desc = make_desc(T, H, I, E, k, block_m, swiglu_limit)
+    def create(cls, T, H, I, E, k, w13_q, w13_s, w2_q, w2_s, block_m=16, swiglu_limit=0.0, device="cuda",
+               flags=0):
+        desc = make_desc(T, H, I, E, k, block_m, swiglu_limit, flags)
         packed = prepack(desc, w13_q, w13_s, w2_q, w2_s)
         ws = torch.empty(max(workspace_bytes(desc), 1024), dtype=torch.uint8, device=device)
         cap = rows_capacity(T, E, k, block_m)

@@ -98,6 +98,11 @@ def test_entry_points_reject_bad_arguments_without_launching(lib):
     assert lib.moe_mxfp4_forward(ctypes.byref(d), fake, fake, fake, fake, fake, fake, fake, fake, 16, null) == 4
     assert lib.moe_mxfp4_forward(ctypes.byref(d), odd, fake, fake, fake, fake, fake, fake, fake, 1 << 40, null) == 3
     assert lib.moe_mxfp4_forward(ctypes.byref(d), null, fake, fake, fake, fake, fake, fake, fake, 1 << 40, null) == 1
+    bad_flags = moe.make_desc(4, 512, 256, 8, 2, 16, 0.0, 2)          # only MOE_FLAG_FAST_COMBINE is defined
+    assert lib.moe_mxfp4_forward(ctypes.byref(bad_flags), fake, fake, fake, fake, fake, fake, fake, fake, 1 << 40,
+                                 null) == 1
+    fast = moe.make_desc(4, 512, 256, 8, 2, 16, 0.0, moe.FLAG_FAST_COMBINE)
+    assert lib.moe_mxfp4_forward(ctypes.byref(fast), fake, fake, fake, fake, fake, fake, fake, fake, 16, null) == 4
     ws16 = ctypes.c_void_p(0x10010)        # 16-byte aligned, not 256: the forward workspace needs 256
     assert lib.moe_mxfp4_forward(ctypes.byref(d), fake, fake, fake, fake, fake, fake, fake, ws16, 1 << 40, null) == 3
     assert lib.moe_mxfp4_prepack(ctypes.byref(d), fake, fake, fake, fake, fake, 16, null) == 4

@@ -64,11 +64,11 @@ def test_decoder_bit_exact_all_codes_all_scales(gpu_lib):
     assert set(np.unique(w13_s).tolist()) == set(range(255))
 
 
-def _run_layer(moe, gpu_layers, L, block_m=16, swiglu_limit=0.0):
+def _run_layer(moe, gpu_layers, L, block_m=16, swiglu_limit=0.0, flags=0):
     x, logits = gpu_layers.inputs(L)
     packed = gpu_layers.packed(L)
     T, H, I, E, k = L["T"], L["H"], L["I"], L["E"], L["k"]
-    d = moe.make_desc(T, H, I, E, k, block_m, swiglu_limit)
+    d = moe.make_desc(T, H, I, E, k, block_m, swiglu_limit, flags)
     ids, w, _ = moe.route(logits, k)
     err = torch.zeros(4, dtype=torch.int32, device="cuda")
     perm = moe.permute(ids, E, block_m, error=err)
@@ -301,6 +301,43 @@ def test_forward_token_major_tiles(gpu_lib, gpu_layers, T, H, I, E, k, limit, bl
     assert np.isfinite(y).all()
     _compare(f"token-major {T}x{H}x{I} E{E} k{k} bm{block_m} L{limit}", y,
              oracle.forward(L, ids_r, w_r, swiglu_limit=limit))
+
+
+FAST_CASES = [("decode_t8_h4096_e256", None), ("tiny_t37_h512_e32", None),
+              ("prefill_t2048_h4096_e256", None), ("prefill_t8191_zipf_h4096_e256", None),
+              (None, (600, 384, 256, 32, 6)), (None, (1000, 256, 384, 5, 3))]
+
+
+@pytest.mark.parametrize("name,shape", FAST_CASES)
+def test_fast_combine_matches_oracle_and_default(gpu_lib, gpu_layers, name, shape):
+    """MOE_FLAG_FAST_COMBINE on every tile family: the decode shapes (up to 16 rows per expert) take
+    the atomic combine (W2 adds w * o into a zeroed y), the larger ones keep the slot-ordered
+    combine. Either way within the parity tolerance of the oracle and equal to the default path up
+    to fp32 rounding order (|diff| <= 1e-5 * max|y|). y starts as NaN, so every output must be
+    written."""
+    moe = gpu_lib
+    if name:
+        L = synth.make_config(name)
+    else:
+        T, H, I, E, k = shape
+        L = synth.make_layer(T=T, H=H, E=E, k=k, I=I, seed=T + H + 1)
+    det = _run_layer(moe, gpu_layers, L)["y"].clone()
+    x, logits = gpu_layers.inputs(L)
+    d = moe.make_desc(L["T"], L["H"], L["I"], L["E"], L["k"], 16, 0.0, moe.FLAG_FAST_COMBINE)
+    ids, w, _ = moe.route(logits, L["k"])
+    perm = moe.permute(ids, L["E"], 16)
+    ws = torch.empty(moe.workspace_bytes(d), dtype=torch.uint8, device="cuda")
+    y = torch.full((L["T"], L["H"]), float("nan"), dtype=torch.float32, device="cuda")
+    moe.forward(d, x, gpu_layers.packed(L), w, perm, ws, y)
+    torch.cuda.synchronize()
+    assert moe.read_device_error(ws[:4].view(torch.int32)) == 0
+    assert torch.isfinite(y).all()
+    diff = (y - det).abs().max().item()
+    assert diff <= 1e-5 * det.abs().max().item(), diff
+    ids_r, w_r, _ = oracle.route(L["logits"], L["k"])
+    tok, what = _compared_tokens(L, ids_r)
+    _compare(f"fast combine {name or shape}: {what or 'all tokens'}", y.cpu().numpy()[tok],
+             oracle.forward(L, ids_r, w_r, tokens=tok))
 
 
 def test_forward_deterministic(gpu_lib, gpu_layers):
