@@ -694,7 +694,10 @@ __device__ __forceinline__ void zero_y(float *y, int64_t n4)
 }
 
 // Gathered activations as NT_X MXFP8 terms: row r of the permutation gets
-// the terms of x[token(r)], padding rows (row_to_pair == -1) get zeros. One
+// the terms of x[token(r)]. Padding rows (row_to_pair == -1) are not written:
+// every GEMM row is computed from its own activation row only (MMA rows, the
+// 32-feature block maxima of h, the epilogue stores), and outputs of padding
+// rows are never stored, so their contents do not matter. One
 // thread per (row, 32-element block). Terms are E4M3 bytes
 // [H/128][NT_X][rows_cap][128] (slab-major: one TMA box fetches the slabs of a
 // stage for all rows and terms of a tile); scales are 32-bit words
@@ -749,8 +752,6 @@ __global__ void gather_quant_kernel(const uint16_t *__restrict__ x, const int32_
         const int e1 = mxfp8_block_exp(mx);
 #pragma unroll
         for (int t = 0; t < NT_X; ++t) {
-            // a padding row (or a bad entry, recorded above) is an all-zero block: zero term bytes and
-            // scale byte 0, what the conversion gives for zeros, written without converting
             uint32_t wq[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u}, sbyte = 0;
             if (real) {
 #pragma unroll
@@ -765,7 +766,7 @@ __global__ void gather_quant_kernel(const uint16_t *__restrict__ x, const int32_
             word |= __shfl_down_sync(0xFFFFFFFFu, sbyte, 1) << 8;
             word |= __shfl_down_sync(0xFFFFFFFFu, sbyte, 2) << 16;
             word |= __shfl_down_sync(0xFFFFFFFFu, sbyte, 3) << 24;
-            if (live) {
+            if (real) {
                 ptx::st_global_v8(xq + (((int64_t)(b >> 2) * NT_X + t) * rows_cap + r) * 128 + (b & 3) * 32, wq);
                 if ((b & 3) == 0)
                     *reinterpret_cast<uint32_t *>(xs + (((int64_t)(b >> 2) * NT_X + t) * rows_sf + r) * 4) = word;
@@ -776,40 +777,25 @@ __global__ void gather_quant_kernel(const uint16_t *__restrict__ x, const int32_
 
 // Gather in two passes for batches with many rows per expert, where the one-pass gather above would
 // convert every token's x k times (once per row). Pass 1, one warp per row: a real row records itself
-// in the inverse map p2r[pair] = row; a padding row gets its zero terms and scale words. Pass 2, one
+// in the inverse map p2r[pair] = row (padding rows are left as they are, see above). Pass 2, one
 // thread per (token, 32-element block) as above: the block's terms are computed once and stored to
 // each of the token's k rows. p2r lives in the fp32 staging region, which only the W2 GEMM writes
 // later; an entry is trusted only if row_to_pair sends its row back to the pair (a pair without a row,
 // i.e. with an expert id the permutation skipped, keeps whatever the region held).
 __global__ void gather_rows_kernel(const int32_t *__restrict__ row_to_pair, const int32_t *__restrict__ padded,
-                                   int E, int H, int64_t P, int64_t rows_cap, int64_t rows_sf,
-                                   uint8_t *__restrict__ xq, uint8_t *__restrict__ xs, int32_t *__restrict__ p2r,
-                                   int32_t *dev_error, float *y_zero, int64_t y_n4)
+                                   int E, int64_t P, int32_t *__restrict__ p2r, int32_t *dev_error, float *y_zero,
+                                   int64_t y_n4)
 {
     griddep_wait();                  // the permutation comes from an earlier kernel
     griddep_launch_dependents();
     zero_y(y_zero, y_n4);
     const int64_t R = __ldg(padded + E);
-    const int lane = threadIdx.x & 31;
-    const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
-    const int slabs = H / 128;
-    const uint32_t zero[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
-    for (int64_t r = blockIdx.x * (int64_t)(blockDim.x >> 5) + (threadIdx.x >> 5); r < R; r += warps) {
+    for (int64_t r = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; r < R; r += (int64_t)gridDim.x * blockDim.x) {
         const int32_t pr = __ldg(row_to_pair + r);
-        if (pr >= 0 && pr < P) {
-            if (lane == 0) p2r[pr] = (int32_t)r;
-            continue;
-        }
-        if (pr >= P && lane == 0) record_error(dev_error, DEV_ERR_ID_RANGE);
-        // zero terms: 4 lanes per 128-byte slab row, 8 slabs per pass of the warp
-        for (int i = lane; i < slabs * 4; i += 32) {
-            const int sl = i >> 2;
-#pragma unroll
-            for (int t = 0; t < NT_X; ++t) {
-                ptx::st_global_v8(xq + (((int64_t)sl * NT_X + t) * rows_cap + r) * 128 + (i & 3) * 32, zero);
-                if ((i & 3) == 0) *reinterpret_cast<uint32_t *>(xs + (((int64_t)sl * NT_X + t) * rows_sf + r) * 4) = 0u;
-            }
-        }
+        if (pr >= 0 && pr < P)
+            p2r[pr] = (int32_t)r;
+        else if (pr >= P)
+            record_error(dev_error, DEV_ERR_ID_RANGE);
     }
 }
 
@@ -978,10 +964,10 @@ cudaError_t launch_forward(const ForwardArgs &a, cudaStream_t s)
     const bool two_pass = a.regime == Regime::Mid || a.regime == Regime::Large || a.regime == Regime::Huge;
     if (two_pass) {
         int32_t *p2r = reinterpret_cast<int32_t *>(a.staging);     // P entries; W2 overwrites them later
-        int grid = (int)((a.rows_cap + 7) / 8);                      // 8 warps (rows) per block
+        int grid = (int)((a.rows_cap + 255) / 256);                  // a thread per row
         if (grid > 8 * 1024) grid = 8 * 1024;
-        err = launch_ex(gather_rows_kernel, dim3(grid), dim3(256), 0, s, pdl, a.row_to_pair, a.padded, a.E, a.H, P,
-                        a.rows_cap, a.rows_sf, a.xq, a.xs, p2r, a.dev_error, y_zero, y_n4);
+        err = launch_ex(gather_rows_kernel, dim3(grid), dim3(256), 0, s, pdl, a.row_to_pair, a.padded, a.E, P, p2r,
+                        a.dev_error, y_zero, y_n4);
         if (err != cudaSuccess) return err;
         const int64_t n = (int64_t)a.T * (a.H / 32);
         grid = (int)((n + 255) / 256);

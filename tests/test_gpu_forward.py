@@ -181,8 +181,9 @@ def test_forward_tiny_intermediates(gpu_lib, gpu_layers):
     ws = r["ws"]
     x = synth.bf16_bits_to_f64(L["x_bits"])
     r2p = r["perm"]["row_to_pair"].cpu().numpy()[:Rv]
-    xg = _terms(ws, lay["xq"], lay["xs"], 2, R, H)[:Rv]
-    want = np.where(r2p[:, None] >= 0, x[np.maximum(r2p, 0) // k], 0.0)
+    real = r2p >= 0                  # padding rows are not written (their outputs are never stored)
+    xg = _terms(ws, lay["xq"], lay["xs"], 2, R, H)[:Rv][real]
+    want = x[r2p[real] // k]
     # exact unless a 32-element block spans more than E4M3's range (then the smallest values keep
     # fewer bits): measured on these inputs about 2 in 10^4 elements, each off by < 1e-6 * max|x|
     assert np.mean(xg == want) > 0.999 and np.abs(xg - want).max() <= 1e-6 * np.abs(x).max()
@@ -194,7 +195,6 @@ def test_forward_tiny_intermediates(gpu_lib, gpu_layers):
     for row in range(Rv):
         p = r2p[row]
         if p < 0:
-            assert np.all(h_gpu[row] == 0), f"padding row {row} not zero"
             continue
         t, e = p // k, ids[p // k, p % k]
         q, s = L["w13_q"][e], L["w13_s"][e]
@@ -212,8 +212,8 @@ def test_forward_tiny_intermediates(gpu_lib, gpu_layers):
                                                  (700, 256, 256, 8, 2, 128)])   # 175: token-major tiles
 def test_gather_two_pass_terms(gpu_lib, gpu_layers, T, H, I, E, k, block_m):
     """Above 16 rows per expert on average the gather converts each token once and stores its terms
-    to all k of its rows (through an inverse of row_to_pair); padding rows get zero terms. Every
-    gathered row against the token's bf16 values."""
+    to all k of its rows (through an inverse of row_to_pair). Every real row against the token's
+    bf16 values (padding rows are not written)."""
     moe = gpu_lib
     L = synth.make_layer(T=T, H=H, E=E, k=k, I=I, seed=T * 3 + E)
     r = _run_layer(moe, gpu_layers, L, block_m)
@@ -223,9 +223,9 @@ def test_gather_two_pass_terms(gpu_lib, gpu_layers, T, H, I, E, k, block_m):
     x = synth.bf16_bits_to_f64(L["x_bits"])
     r2p = r["perm"]["row_to_pair"].cpu().numpy()[:Rv]
     assert (r2p < 0).any(), "the case should hold padding rows"
-    xg = _terms(r["ws"], lay["xq"], lay["xs"], 2, R, H)[:Rv]
-    want = np.where(r2p[:, None] >= 0, x[np.maximum(r2p, 0) // k], 0.0)
-    assert np.all(xg[r2p < 0] == 0)
+    real = r2p >= 0
+    xg = _terms(r["ws"], lay["xq"], lay["xs"], 2, R, H)[:Rv][real]
+    want = x[r2p[real] // k]
     assert np.mean(xg == want) > 0.999 and np.abs(xg - want).max() <= 1e-6 * np.abs(x).max()
 
 
