@@ -351,7 +351,7 @@ moe_status_t moe_mxfp4_forward_timed(const moe_layer_desc *d, const uint16_t *d_
     a.k = d->k;
     a.block_m = d->block_m;
     a.swiglu_limit = d->swiglu_limit;
-    a.fast_combine = false;      // set below, once the regime is known
+    a.fast_combine = (d->flags & MOE_FLAG_FAST_COMBINE) != 0;   // launch_forward decides where it applies
     a.rows_cap = R;
     a.rows_sf = scale_rows(d);
     a.x = d_x;
@@ -370,11 +370,6 @@ moe_status_t moe_mxfp4_forward_timed(const moe_layer_desc *d, const uint16_t *d_
     a.num_sms = sm_count();
     a.events = events;
     a.regime = pick_regime(d->T, d->k, d->E, d->H);
-    // The flag permits the atomic combine; it is used where it measured faster (up to 16 rows per
-    // expert on average). Larger batches keep the slot-ordered combine: their W2 epilogues would
-    // issue T*k*H reductions, which cost more in L2 than the per-pair rows' round trip.
-    a.fast_combine = (d->flags & MOE_FLAG_FAST_COMBINE) != 0 &&
-                     (a.regime == Regime::Tiny || a.regime == Regime::Small);
     const uint32_t sps = (uint32_t)regime_sps(a.regime);
     const uint8_t *w13 = a.packed, *w2 = a.packed + packed_w13_bytes(d->E, d->H, d->I);
     const uint64_t rows13 = (uint64_t)d->E * 2 * d->I * (d->H / KSLAB);   // 128-element rows of W13 nibbles

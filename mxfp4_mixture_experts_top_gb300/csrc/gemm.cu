@@ -155,7 +155,10 @@ struct Smem {
 
 
 
-template <class C>
+// FAST (W2 of the decode tiles only): the epilogue adds w * o into y with reduction atomics instead of
+// writing the per-pair rows (MOE_FLAG_FAST_COMBINE); a separate instantiation, so the default kernels
+// carry no code of it.
+template <class C, bool FAST = false>
 __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_kernel(const __grid_constant__ GemmParams p)
 {
     constexpr int MODE = C::MODE, NMAX = C::NMAX, NT = C::NT, SPS = C::SPS, NP = C::NP;
@@ -645,7 +648,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_kernel(const __grid_co
                 } else if (ok) {
                     const int c = tl.mb * TILE_ROWS + warp * 32 + lane;
                     const int my_pair = (lane < 16) ? __ldg(p.row_to_pair + tl.row0 + c0 + lane) : -1;
-                    if (p.y) {
+                    if constexpr (FAST) {
                         // fast combine: w * o added into the token's row of y; lane j < 16 holds row j's weight
                         const float my_w = (my_pair >= 0 && my_pair < p.P) ? __ldg(p.topk_w + my_pair) : 0.f;
 #pragma unroll
@@ -892,7 +895,7 @@ __global__ void combine_kernel(const float *__restrict__ staging, const float *_
     }
 }
 
-template <class C>
+template <class C, bool FAST = false>
 cudaError_t launch_gemm(const GemmParams &p, int grid, cudaStream_t s, bool pdl)
 {
     static unsigned long long attr_set = 0;   // bit d: attribute set on device d
@@ -900,12 +903,12 @@ cudaError_t launch_gemm(const GemmParams &p, int grid, cudaStream_t s, bool pdl)
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 64 || !((attr_set >> dev) & 1ull)) {
-        cudaError_t e = cudaFuncSetAttribute(moe_gemm_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaError_t e = cudaFuncSetAttribute(moe_gemm_kernel<C, FAST>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)Smem<C>::bytes(C::EMAX));
         if (e != cudaSuccess) return e;
         if (dev < 64) __atomic_fetch_or(&attr_set, 1ull << dev, __ATOMIC_RELAXED);
     }
-    return launch_ex(moe_gemm_kernel<C>, dim3(grid), dim3(C::THREADS), smem, s, pdl, p);
+    return launch_ex(moe_gemm_kernel<C, FAST>, dim3(grid), dim3(C::THREADS), smem, s, pdl, p);
 }
 
 }  // namespace
@@ -959,7 +962,12 @@ cudaError_t launch_forward(const ForwardArgs &a, cudaStream_t s)
     for (int i = 0; i < 5 && a.events; ++i)
         if (a.events[i]) pdl = false;
     mark(a, 0, s);
-    float *y_zero = a.fast_combine ? a.y : nullptr;
+    // The flag permits the atomic combine; it is taken where it measured faster, up to 16 rows per
+    // expert on average (the weight-major decode tiles). Larger batches keep the slot-ordered combine:
+    // their W2 epilogues would issue T*k*H reductions, which cost the L2 more than the per-pair rows'
+    // round trip.
+    const bool fast = a.fast_combine && (a.regime == Regime::Tiny || a.regime == Regime::Small);
+    float *y_zero = fast ? a.y : nullptr;
     const int64_t y_n4 = (int64_t)a.T * a.H / 4;
     const bool two_pass = a.regime == Regime::Mid || a.regime == Regime::Large || a.regime == Regime::Huge;
     if (two_pass) {
@@ -1026,7 +1034,7 @@ cudaError_t launch_forward(const ForwardArgs &a, cudaStream_t s)
     mark(a, 2, s);
 
     // W2: K = I, 128 output features per weight tile
-    g.y = a.fast_combine ? a.y : nullptr;
+    g.y = fast ? a.y : nullptr;
     g.tm_a = a.tmap_w2;
     g.tm_a1 = a.tmap_w2_1;
     g.tm_b = a.tmap_hq;
@@ -1037,15 +1045,18 @@ cudaError_t launch_forward(const ForwardArgs &a, cudaStream_t s)
     g.K = a.I;
     g.MB = a.H / TILE_ROWS;
     err = rg == Regime::Huge  ? launch_gemm_rows(g, 1, a.num_sms, s, pdl)
-        : rg == Regime::Tiny  ? (a.E <= W2Tiny::EMAX ? launch_gemm<W2Tiny>(g, a.num_sms, s, pdl)
-                                                     : launch_gemm<W2TinyWideE>(g, a.num_sms, s, pdl))
-        : rg == Regime::Small ? launch_gemm<W2Small>(g, a.num_sms, s, pdl)
+        : rg == Regime::Tiny  ? (a.E <= W2Tiny::EMAX ? (fast ? launch_gemm<W2Tiny, true>(g, a.num_sms, s, pdl)
+                                                          : launch_gemm<W2Tiny>(g, a.num_sms, s, pdl))
+                                                     : (fast ? launch_gemm<W2TinyWideE, true>(g, a.num_sms, s, pdl)
+                                                          : launch_gemm<W2TinyWideE>(g, a.num_sms, s, pdl)))
+        : rg == Regime::Small ? (fast ? launch_gemm<W2Small, true>(g, a.num_sms, s, pdl)
+                                      : launch_gemm<W2Small>(g, a.num_sms, s, pdl))
         : rg == Regime::Mid   ? launch_gemm<W2Mid>(g, a.num_sms, s, pdl)
                               : (a.E <= W2Large::EMAX ? launch_gemm<W2Large>(g, a.num_sms, s, pdl)
                                                       : launch_gemm<W2LargeWideE>(g, a.num_sms, s, pdl));
     if (err != cudaSuccess) return err;
     mark(a, 3, s);
-    if (!a.fast_combine) {           // the fast combine has already added every pair into y
+    if (!fast) {                     // the fast combine has already added every pair into y
         const int64_t n = (int64_t)a.T * (a.H / 4);
         int grid = (int)((n + 255) / 256);
         if (grid > 4 * 1024) grid = 4 * 1024;
@@ -1055,7 +1066,7 @@ cudaError_t launch_forward(const ForwardArgs &a, cudaStream_t s)
         if (err != cudaSuccess) return err;
     }
     mark(a, 4, s);
-    note_launch((two_pass ? 5 : 4) - (a.fast_combine ? 1 : 0));
+    note_launch((two_pass ? 5 : 4) - (fast ? 1 : 0));
     return cudaSuccess;
 }
 

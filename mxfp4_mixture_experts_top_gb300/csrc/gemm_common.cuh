@@ -27,7 +27,7 @@ struct GemmParams {
     uint8_t *hq;              // W13 out: h terms [I/128][NTO][rows_cap][128]
     uint8_t *hs;              // W13 out: h term scale words [I/128][NTO][rows_sf], byte = K-block % 4
     float *staging;           // W2 out [P, H]
-    float *y;                 // fast combine: W2 adds w[pair] * o into y[pair / k] (nullptr: staging)
+    float *y;                 // fast combine (weight-major W2 only): adds w[pair] * o into y[pair / k]; nullptr: staging
     const float *topk_w;      // [T, k], with y
     int32_t *dev_error;
 };

@@ -370,14 +370,12 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_rows_kernel(const __gr
             const bool row_ok = trow < tl.n;
             const int64_t row = (int64_t)tl.row0 + trow;
             int pair = -1;
-            float wpair = 0.f;                              // fast combine: the pair's routing weight
             if (MODE == 1 && row_ok) {
                 pair = __ldg(p.row_to_pair + row);
                 if (pair >= p.P) {
                     record_error(p.dev_error, DEV_ERR_ID_RANGE);
                     pair = -1;
                 }
-                if (pair >= 0 && p.y) wpair = __ldg(p.topk_w + pair);
             }
             uint32_t sbytes[NT] = {0u, 0u};                 // W13: this warp's two scale bytes per term
             for (int ch = 0; ch < 2; ++ch) {
@@ -431,18 +429,6 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_rows_kernel(const __gr
                         ptx::st_global_v8(p.hq + (((int64_t)tl.mb * NT + t) * p.rows_cap + row) * 128 + blk * 32, w);
                         sbytes[t] |= sb << (8 * ch);
                     }
-                } else if (pair >= 0 && p.y) {
-                    // fast combine: w * o added into the token's row of y, 16 bytes per reduction
-                    float *dst = p.y + (int64_t)(pair / p.k) * p.H + (int64_t)tl.mb * C::TN + c0;
-#pragma unroll
-                    for (int z = 0; z < 8; ++z)
-                        ptx::red_add_v4_f32(dst + 4 * z, wpair * __uint_as_float(a0[4 * z]), wpair * __uint_as_float(a0[4 * z + 1]),
-                                            wpair * __uint_as_float(a0[4 * z + 2]), wpair * __uint_as_float(a0[4 * z + 3]));
-#pragma unroll
-                    for (int z = 0; z < 8; ++z)
-                        ptx::red_add_v4_f32(dst + 32 + 4 * z, wpair * __uint_as_float(a1[4 * z]),
-                                            wpair * __uint_as_float(a1[4 * z + 1]), wpair * __uint_as_float(a1[4 * z + 2]),
-                                            wpair * __uint_as_float(a1[4 * z + 3]));
                 } else if (pair >= 0) {
                     // 256 contiguous bytes of the pair's staging row per chunk, in 32-byte stores (the
                     // combine reads them back once, after the whole launch)

@@ -88,7 +88,7 @@ size_t packed_w2_bytes(int E, int H, int I);
 struct ForwardArgs {
     int T, H, I, E, k, block_m;
     float swiglu_limit;
-    bool fast_combine;           // W2 adds w * o into y with reduction atomics (y zeroed by the gather)
+    bool fast_combine;           // MOE_FLAG_FAST_COMBINE given: the decode tiles' W2 adds w * o into y
     int64_t rows_cap, rows_sf;   // permutation rows; rows of the scale-word arrays (a multiple of 4)
     const uint16_t *x;
     const uint8_t *packed;

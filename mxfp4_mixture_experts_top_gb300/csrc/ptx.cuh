@@ -180,12 +180,6 @@ __device__ __forceinline__ void red_add_f32(float *p, float v)
     asm volatile("red.global.add.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
 }
 
-// Four consecutive fp32 adds in one reduction (p 16-byte aligned; sm_90 and later).
-__device__ __forceinline__ void red_add_v4_f32(float *p, float a, float b, float c, float d)
-{
-    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
-}
-
 // ----------------------------------------------------------------- tcgen05
 // Allocate `ncols` TMEM columns (power of two >= 32); whole warp executes.
 // The TMEM base address is written to shared memory at `dst`.

@@ -289,7 +289,9 @@ def test_forward_fuzz_shapes(gpu_lib, gpu_layers, T, H, I, E, k):
 @pytest.mark.parametrize("block_m", [16, 128])
 @pytest.mark.parametrize("T,H,I,E,k,limit", [(1200, 512, 256, 16, 4, 0.0),   # 300 rows per expert: 3 token blocks
                                              (1000, 256, 384, 5, 3, 10.0),   # 600 rows per expert, clamp, I/128 odd
-                                             (520, 768, 128, 2, 1, 0.0)])    # 260 rows per expert, three W2 blocks
+                                             (520, 768, 128, 2, 1, 0.0),     # 260 rows per expert, three W2 blocks
+                                             (300, 256, 128, 1, 1, 0.0),     # one expert, k = 1
+                                             (11000, 256, 128, 1024, 6, 0.0)])  # 1,024 experts, 64.5 rows each
 def test_forward_token_major_tiles(gpu_lib, gpu_layers, T, H, I, E, k, limit, block_m):
     """More than 64 rows per expert on average selects the token-major tiles (128 token rows x 256
     weight rows, terms summed by the tensor core): every output against the oracle, with small and
