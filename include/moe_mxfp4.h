@@ -51,7 +51,7 @@
 extern "C" {
 #endif
 
-#define MOE_ABI_VERSION 3
+#define MOE_ABI_VERSION 4
 
 /* Size of the static scratch array behind moe_mxfp4_forward_noalloc. */
 #define MOE_NOALLOC_SCRATCH_BYTES (32u << 20)
@@ -73,6 +73,8 @@ typedef enum {
  *   the permutation (16, 32, 64 or 128).
  *   swiglu_limit > 0 enables the clamp gate = min(gate, L),
  *   up = clamp(up, -L, L) before SiLU(gate) * up; <= 0 disables it.
+ *   out_dtype: MOE_OUT_F32 (y fp32, the default) or MOE_OUT_BF16 (y as bf16
+ *   bits: the fp32 sum of the slot-ordered combine rounded to nearest even).
  *   flags: 0 or MOE_FLAG_FAST_COMBINE.
  * Supported: 1 <= k <= min(E, 32), E <= 1024, H and I multiples of 128. */
 
@@ -87,12 +89,16 @@ typedef enum {
  * sum order depends on the order the GPU retires the adds: results match the
  * default path up to fp32 rounding (a few ulp of y) and are not
  * bit-reproducible from run to run. The default (flags 0) is always the
- * deterministic slot-ordered combine.
+ * deterministic slot-ordered combine, and so is MOE_OUT_BF16 output.
  */
 #define MOE_FLAG_FAST_COMBINE 1u
+
+typedef enum { MOE_OUT_F32 = 0, MOE_OUT_BF16 = 1 } moe_out_dtype_t;
+
 typedef struct moe_layer_desc {
     int T, H, I, E, k, block_m;
     float swiglu_limit;
+    int out_dtype;        /* moe_out_dtype_t */
     unsigned flags;
 } moe_layer_desc;
 
@@ -223,7 +229,8 @@ size_t moe_mxfp4_workspace_bytes(const moe_layer_desc *desc);
  *   d_topk_w         fp32 [T, k] (from moe_route).
  *   d_offsets, d_padded_offsets, d_row_to_pair   from moe_permute.
  * Output:
- *   d_y              fp32 [T, H], fully overwritten.
+ *   d_y              fp32 [T, H] (out_dtype MOE_OUT_F32) or bf16 bits [T, H]
+ *                    (MOE_OUT_BF16), fully overwritten.
  * d_workspace: moe_mxfp4_workspace_bytes(desc) bytes, 256-byte aligned
  * (MOE_ERR_MISALIGNED otherwise), contents need not be initialised; the call
  * resets its device error word.
@@ -232,15 +239,18 @@ size_t moe_mxfp4_workspace_bytes(const moe_layer_desc *desc);
  * of MXFP8 terms (E4M3 values, one E8M0 scale per 32 K-elements, term scales
  * 2^-4 apart): x in 2 terms (exact for bf16 unless a 32-element block spans
  * more than 2^17), SiLU(gate)*up in 2 terms (about 8 significant bits, a bf16 h);
- * fp32 accumulation; output fp32. Result within 2e-2 * rms of the float64
- * oracle (measured errors are up to about 4e-3 * rms).
- * Launches 4 kernels on `stream`; deterministic (bit-identical reruns). The
- * GEMMs stream their weights before the kernel ahead of them has finished.
+ * fp32 accumulation; output fp32 (or its bf16 rounding). Result within
+ * 2e-2 * rms of the float64 oracle (measured errors are up to about
+ * 4e-3 * rms; bf16 output adds its rounding, at most 2^-9 |y|).
+ * Launches 4 or 5 kernels on `stream` (one fewer with the atomic combine);
+ * deterministic (bit-identical reruns) unless MOE_FLAG_FAST_COMBINE takes the
+ * atomic combine. The GEMMs stream their weights before the kernel ahead of
+ * them has finished.
  */
 moe_status_t moe_mxfp4_forward(const moe_layer_desc *desc, const uint16_t *d_x,
                                const void *d_packed, const float *d_topk_w,
                                const int32_t *d_offsets, const int32_t *d_padded_offsets,
-                               const int32_t *d_row_to_pair, float *d_y,
+                               const int32_t *d_row_to_pair, void *d_y,
                                void *d_workspace, size_t workspace_bytes, void *stream);
 
 /*
@@ -254,7 +264,7 @@ moe_status_t moe_mxfp4_forward(const moe_layer_desc *desc, const uint16_t *d_x,
 moe_status_t moe_mxfp4_forward_timed(const moe_layer_desc *desc, const uint16_t *d_x,
                                      const void *d_packed, const float *d_topk_w,
                                      const int32_t *d_offsets, const int32_t *d_padded_offsets,
-                                     const int32_t *d_row_to_pair, float *d_y,
+                                     const int32_t *d_row_to_pair, void *d_y,
                                      void *d_workspace, size_t workspace_bytes,
                                      void *const *events, void *stream);
 
@@ -295,7 +305,7 @@ moe_status_t moe_mxfp4_workspace_layout(const moe_layer_desc *desc, size_t out[7
 moe_status_t moe_mxfp4_forward_noalloc(const moe_layer_desc *desc, const uint16_t *d_x,
                                        const void *d_packed, const float *d_topk_w,
                                        const int32_t *d_offsets, const int32_t *d_padded_offsets,
-                                       const int32_t *d_row_to_pair, float *d_y, void *stream);
+                                       const int32_t *d_row_to_pair, void *d_y, void *stream);
 
 /*
  * Read and clear the device error word of moe_mxfp4_forward_noalloc on the

@@ -130,6 +130,7 @@ moe_status_t check_desc(const moe_layer_desc *d)
     if (!d) return MOE_ERR_INVALID_ARG;
     if (d->T < 0 || d->H <= 0 || d->I <= 0 || d->E <= 0 || d->k <= 0 || d->k > d->E) return MOE_ERR_INVALID_ARG;
     if (d->flags & ~MOE_FLAG_FAST_COMBINE) return MOE_ERR_INVALID_ARG;
+    if (d->out_dtype != MOE_OUT_F32 && d->out_dtype != MOE_OUT_BF16) return MOE_ERR_INVALID_ARG;
     if (d->E > 1024 || d->k > 32) return MOE_ERR_UNSUPPORTED;
     if (d->H % 128 || d->I % 128) return MOE_ERR_UNSUPPORTED;
     if (d->block_m != 16 && d->block_m != 32 && d->block_m != 64 && d->block_m != 128) return MOE_ERR_UNSUPPORTED;
@@ -325,7 +326,7 @@ moe_status_t moe_mxfp4_workspace_layout(const moe_layer_desc *d, size_t out[7])
 
 moe_status_t moe_mxfp4_forward_timed(const moe_layer_desc *d, const uint16_t *d_x, const void *d_packed,
                                      const float *d_topk_w, const int32_t *d_offsets,
-                                     const int32_t *d_padded_offsets, const int32_t *d_row_to_pair, float *d_y,
+                                     const int32_t *d_padded_offsets, const int32_t *d_row_to_pair, void *d_y,
                                      void *d_workspace, size_t workspace_bytes, void *const *events, void *stream)
 {
     moe_status_t st = check_desc(d);
@@ -361,6 +362,7 @@ moe_status_t moe_mxfp4_forward_timed(const moe_layer_desc *d, const uint16_t *d_
     a.padded = d_padded_offsets;
     a.row_to_pair = d_row_to_pair;
     a.y = d_y;
+    a.y_bf16 = d->out_dtype == MOE_OUT_BF16;
     a.dev_error = reinterpret_cast<int32_t *>(ws + L.err);
     a.xq = ws + L.xq;
     a.xs = ws + L.xs;
@@ -397,7 +399,7 @@ moe_status_t moe_mxfp4_forward_timed(const moe_layer_desc *d, const uint16_t *d_
 
 moe_status_t moe_mxfp4_forward(const moe_layer_desc *d, const uint16_t *d_x, const void *d_packed,
                                const float *d_topk_w, const int32_t *d_offsets, const int32_t *d_padded_offsets,
-                               const int32_t *d_row_to_pair, float *d_y, void *d_workspace, size_t workspace_bytes,
+                               const int32_t *d_row_to_pair, void *d_y, void *d_workspace, size_t workspace_bytes,
                                void *stream)
 {
     return moe_mxfp4_forward_timed(d, d_x, d_packed, d_topk_w, d_offsets, d_padded_offsets, d_row_to_pair, d_y,

@@ -872,9 +872,11 @@ __global__ void gather_tokens_kernel(const uint16_t *__restrict__ x, const int32
     }
 }
 
-// y[t, c] = sum_j w[t, j] * staging[t*k + j, c], slots in ascending order.
+// y[t, c] = sum_j w[t, j] * staging[t*k + j, c], slots in ascending order, in fp32; BF16: y is stored as
+// bf16 bits, the fp32 sum rounded to nearest even.
+template <bool BF16>
 __global__ void combine_kernel(const float *__restrict__ staging, const float *__restrict__ w, int T, int H,
-                               int k, float *__restrict__ y)
+                               int k, void *__restrict__ y)
 {
     griddep_wait();                  // staging comes from the W2 GEMM
     const int vec = H / 4;
@@ -891,7 +893,15 @@ __global__ void combine_kernel(const float *__restrict__ staging, const float *_
             acc.z = fmaf(wj, s.z, acc.z);
             acc.w = fmaf(wj, s.w, acc.w);
         }
-        reinterpret_cast<float4 *>(y + t * H)[c4] = acc;
+        if (BF16) {
+            const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y), hi = __floats2bfloat162_rn(acc.z, acc.w);
+            uint2 v;
+            v.x = *reinterpret_cast<const uint32_t *>(&lo);
+            v.y = *reinterpret_cast<const uint32_t *>(&hi);
+            reinterpret_cast<uint2 *>(static_cast<uint16_t *>(y) + t * H)[c4] = v;
+        } else {
+            reinterpret_cast<float4 *>(static_cast<float *>(y) + t * H)[c4] = acc;
+        }
     }
 }
 
@@ -966,8 +976,8 @@ cudaError_t launch_forward(const ForwardArgs &a, cudaStream_t s)
     // expert on average (the weight-major decode tiles). Larger batches keep the slot-ordered combine:
     // their W2 epilogues would issue T*k*H reductions, which cost the L2 more than the per-pair rows'
     // round trip.
-    const bool fast = a.fast_combine && (a.regime == Regime::Tiny || a.regime == Regime::Small);
-    float *y_zero = fast ? a.y : nullptr;
+    const bool fast = a.fast_combine && !a.y_bf16 && (a.regime == Regime::Tiny || a.regime == Regime::Small);
+    float *y_zero = fast ? static_cast<float *>(a.y) : nullptr;
     const int64_t y_n4 = (int64_t)a.T * a.H / 4;
     const bool two_pass = a.regime == Regime::Mid || a.regime == Regime::Large || a.regime == Regime::Huge;
     if (two_pass) {
@@ -1034,7 +1044,7 @@ cudaError_t launch_forward(const ForwardArgs &a, cudaStream_t s)
     mark(a, 2, s);
 
     // W2: K = I, 128 output features per weight tile
-    g.y = fast ? a.y : nullptr;
+    g.y = fast ? static_cast<float *>(a.y) : nullptr;
     g.tm_a = a.tmap_w2;
     g.tm_a1 = a.tmap_w2_1;
     g.tm_b = a.tmap_hq;
@@ -1061,8 +1071,10 @@ cudaError_t launch_forward(const ForwardArgs &a, cudaStream_t s)
         int grid = (int)((n + 255) / 256);
         if (grid > 4 * 1024) grid = 4 * 1024;
         if (grid < 1) grid = 1;
-        err = launch_ex(combine_kernel, dim3(grid), dim3(256), 0, s, pdl, (const float *)a.staging, a.topk_w, a.T,
-                        a.H, a.k, a.y);
+        err = a.y_bf16 ? launch_ex(combine_kernel<true>, dim3(grid), dim3(256), 0, s, pdl, (const float *)a.staging,
+                                   a.topk_w, a.T, a.H, a.k, a.y)
+                       : launch_ex(combine_kernel<false>, dim3(grid), dim3(256), 0, s, pdl, (const float *)a.staging,
+                                   a.topk_w, a.T, a.H, a.k, a.y);
         if (err != cudaSuccess) return err;
     }
     mark(a, 4, s);

@@ -94,7 +94,8 @@ struct ForwardArgs {
     const uint8_t *packed;
     const float *topk_w;
     const int32_t *offsets, *padded, *row_to_pair;
-    float *y;
+    void *y;                     // fp32 [T, H], or bf16 bits with y_bf16
+    bool y_bf16;
     int32_t *dev_error;
     uint8_t *xq, *xs;      // x terms [H/128][NT_X][rows_cap][128], scale words [H/128][NT_X][rows_sf]
     uint8_t *hq, *hs;      // h terms [I/128][nt_h][rows_cap][128], scale words [I/128][nt_h][rows_sf]

@@ -50,7 +50,7 @@ moe_status_t scratch_on_current_device(void **out)
 extern "C" moe_status_t moe_mxfp4_forward_noalloc(const moe_layer_desc *desc, const uint16_t *d_x,
                                                   const void *d_packed, const float *d_topk_w,
                                                   const int32_t *d_offsets, const int32_t *d_padded_offsets,
-                                                  const int32_t *d_row_to_pair, float *d_y, void *stream)
+                                                  const int32_t *d_row_to_pair, void *d_y, void *stream)
 {
     size_t layout[7];
     const moe_status_t valid = moe_mxfp4_workspace_layout(desc, layout);   // same checks as the forward

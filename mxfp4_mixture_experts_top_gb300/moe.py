@@ -38,7 +38,7 @@ class MoeError(RuntimeError):
 class LayerDesc(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int), ("H", ctypes.c_int), ("I", ctypes.c_int), ("E", ctypes.c_int),
                 ("k", ctypes.c_int), ("block_m", ctypes.c_int), ("swiglu_limit", ctypes.c_float),
-                ("flags", ctypes.c_uint)]
+                ("out_dtype", ctypes.c_int), ("flags", ctypes.c_uint)]
 
 
 _lib = None
@@ -185,10 +185,11 @@ def route_permute(logits: torch.Tensor, k: int, block_m: int, out=None, perm_out
 
 
 FLAG_FAST_COMBINE = 1   # MOE_FLAG_FAST_COMBINE
+OUT_F32, OUT_BF16 = 0, 1  # moe_out_dtype_t
 
 
-def make_desc(T, H, I, E, k, block_m=16, swiglu_limit=0.0, flags=0) -> LayerDesc:
-    return LayerDesc(T, H, I, E, k, block_m, float(swiglu_limit), int(flags))
+def make_desc(T, H, I, E, k, block_m=16, swiglu_limit=0.0, flags=0, out_dtype=OUT_F32) -> LayerDesc:
+    return LayerDesc(T, H, I, E, k, block_m, float(swiglu_limit), int(out_dtype), int(flags))
 
 
 def packed_bytes(desc: LayerDesc) -> int:
@@ -229,8 +230,10 @@ def forward(desc: LayerDesc, x: torch.Tensor, packed: torch.Tensor, topk_w: torc
             workspace: torch.Tensor, y: torch.Tensor = None, stream=None) -> torch.Tensor:
     """moe_mxfp4_forward: y fp32 [T, H]."""
     _cuda(x, torch.bfloat16, "x")
+    ydt = torch.bfloat16 if desc.out_dtype == OUT_BF16 else torch.float32
     if y is None:
-        y = torch.empty((desc.T, desc.H), dtype=torch.float32, device=x.device)
+        y = torch.empty((desc.T, desc.H), dtype=ydt, device=x.device)
+    _cuda(y, ydt, "y")
     _check(load().moe_mxfp4_forward(ctypes.byref(desc), _ptr(x), _ptr(packed), _ptr(topk_w), _ptr(perm["offsets"]),
                                     _ptr(perm["padded_offsets"]), _ptr(perm["row_to_pair"]), _ptr(y),
                                     _ptr(workspace), workspace.numel() * workspace.element_size(),
@@ -246,8 +249,10 @@ def forward_noalloc(desc: LayerDesc, x: torch.Tensor, packed: torch.Tensor, topk
     """moe_mxfp4_forward_noalloc: the forward with the library's static scratch array as its
     workspace, for callers that cannot allocate device memory (y must be passed in then)."""
     _cuda(x, torch.bfloat16, "x")
+    ydt = torch.bfloat16 if desc.out_dtype == OUT_BF16 else torch.float32
     if y is None:
-        y = torch.empty((desc.T, desc.H), dtype=torch.float32, device=x.device)
+        y = torch.empty((desc.T, desc.H), dtype=ydt, device=x.device)
+    _cuda(y, ydt, "y")
     _check(load().moe_mxfp4_forward_noalloc(ctypes.byref(desc), _ptr(x), _ptr(packed), _ptr(topk_w),
                                             _ptr(perm["offsets"]), _ptr(perm["padded_offsets"]),
                                             _ptr(perm["row_to_pair"]), _ptr(y), _stream(stream)),
@@ -346,8 +351,8 @@ class MoELayer:
 
     @classmethod
     def create(cls, T, H, I, E, k, w13_q, w13_s, w2_q, w2_s, block_m=16, swiglu_limit=0.0, device="cuda",
-               flags=0):
-        desc = make_desc(T, H, I, E, k, block_m, swiglu_limit, flags)
+               flags=0, out_dtype=OUT_F32):
+        desc = make_desc(T, H, I, E, k, block_m, swiglu_limit, flags, out_dtype)
         packed = prepack(desc, w13_q, w13_s, w2_q, w2_s)
         ws = torch.empty(max(workspace_bytes(desc), 1024), dtype=torch.uint8, device=device)
         cap = rows_capacity(T, E, k, block_m)
@@ -361,7 +366,8 @@ class MoELayer:
                               row_to_pair=torch.empty(max(cap, 1), dtype=torch.int32, device=dev),
                               pair_to_row=torch.empty(max(T * k, 1), dtype=torch.int32, device=dev)),
                     perm_err=torch.zeros(4, dtype=torch.int32, device=dev),
-                    y=torch.empty((T, H), dtype=torch.float32, device=dev))
+                    y=torch.empty((T, H), dtype=torch.bfloat16 if out_dtype == OUT_BF16 else torch.float32,
+                                  device=dev))
         return cls(desc, packed, ws, bufs)
 
     def __call__(self, x: torch.Tensor, logits: torch.Tensor, stream=None) -> torch.Tensor:

@@ -35,7 +35,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert moe.abi_version() == 3
+    assert moe.abi_version() == 4
     for s in range(8):
         assert lib.moe_status_string(s)
     assert b"unknown" in lib.moe_status_string(99)
@@ -98,6 +98,12 @@ def test_entry_points_reject_bad_arguments_without_launching(lib):
     assert lib.moe_mxfp4_forward(ctypes.byref(d), fake, fake, fake, fake, fake, fake, fake, fake, 16, null) == 4
     assert lib.moe_mxfp4_forward(ctypes.byref(d), odd, fake, fake, fake, fake, fake, fake, fake, 1 << 40, null) == 3
     assert lib.moe_mxfp4_forward(ctypes.byref(d), null, fake, fake, fake, fake, fake, fake, fake, 1 << 40, null) == 1
+    bad_out = moe.make_desc(4, 512, 256, 8, 2, 16, 0.0, 0, 2)         # out_dtype is MOE_OUT_F32 or MOE_OUT_BF16
+    assert lib.moe_mxfp4_forward(ctypes.byref(bad_out), fake, fake, fake, fake, fake, fake, fake, fake, 1 << 40,
+                                 null) == 1
+    bf16_out = moe.make_desc(4, 512, 256, 8, 2, 16, 0.0, 0, moe.OUT_BF16)
+    assert lib.moe_mxfp4_forward(ctypes.byref(bf16_out), fake, fake, fake, fake, fake, fake, fake, fake, 16,
+                                 null) == 4
     bad_flags = moe.make_desc(4, 512, 256, 8, 2, 16, 0.0, 2)          # only MOE_FLAG_FAST_COMBINE is defined
     assert lib.moe_mxfp4_forward(ctypes.byref(bad_flags), fake, fake, fake, fake, fake, fake, fake, fake, 1 << 40,
                                  null) == 1

@@ -342,6 +342,25 @@ def test_fast_combine_matches_oracle_and_default(gpu_lib, gpu_layers, name, shap
              oracle.forward(L, ids_r, w_r, tokens=tok))
 
 
+@pytest.mark.parametrize("name", ["decode_t8_h4096_e256", "tiny_t37_h512_e32", "prefill_t8191_zipf_h4096_e256"])
+def test_bf16_output_is_the_rounded_fp32_output(gpu_lib, gpu_layers, name):
+    """out_dtype MOE_OUT_BF16: y is the fp32 result of the same slot-ordered combine rounded to
+    nearest even, bit for bit (also with MOE_FLAG_FAST_COMBINE, which bf16 output does not take)."""
+    moe = gpu_lib
+    L = synth.make_config(name)
+    ref = _run_layer(moe, gpu_layers, L)["y"]
+    x, logits = gpu_layers.inputs(L)
+    ids, w, _ = moe.route(logits, L["k"])
+    perm = moe.permute(ids, L["E"], 16)
+    for flags in (0, moe.FLAG_FAST_COMBINE):
+        d = moe.make_desc(L["T"], L["H"], L["I"], L["E"], L["k"], 16, 0.0, flags, moe.OUT_BF16)
+        ws = torch.empty(moe.workspace_bytes(d), dtype=torch.uint8, device="cuda")
+        y = moe.forward(d, x, gpu_layers.packed(L), w, perm, ws)
+        torch.cuda.synchronize()
+        assert y.dtype == torch.bfloat16 and moe.read_device_error(ws[:4].view(torch.int32)) == 0
+        assert torch.equal(y, ref.to(torch.bfloat16)), f"flags {flags}"
+
+
 def test_forward_deterministic(gpu_lib, gpu_layers):
     L = synth.make_config("decode_t512_h4096_e256")
     a = _run_layer(gpu_lib, gpu_layers, L)["y"].clone()
