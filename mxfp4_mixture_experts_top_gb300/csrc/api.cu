@@ -393,7 +393,8 @@ moe_status_t moe_mxfp4_forward_timed(const moe_layer_desc *d, const uint16_t *d_
     if (!get_map(&a.tmap_xs1, 2, a.xs, (uint64_t)a.rows_sf, NT_X, s13, n13, 1, &st)) return st;
     if (!get_map(&a.tmap_hs, 2, a.hs, (uint64_t)a.rows_sf, NT_H, s2, n2, sps, &st)) return st;
     if (!get_map(&a.tmap_hs1, 2, a.hs, (uint64_t)a.rows_sf, NT_H, s2, n2, 1, &st)) return st;
-    if (cudaMemsetAsync(a.dev_error, 0, sizeof(int32_t), s) != cudaSuccess) return MOE_ERR_CUDA;
+    // the first kernel of the forward clears the device error word (a memset here would break the
+    // programmatic-dependent-launch chain between the permutation and the gather)
     return from_cuda(launch_forward(a, s));
 }
 

@@ -716,6 +716,9 @@ __global__ void gather_quant_kernel(const uint16_t *__restrict__ x, const int32_
                                     int64_t rows_cap, int64_t rows_sf, uint8_t *__restrict__ xq,
                                     uint8_t *__restrict__ xs, int32_t *dev_error, float *y_zero, int64_t y_n4)
 {
+    // The forward's device error word: cleared here, before anything of this call can record into it
+    // (bad permutation rows are recorded by the W2 GEMM, time-outs by the GEMMs, all later).
+    if (blockIdx.x == 0 && threadIdx.x == 0) *dev_error = 0;
     griddep_wait();                  // the permutation (and x) come from earlier kernels
     griddep_launch_dependents();
     zero_y(y_zero, y_n4);
@@ -732,7 +735,6 @@ __global__ void gather_quant_kernel(const uint16_t *__restrict__ x, const int32_
         const int b = live ? (int)(idx - r * nblk) : 0;
         const int32_t pr = live ? __ldg(row_to_pair + r) : -1;
         const bool real = live && pr >= 0 && pr < P;
-        if (live && pr >= P && b == 0) record_error(dev_error, DEV_ERR_ID_RANGE);
         float v[32];
         if (real) {
             const uint4 *src = reinterpret_cast<const uint4 *>(x + (int64_t)(pr / k) * H + b * 32);
@@ -789,16 +791,14 @@ __global__ void gather_rows_kernel(const int32_t *__restrict__ row_to_pair, cons
                                    int E, int64_t P, int32_t *__restrict__ p2r, int32_t *dev_error, float *y_zero,
                                    int64_t y_n4)
 {
+    if (blockIdx.x == 0 && threadIdx.x == 0) *dev_error = 0;   // the forward's error word, as above
     griddep_wait();                  // the permutation comes from an earlier kernel
     griddep_launch_dependents();
     zero_y(y_zero, y_n4);
     const int64_t R = __ldg(padded + E);
     for (int64_t r = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; r < R; r += (int64_t)gridDim.x * blockDim.x) {
         const int32_t pr = __ldg(row_to_pair + r);
-        if (pr >= 0 && pr < P)
-            p2r[pr] = (int32_t)r;
-        else if (pr >= P)
-            record_error(dev_error, DEV_ERR_ID_RANGE);
+        if (pr >= 0 && pr < P) p2r[pr] = (int32_t)r;   // entries >= P are recorded by the W2 GEMM
     }
 }
 
