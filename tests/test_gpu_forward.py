@@ -361,6 +361,32 @@ def test_bf16_output_is_the_rounded_fp32_output(gpu_lib, gpu_layers, name):
         assert torch.equal(y, ref.to(torch.bfloat16)), f"flags {flags}"
 
 
+@pytest.mark.parametrize("name", ["tiny_t37_h512_e32", "prefill_t2048_h4096_e256", "prefill_t8191_zipf_h4096_e256"])
+def test_forward_reports_bad_rows_and_clears_the_word_on_the_next_call(gpu_lib, gpu_layers, name):
+    """A row_to_pair entry >= T*k is recorded in the workspace's error word (by the W2 GEMM) on both
+    gather paths; the next forward clears the word first thing, so a clean call after a bad one
+    reads 0 without an explicit clear in between."""
+    moe = gpu_lib
+    L = synth.make_config(name)
+    x, logits = gpu_layers.inputs(L)
+    T, k = L["T"], L["k"]
+    d = moe.make_desc(T, L["H"], L["I"], L["E"], k, 16)
+    ids, w, _ = moe.route(logits, k)
+    perm = moe.permute(ids, L["E"], 16)
+    ws = torch.empty(moe.workspace_bytes(d), dtype=torch.uint8, device="cuda")
+    bad = {n: v.clone() for n, v in perm.items()}
+    r2p = bad["row_to_pair"].cpu().numpy()
+    row = int(np.flatnonzero(r2p >= 0)[len(np.flatnonzero(r2p >= 0)) // 2])
+    bad["row_to_pair"][row] = T * k + 5
+    moe.forward(d, x, gpu_layers.packed(L), w, bad, ws)
+    torch.cuda.synchronize()
+    word = ws[:4].view(torch.int32)
+    assert int(word.item()) == 6                                      # MOE_ERR_DEVICE, not yet cleared
+    moe.forward(d, x, gpu_layers.packed(L), w, perm, ws)
+    torch.cuda.synchronize()
+    assert moe.read_device_error(word) == 0
+
+
 def test_forward_deterministic(gpu_lib, gpu_layers):
     L = synth.make_config("decode_t512_h4096_e256")
     a = _run_layer(gpu_lib, gpu_layers, L)["y"].clone()
