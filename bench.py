@@ -78,9 +78,13 @@ def algorithmic(L, ids, nt_x=NT_X, nt_h=NT_H):
     layer = touched * (w13 + w2) + T * H * 2 + T * E * 4 + T * H * 4
     flops = 6.0 * P * H * I
     mma_flops = 2.0 * P * H * I * (2 * nt_x + nt_h)
-    return dict(touched=touched, w13_kernel_bytes=w13_kernel, w2_kernel_bytes=w2_kernel, layer_bytes=layer,
-                flops=flops, w13_flops=4.0 * P * H * I, w2_flops=2.0 * P * H * I,
-                w13_mma_flops=4.0 * P * H * I * nt_x, w2_mma_flops=2.0 * P * H * I * nt_h, mma_flops=mma_flops)
+    d = dict(touched=touched, w13_kernel_bytes=w13_kernel, w2_kernel_bytes=w2_kernel, layer_bytes=layer,
+             flops=flops, w13_flops=4.0 * P * H * I, w2_flops=2.0 * P * H * I,
+             w13_mma_flops=4.0 * P * H * I * nt_x, w2_mma_flops=2.0 * P * H * I * nt_h, mma_flops=mma_flops)
+    # both GEMMs in one launch (the smallest batches): the sum of the two
+    for key in ("kernel_bytes", "flops", "mma_flops"):
+        d[f"gemms_{key}"] = d[f"w13_{key}"] + d[f"w2_{key}"]
+    return d
 
 
 def term_counts(moe, desc):
@@ -91,21 +95,20 @@ def term_counts(moe, desc):
 
 
 KERNEL_NAMES = {"w13": "moe_gemm_kernel<W13*> (grouped W13 GEMM + SiLU*up + h terms)",
-                "w2": "moe_gemm_kernel<W2*> (grouped W2 GEMM)"}
+                "w2": "moe_gemm_kernel<W2*> (grouped W2 GEMM)",
+                "gemms": "moe_gemm_decode_kernel (W13 GEMM + SiLU*up + h terms, then W2: one persistent launch)"}
 ROWS_KERNEL_NAMES = {"w13": "moe_gemm_rows_kernel<W13Rows> (token-major grouped W13 GEMM + SiLU*up + h terms)",
                      "w2": "moe_gemm_rows_kernel<W2Rows> (token-major grouped W2 GEMM)"}
 
 
-def kernel_names(L):
-    """Names of the two GEMM kernels the library launches for this layer: the token-major tiles above
-    64 rows per expert on average when H is a multiple of 256, the weight-major tiles otherwise (the
-    library's tile choice, restated here only to label the JSON line)."""
-    rows = L["T"] * L["k"] / L["E"] > 64 and L["H"] % 256 == 0
-    return ROWS_KERNEL_NAMES if rows else KERNEL_NAMES
+def kernel_names(plan):
+    """Names of the GEMM kernels the library launches for a layer, from its forward plan: token-major
+    tiles in the "huge" regime, weight-major tiles otherwise (one fused launch where the plan says so)."""
+    return ROWS_KERNEL_NAMES if plan["regime"] == "huge" else KERNEL_NAMES
 
 
 def kernel_roofline(name, key, alg, ms, peaks, names=KERNEL_NAMES):
-    """Roofline of one GEMM launch (key "w13" or "w2"): bound by HBM or by the tensor pipe,
+    """Roofline of one GEMM launch (key "w13", "w2", or "gemms" for both in one launch): bound by HBM or by the tensor pipe,
     whichever needs more time for the work it executes (all activation terms) at the measured
     peaks; `achieved` counts the algorithmic (useful) bytes or flops."""
     hbm, bf16, bf16_sus, kind = peaks
@@ -326,13 +329,16 @@ def time_workload(moe, L, steps, warmup, flush_buf, events_per_step=True):
     layer = moe.MoELayer.create(T, H, I, E, k, *w, block_m=16, device=dev)
     del w
     b = layer.bufs
+    fused = moe.forward_plan(layer.desc)["fused_gemms"]
 
     def step(evs):
-        """One layer step with an event between kernels: each kernel timed alone (no overlap)."""
+        """One layer step with an event between kernels: each kernel timed alone (no overlap). Where the
+        library runs both GEMMs as one launch, no event goes between them, so that launch is timed."""
         evs[0].record()
         moe.route_permute(logits, k, 16, out=(b["ids"], b["w"], b["bm"]), perm_out=b["perm"], error=b["perm_err"])
         evs[1].record()
-        moe.forward_timed(layer.desc, x, layer.packed, b["w"], b["perm"], layer.workspace, b["y"], evs[2:7])
+        lib_ev = [evs[2], evs[3], None, evs[5], evs[6]] if fused else evs[2:7]
+        moe.forward_timed(layer.desc, x, layer.packed, b["w"], b["perm"], layer.workspace, b["y"], lib_ev)
 
     def step_fast():
         """One layer step as a user runs it: consecutive kernels overlap their start with the previous end."""
@@ -424,17 +430,21 @@ def time_fast_combine(moe, layer, x, logits, flush_buf, steps):
     return st
 
 
-def summarize(evsets):
+def summarize(evsets, fused=False):
     # events: 0 start, 1 after route+permute, 2 before gather, 3 after gather, 4 after W13, 5 after W2, 6 after combine
-    keys = ["route_permute", "gather", "w13", "w2", "combine"]
+    # (with both GEMMs in one launch, event 4 is not recorded and "gemms" is the launch from 3 to 5)
+    keys = ["route_permute", "gather"] + (["gemms"] if fused else ["w13", "w2"]) + ["combine"]
     out = {k: [] for k in keys}
     total = []
     for ev in evsets:
         t = [ev[0].elapsed_time(e) for e in ev]
         out["route_permute"].append(t[2] - t[0])
         out["gather"].append(t[3] - t[2])
-        out["w13"].append(t[4] - t[3])
-        out["w2"].append(t[5] - t[4])
+        if fused:
+            out["gemms"].append(t[5] - t[3])
+        else:
+            out["w13"].append(t[4] - t[3])
+            out["w2"].append(t[5] - t[4])
         out["combine"].append(t[6] - t[5])
         total.append(t[6])
     return {k: float(np.mean(v)) for k, v in out.items()}, float(np.sum(total)), [float(v) for v in total]
@@ -460,7 +470,8 @@ def measure_config(moe, name, L, steps, warmup, flush_buf, peaks):
         step(ev)
     torch.cuda.synchronize()
     assert lay.forward_error() == 0, f"device error in {name}"
-    pk, _, _ = summarize(evs)
+    plan = moe.forward_plan(lay.desc)
+    pk, _, _ = summarize(evs, plan["fused_gemms"])
     route_us = route_us_graph(moe, lay, load_logits(lay, L), flush_buf)
     nt_x, nt_h = term_counts(moe, lay.desc)
     a = algorithmic(L, lay.bufs["ids"].cpu().numpy(), nt_x, nt_h)
@@ -476,9 +487,13 @@ def measure_config(moe, name, L, steps, warmup, flush_buf, peaks):
                            "flops": a["flops"],
                            "mxf8_frac_useful": a["flops"] / (ms / 1e3) / 1e12 / mxf8,
                            "mxf8_frac_executed": a["mma_flops"] / (ms / 1e3) / 1e12 / mxf8},
-        "w13_roofline": kernel_roofline(name, "w13", a, pk["w13"], peaks, kernel_names(L)),
-        "w2_roofline": kernel_roofline(name, "w2", a, pk["w2"], peaks, kernel_names(L)),
+        "forward_plan": plan,
     }
+    if plan["fused_gemms"]:
+        out["gemms_roofline"] = kernel_roofline(name, "gemms", a, pk["gemms"], peaks, kernel_names(plan))
+    else:
+        out["w13_roofline"] = kernel_roofline(name, "w13", a, pk["w13"], peaks, kernel_names(plan))
+        out["w2_roofline"] = kernel_roofline(name, "w2", a, pk["w2"], peaks, kernel_names(plan))
     return out, lay, a
 
 
@@ -527,7 +542,8 @@ def run_ours(args, world, rank, local):
         flush_buf.zero_()
         step(ev)
     torch.cuda.synchronize()
-    per_kernel, _, _ = summarize(evsets)
+    plan = moe.forward_plan(layer.desc)
+    per_kernel, _, _ = summarize(evsets, plan["fused_gemms"])
     route_us = route_us_graph(moe, layer, logits, flush_buf)
     ms_per_step = total_ms / args.steps
     value = world * T / (ms_per_step / 1e3)
@@ -535,10 +551,14 @@ def run_ours(args, world, rank, local):
     ids = layer.bufs["ids"].cpu().numpy()
     nt_x, nt_h = term_counts(moe, layer.desc)
     alg = algorithmic(L, ids, nt_x, nt_h)
-    dominant = "w13" if per_kernel["w13"] >= per_kernel["w2"] else "w2"
-    roofline = kernel_roofline(args.workload, dominant, alg, per_kernel[dominant], peaks, kernel_names(L))
-    other = kernel_roofline(args.workload, "w2" if dominant == "w13" else "w13", alg,
-                            per_kernel["w2" if dominant == "w13" else "w13"], peaks, kernel_names(L))
+    if plan["fused_gemms"]:
+        roofline = kernel_roofline(args.workload, "gemms", alg, per_kernel["gemms"], peaks, kernel_names(plan))
+        other = None
+    else:
+        dominant = "w13" if per_kernel["w13"] >= per_kernel["w2"] else "w2"
+        roofline = kernel_roofline(args.workload, dominant, alg, per_kernel[dominant], peaks, kernel_names(plan))
+        other = kernel_roofline(args.workload, "w2" if dominant == "w13" else "w13", alg,
+                                per_kernel["w2" if dominant == "w13" else "w13"], peaks, kernel_names(plan))
     layer_gbs = alg["layer_bytes"] / (ms_per_step / 1e3) / 1e9
     layer_tflops = alg["flops"] / (ms_per_step / 1e3) / 1e12
 
@@ -672,6 +692,7 @@ def run_ours(args, world, rank, local):
                                "mxf8_frac_useful_of_sustained": layer_tflops / (MXF8_OVER_BF16 * bf16_sus)},
             "roofline": roofline,
             "other_gemm_roofline": other,
+            "forward_plan": plan,
             "e2e": e2e,
             "gpu_launches": launches,
             "wall_s_timed": wall,

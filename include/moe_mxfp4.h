@@ -213,7 +213,9 @@ moe_status_t moe_mxfp4_dequant_bf16(const moe_layer_desc *desc, const void *d_pa
                                     int which, int expert, uint16_t *d_out, void *stream);
 
 /* Workspace bytes moe_mxfp4_forward needs for desc (all of T, H, I, E, k,
- * block_m matter). The first 256 bytes hold the forward's device error word. */
+ * block_m matter). The first 4 KB hold the forward's device error word
+ * (bytes 0-3) and the per-expert progress counters of the fused decode GEMMs
+ * (from byte 256). */
 size_t moe_mxfp4_workspace_bytes(const moe_layer_desc *desc);
 
 /*
@@ -242,7 +244,7 @@ size_t moe_mxfp4_workspace_bytes(const moe_layer_desc *desc);
  * fp32 accumulation; output fp32 (or its bf16 rounding). Result within
  * 2e-2 * rms of the float64 oracle (measured errors are up to about
  * 4e-3 * rms; bf16 output adds its rounding, at most 2^-9 |y|).
- * Launches 4 or 5 kernels on `stream` (one fewer with the atomic combine);
+ * Launches 3 to 5 kernels on `stream` (moe_mxfp4_forward_plan says which);
  * deterministic (bit-identical reruns) unless MOE_FLAG_FAST_COMBINE takes the
  * atomic combine. The GEMMs stream their weights before the kernel ahead of
  * them has finished.
@@ -254,12 +256,15 @@ moe_status_t moe_mxfp4_forward(const moe_layer_desc *desc, const uint16_t *d_x,
                                void *d_workspace, size_t workspace_bytes, void *stream);
 
 /*
- * moe_mxfp4_forward with timing: identical work, plus cudaEventRecord of
+ * moe_mxfp4_forward with timing: identical results, plus cudaEventRecord of
  * events[0..4] (cudaEvent_t passed as void*, created by the caller on this
  * device) on `stream` before the gather, after the gather, after the W13 GEMM,
  * after the W2 GEMM and after the combine. NULL entries are skipped. With any
  * event given, the kernels run one after another without overlap, so each
- * interval is one kernel's time.
+ * interval is one kernel's time. Where moe_mxfp4_forward_plan reports one
+ * launch for both GEMMs, a non-NULL events[2] splits them into two launches
+ * (same results, bit for bit); with events[2] NULL the interval from
+ * events[1] to events[3] is the fused launch.
  */
 moe_status_t moe_mxfp4_forward_timed(const moe_layer_desc *desc, const uint16_t *d_x,
                                      const void *d_packed, const float *d_topk_w,
@@ -279,6 +284,21 @@ moe_status_t moe_mxfp4_forward_timed(const moe_layer_desc *desc, const uint16_t 
  * bytes. R = moe_permute_rows_capacity(T, E, k, block_m). An element's value
  * is the sum over terms of E4M3 value * 2^(scale byte - 127). */
 moe_status_t moe_mxfp4_workspace_layout(const moe_layer_desc *desc, size_t out[7]);
+
+/*
+ * What moe_mxfp4_forward launches for desc (no device work; only the shape,
+ * flags and out_dtype of desc matter). out[0]: the GEMM tile regime, by
+ * average rows per expert T*k/E: 0 up to 2 (weight tiles of 16 token rows),
+ * 1 up to 16 (32 rows), 2 up to 64 (64 rows), 3 above 64 with H not a
+ * multiple of 256 (96 rows), 4 above 64 with H a multiple of 256 (token-major
+ * tiles of 128 rows x 256 weight rows). out[1]: 1 when W13 and W2 run as one
+ * persistent launch (regime 0 with E <= 512, H and I multiples of 256 and at
+ * least 512): each expert's W2 tiles start once its W13 tiles have stored
+ * their h rows, tracked by per-expert counters in the workspace. out[2]: 1
+ * when MOE_FLAG_FAST_COMBINE is taken (regimes 0 and 1, fp32 output).
+ * out[3]: kernels launched. Returns check failures as moe_mxfp4_forward does.
+ */
+moe_status_t moe_mxfp4_forward_plan(const moe_layer_desc *desc, int out[4]);
 
 /*
  * Forward without a caller workspace, for callers that cannot allocate device

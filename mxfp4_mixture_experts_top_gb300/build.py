@@ -18,7 +18,7 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmoe_mxfp4.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 
-SOURCES = ["api.cu", "route.cu", "permute.cu", "prepack.cu", "gemm.cu", "gemm_rows.cu", "ep.cu", "noalloc.cu", "selftest.cu"]
+SOURCES = ["api.cu", "route.cu", "permute.cu", "prepack.cu", "gemm.cu", "gemm_rows.cu", "gemm_decode.cu", "ep.cu", "noalloc.cu", "selftest.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2", "-I", CSRC, "-I", INCLUDE]
 

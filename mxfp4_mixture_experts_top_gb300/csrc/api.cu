@@ -159,7 +159,7 @@ Layout workspace_layout(const moe_layer_desc *d)
     const int64_t RS = scale_rows(d);
     Layout L;
     L.err = 0;
-    L.xq = 1024;
+    L.xq = 4096;                 // error word at 0, fused-decode expert counters from byte 256
     L.xs = align_up(L.xq + (size_t)NT_X * R * d->H, 1024);
     L.hq = align_up(L.xs + (size_t)NT_X * RS * (d->H / 32), 1024);
     L.hs = align_up(L.hq + (size_t)NT_H * R * d->I, 1024);
@@ -324,6 +324,21 @@ moe_status_t moe_mxfp4_workspace_layout(const moe_layer_desc *d, size_t out[7])
     return MOE_OK;
 }
 
+moe_status_t moe_mxfp4_forward_plan(const moe_layer_desc *d, int out[4])
+{
+    moe_status_t st = check_desc(d);
+    if (st != MOE_OK) return st;
+    if (!out) return MOE_ERR_INVALID_ARG;
+    const Regime rg = pick_regime(d->T, d->k, d->E, d->H);
+    const ForwardPlan pl = plan_forward(rg, d->H, d->I, d->E, (d->flags & MOE_FLAG_FAST_COMBINE) != 0,
+                                        d->out_dtype == MOE_OUT_BF16, false);
+    out[0] = (int)rg;
+    out[1] = pl.fused ? 1 : 0;
+    out[2] = pl.fast ? 1 : 0;
+    out[3] = pl.launches;
+    return MOE_OK;
+}
+
 moe_status_t moe_mxfp4_forward_timed(const moe_layer_desc *d, const uint16_t *d_x, const void *d_packed,
                                      const float *d_topk_w, const int32_t *d_offsets,
                                      const int32_t *d_padded_offsets, const int32_t *d_row_to_pair, void *d_y,
@@ -362,6 +377,7 @@ moe_status_t moe_mxfp4_forward_timed(const moe_layer_desc *d, const uint16_t *d_
     a.padded = d_padded_offsets;
     a.row_to_pair = d_row_to_pair;
     a.y = d_y;
+    a.done13 = reinterpret_cast<uint32_t *>(ws + L.err + 256);
     a.y_bf16 = d->out_dtype == MOE_OUT_BF16;
     a.dev_error = reinterpret_cast<int32_t *>(ws + L.err);
     a.xq = ws + L.xq;

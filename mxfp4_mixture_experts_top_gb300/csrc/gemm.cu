@@ -450,7 +450,8 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_kernel(const __grid_co
         }
         if (!ok && lane == 0) fail();
     } else if (warp == 8 || (C::MW == 2 && warp == 11)) {
-        // ===================== MMA issuers: stage s belongs to warp s % MW. The warp waits for the stage's
+        // ===================== MMA issuers: stage s belongs to warp s % MW (s counted from the tile's
+        // start when stages align with tiles, else over the CTA's whole stage sequence). The warp waits for the stage's
         // scale-factor cell only: the copiers fill it after the stage's weights and activations have
         // landed, so that one wait covers all three. One elected lane issues the stage's block-scaled MMAs
         // (four of K = 32 per slab) into the warp's own accumulator set and commits the stage to
@@ -489,7 +490,10 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_kernel(const __grid_co
         };
         for (int i0 = 0; i0 < n_slabs && ok; i0 += SPS, ++st) {
             const int nsl = n_slabs - i0 < SPS ? n_slabs - i0 : SPS;
-            const bool mine = (st % C::MW) == q;
+            // when stages align with tiles, ownership counts stages from the tile's start, so the K split
+            // between the two accumulator sets (and the rounding of their sum) does not depend on which
+            // CTA ran the tile or on how many tiles it ran before
+            const bool mine = (((slabs % SPS) == 0 ? ka / SPS : st) % C::MW) == q;
             if (mine) {
                 if (!__all_sync(0xFFFFFFFFu, ptx::mbar_wait(&sf_full[sc], sph, s_abort, LIM))) { ok = false; break; }
                 ptx::tc_fence_after();
@@ -557,7 +561,9 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_kernel(const __grid_co
             const Tile tl = decode_tile<C::NMAX>(t, tile_start, E, MB, s_cnt, s_pad0);
             // MMA warp q wrote into the tile iff one of the tile's stages is one of its stages
             const int s_first = (j * slabs) / SPS, s_last = (j * slabs + slabs - 1) / SPS;
-            const unsigned wrote = (C::MW == 1 || s_last > s_first) ? ((1u << C::MW) - 1u) : (1u << (s_first % C::MW));
+            const unsigned wrote = (C::MW == 1 || s_last > s_first) ? ((1u << C::MW) - 1u)
+                                 : (slabs % SPS) == 0        ? 1u
+                                                             : (1u << (s_first % C::MW));
             ok = ok && __all_sync(0xFFFFFFFFu, ptx::mbar_wait(&d_full[di], dph, s_abort, LIM));
             ptx::tc_fence_after();
             for (int c0 = 0; c0 < tl.n; c0 += 16, ++chunk) {
@@ -714,12 +720,17 @@ __device__ __forceinline__ void zero_y(float *y, int64_t n4)
 __global__ void gather_quant_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ row_to_pair,
                                     const int32_t *__restrict__ padded, int E, int H, int k, int64_t P,
                                     int64_t rows_cap, int64_t rows_sf, uint8_t *__restrict__ xq,
-                                    uint8_t *__restrict__ xs, int32_t *dev_error, float *y_zero, int64_t y_n4)
+                                    uint8_t *__restrict__ xs, int32_t *dev_error, float *y_zero, int64_t y_n4,
+                                    uint32_t *zero_counts)
 {
-    // The forward's device error word: cleared here, before anything of this call can record into it
-    // (bad permutation rows are recorded by the W2 GEMM, time-outs by the GEMMs, all later).
-    if (blockIdx.x == 0 && threadIdx.x == 0) *dev_error = 0;
     griddep_wait();                  // the permutation (and x) come from earlier kernels
+    // The forward's device error word and the fused decode GEMMs' per-expert counters are reset only
+    // now: a kernel of the previous call may run until this wait returns (the fused decode kernel
+    // lets its successor start early). Every kernel of this call that records an error or counts
+    // tiles waits for this grid to complete first.
+    if (blockIdx.x == 0 && threadIdx.x == 0) *dev_error = 0;
+    if (zero_counts && blockIdx.x == 0)
+        for (int e = threadIdx.x; e < E; e += blockDim.x) zero_counts[e] = 0u;
     griddep_launch_dependents();
     zero_y(y_zero, y_n4);
     const int64_t R = __ldg(padded + E);
@@ -791,8 +802,8 @@ __global__ void gather_rows_kernel(const int32_t *__restrict__ row_to_pair, cons
                                    int E, int64_t P, int32_t *__restrict__ p2r, int32_t *dev_error, float *y_zero,
                                    int64_t y_n4)
 {
-    if (blockIdx.x == 0 && threadIdx.x == 0) *dev_error = 0;   // the forward's error word, as above
     griddep_wait();                  // the permutation comes from an earlier kernel
+    if (blockIdx.x == 0 && threadIdx.x == 0) *dev_error = 0;   // the forward's error word, as above
     griddep_launch_dependents();
     zero_y(y_zero, y_n4);
     const int64_t R = __ldg(padded + E);
@@ -962,6 +973,22 @@ static void mark(const ForwardArgs &a, int i, cudaStream_t s)
     if (a.events && a.events[i]) cudaEventRecord(static_cast<cudaEvent_t>(a.events[i]), s);
 }
 
+ForwardPlan plan_forward(Regime rg, int H, int I, int E, bool fast_flag, bool y_bf16, bool split_gemms)
+{
+    ForwardPlan pl;
+    pl.two_pass = rg == Regime::Mid || rg == Regime::Large || rg == Regime::Huge;
+    // The flag permits the atomic combine; it is taken where it measured faster, up to 16 rows per
+    // expert on average (the weight-major decode tiles). Larger batches keep the slot-ordered combine:
+    // their W2 epilogues would issue T*k*H reductions, which cost the L2 more than the per-pair rows'
+    // round trip.
+    pl.fast = fast_flag && !y_bf16 && (rg == Regime::Tiny || rg == Regime::Small);
+    // The smallest batches run both GEMMs in one persistent launch (gemm_decode.cu), unless an event
+    // is to be recorded between them.
+    pl.fused = rg == Regime::Tiny && !split_gemms && decode_fused_supported(H, I, E);
+    pl.launches = (pl.two_pass ? 2 : 1) + (pl.fused ? 1 : 2) + (pl.fast ? 0 : 1);
+    return pl;
+}
+
 cudaError_t launch_forward(const ForwardArgs &a, cudaStream_t s)
 {
     const int64_t P = (int64_t)a.T * a.k;
@@ -971,15 +998,12 @@ cudaError_t launch_forward(const ForwardArgs &a, cudaStream_t s)
     bool pdl = true;
     for (int i = 0; i < 5 && a.events; ++i)
         if (a.events[i]) pdl = false;
+    const ForwardPlan pl = plan_forward(a.regime, a.H, a.I, a.E, a.fast_combine, a.y_bf16,
+                                        a.events && a.events[2]);
     mark(a, 0, s);
-    // The flag permits the atomic combine; it is taken where it measured faster, up to 16 rows per
-    // expert on average (the weight-major decode tiles). Larger batches keep the slot-ordered combine:
-    // their W2 epilogues would issue T*k*H reductions, which cost the L2 more than the per-pair rows'
-    // round trip.
-    const bool fast = a.fast_combine && !a.y_bf16 && (a.regime == Regime::Tiny || a.regime == Regime::Small);
+    const bool fast = pl.fast, two_pass = pl.two_pass, fused = pl.fused;
     float *y_zero = fast ? static_cast<float *>(a.y) : nullptr;
     const int64_t y_n4 = (int64_t)a.T * a.H / 4;
-    const bool two_pass = a.regime == Regime::Mid || a.regime == Regime::Large || a.regime == Regime::Huge;
     if (two_pass) {
         int32_t *p2r = reinterpret_cast<int32_t *>(a.staging);     // P entries; W2 overwrites them later
         int grid = (int)((a.rows_cap + 255) / 256);                  // a thread per row
@@ -1000,7 +1024,8 @@ cudaError_t launch_forward(const ForwardArgs &a, cudaStream_t s)
         if (grid > 8 * 1024) grid = 8 * 1024;
         if (grid < 1) grid = 1;
         err = launch_ex(gather_quant_kernel, dim3(grid), dim3(256), 0, s, pdl, a.x, a.row_to_pair, a.padded, a.E,
-                        a.H, a.k, P, a.rows_cap, a.rows_sf, a.xq, a.xs, a.dev_error, y_zero, y_n4);
+                        a.H, a.k, P, a.rows_cap, a.rows_sf, a.xq, a.xs, a.dev_error, y_zero, y_n4,
+                        fused ? a.done13 : nullptr);
         if (err != cudaSuccess) return err;
     }
     mark(a, 1, s);
@@ -1034,7 +1059,23 @@ cudaError_t launch_forward(const ForwardArgs &a, cudaStream_t s)
     g.K = a.H;
     g.MB = a.I / 64;
     const Regime rg = a.regime;
-    err = rg == Regime::Huge  ? launch_gemm_rows(g, 0, a.num_sms, s, pdl)
+    if (fused) {
+        GemmParams g2 = g;
+        g2.y = fast ? static_cast<float *>(a.y) : nullptr;
+        g2.tm_a = a.tmap_w2;
+        g2.tm_a1 = a.tmap_w2_1;
+        g2.tm_b = a.tmap_hq;
+        g2.tm_b1 = a.tmap_hq1;
+        g2.tm_bs = a.tmap_hs;
+        g2.tm_bs1 = a.tmap_hs1;
+        g2.wsf = a.packed + packed_w13_bytes(a.E, a.H, a.I) + (size_t)a.E * a.H * (a.I / 2);
+        g2.K = a.I;
+        g2.MB = a.H / TILE_ROWS;
+        err = launch_gemm_decode(g, g2, a.done13, fast, a.num_sms, s, pdl);
+        if (err != cudaSuccess) return err;
+    }
+    err = fused               ? cudaSuccess
+        : rg == Regime::Huge  ? launch_gemm_rows(g, 0, a.num_sms, s, pdl)
         : rg == Regime::Tiny  ? launch_gemm<W13Tiny>(g, a.num_sms, s, pdl)
         : rg == Regime::Small ? launch_gemm<W13Small>(g, a.num_sms, s, pdl)
         : rg == Regime::Mid   ? launch_gemm<W13Mid>(g, a.num_sms, s, pdl)
@@ -1054,7 +1095,8 @@ cudaError_t launch_forward(const ForwardArgs &a, cudaStream_t s)
     g.wsf = a.packed + packed_w13_bytes(a.E, a.H, a.I) + (size_t)a.E * a.H * (a.I / 2);
     g.K = a.I;
     g.MB = a.H / TILE_ROWS;
-    err = rg == Regime::Huge  ? launch_gemm_rows(g, 1, a.num_sms, s, pdl)
+    err = fused               ? cudaSuccess
+        : rg == Regime::Huge  ? launch_gemm_rows(g, 1, a.num_sms, s, pdl)
         : rg == Regime::Tiny  ? (a.E <= W2Tiny::EMAX ? (fast ? launch_gemm<W2Tiny, true>(g, a.num_sms, s, pdl)
                                                           : launch_gemm<W2Tiny>(g, a.num_sms, s, pdl))
                                                      : (fast ? launch_gemm<W2TinyWideE, true>(g, a.num_sms, s, pdl)
@@ -1078,7 +1120,7 @@ cudaError_t launch_forward(const ForwardArgs &a, cudaStream_t s)
         if (err != cudaSuccess) return err;
     }
     mark(a, 4, s);
-    note_launch((two_pass ? 5 : 4) - (fast ? 1 : 0));
+    note_launch(pl.launches);
     return cudaSuccess;
 }
 

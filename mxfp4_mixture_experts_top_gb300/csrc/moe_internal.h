@@ -97,6 +97,7 @@ struct ForwardArgs {
     void *y;                     // fp32 [T, H], or bf16 bits with y_bf16
     bool y_bf16;
     int32_t *dev_error;
+    uint32_t *done13;      // [E] per-expert W13 tiles finished (the fused decode GEMMs), in the workspace
     uint8_t *xq, *xs;      // x terms [H/128][NT_X][rows_cap][128], scale words [H/128][NT_X][rows_sf]
     uint8_t *hq, *hs;      // h terms [I/128][nt_h][rows_cap][128], scale words [I/128][nt_h][rows_sf]
     float *staging;
@@ -107,6 +108,16 @@ struct ForwardArgs {
     int num_sms;
     void *const *events;   // optional: 5 cudaEvent_t recorded between kernels
 };
+
+// What a forward launches for one layer shape (the single place that decides it).
+struct ForwardPlan {
+    bool two_pass;   // gather in two kernels (inverse map, then one conversion per token)
+    bool fused;      // W13 and W2 in one persistent launch (gemm_decode.cu)
+    bool fast;       // W2 adds w * o into y with reduction atomics; no combine kernel
+    int launches;    // kernels launched
+};
+// split_gemms: an event is recorded between the W13 and the W2 GEMM, so they stay two launches.
+ForwardPlan plan_forward(Regime rg, int H, int I, int E, bool fast_flag, bool y_bf16, bool split_gemms);
 
 cudaError_t launch_forward(const ForwardArgs &a, cudaStream_t s);
 

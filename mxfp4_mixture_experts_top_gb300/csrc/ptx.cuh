@@ -180,6 +180,30 @@ __device__ __forceinline__ void red_add_f32(float *p, float v)
     asm volatile("red.global.add.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
 }
 
+// Make this thread's earlier generic-proxy writes to global memory visible to async-proxy (TMA)
+// reads, and order its later async-proxy operations after its earlier generic ones.
+__device__ __forceinline__ void fence_proxy_async_global()
+{
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t *p)
+{
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void red_release_gpu_add(uint32_t *p, uint32_t v)
+{
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void nanosleep_ns(uint32_t ns)
+{
+    asm volatile("nanosleep.u32 %0;" ::"r"(ns));
+}
+
 // ----------------------------------------------------------------- tcgen05
 // Allocate `ncols` TMEM columns (power of two >= 32); whole warp executes.
 // The TMEM base address is written to shared memory at `dst`.

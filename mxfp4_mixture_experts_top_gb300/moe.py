@@ -23,7 +23,7 @@ STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
 # Every symbol the header declares (checked by the CPU test suite).
 EXPORTS = ["moe_abi_version", "moe_status_string", "moe_route", "moe_permute_rows_capacity", "moe_permute",
            "moe_mxfp4_packed_bytes", "moe_mxfp4_prepack", "moe_mxfp4_dequant_bf16", "moe_mxfp4_workspace_bytes",
-           "moe_mxfp4_forward", "moe_mxfp4_forward_timed", "moe_mxfp4_workspace_layout", "moe_read_device_error", "moe_launch_count",
+           "moe_mxfp4_forward", "moe_mxfp4_forward_timed", "moe_mxfp4_workspace_layout", "moe_mxfp4_forward_plan", "moe_read_device_error", "moe_launch_count",
            "moe_selftest_bounded_wait",
            "moe_mxfp4_forward_noalloc", "moe_route_permute", "moe_permute_workspace_size", "moe_clear_cache",
            "moe_mxfp4_noalloc_read_device_error", "moe_ep_dispatch_pack", "moe_ep_combine"]
@@ -69,6 +69,7 @@ def load(path: str = LIB_PATH):
             "moe_mxfp4_forward": ([D, P, P, P, P, P, P, P, P, sz, P], i32),
             "moe_mxfp4_forward_timed": ([D, P, P, P, P, P, P, P, P, sz, P, P], i32),
             "moe_mxfp4_workspace_layout": ([D, ctypes.POINTER(ctypes.c_size_t * 7)], i32),
+            "moe_mxfp4_forward_plan": ([D, ctypes.POINTER(ctypes.c_int * 4)], i32),
             "moe_read_device_error": ([P, ctypes.POINTER(ctypes.c_int), P], i32),
             "moe_launch_count": ([], ctypes.c_uint64),
             "moe_selftest_bounded_wait": ([ctypes.c_uint64, ctypes.c_uint64, P, P, P], i32),
@@ -204,6 +205,17 @@ def workspace_layout(desc: LayerDesc):
     arr = (ctypes.c_size_t * 7)()
     _check(load().moe_mxfp4_workspace_layout(ctypes.byref(desc), ctypes.byref(arr)), "moe_mxfp4_workspace_layout")
     return dict(error=arr[0], xq=arr[1], xs=arr[2], hq=arr[3], hs=arr[4], staging=arr[5], total=arr[6])
+
+
+REGIMES = ("tiny", "small", "mid", "large", "huge")
+
+
+def forward_plan(desc: LayerDesc):
+    """moe_mxfp4_forward_plan: the tile regime, whether W13 and W2 run as one launch, whether the
+    atomic combine is taken, and the number of kernels moe_mxfp4_forward launches."""
+    arr = (ctypes.c_int * 4)()
+    _check(load().moe_mxfp4_forward_plan(ctypes.byref(desc), ctypes.byref(arr)), "moe_mxfp4_forward_plan")
+    return dict(regime=REGIMES[arr[0]], fused_gemms=bool(arr[1]), fast_combine=bool(arr[2]), launches=arr[3])
 
 
 def prepack(desc: LayerDesc, w13_q, w13_s, w2_q, w2_s, stream=None) -> torch.Tensor:

@@ -82,6 +82,31 @@ def test_desc_validation(lib, T, H, I, E, k, bm, code):
     assert lib.moe_mxfp4_workspace_layout(ctypes.byref(d), ctypes.byref(arr)) == code
 
 
+@pytest.mark.parametrize("T,H,I,E,k,flags,out,want", [
+    # decode: 48 pairs over 256 experts, both GEMMs in one launch: gather, GEMMs, combine
+    (8, 4096, 2048, 256, 6, 0, 0, ("tiny", True, False, 3)),
+    (8, 4096, 2048, 256, 6, 1, 0, ("tiny", True, True, 2)),        # atomic combine: no combine kernel
+    (8, 4096, 2048, 256, 6, 1, 1, ("tiny", True, False, 3)),       # bf16 output keeps the slot-ordered combine
+    (8, 4096, 2048, 1024, 6, 0, 0, ("tiny", False, False, 4)),     # more than 512 experts: two GEMM launches
+    (1, 384, 512, 8, 1, 0, 0, ("tiny", False, False, 4)),          # H not a multiple of 256
+    (2, 512, 256, 8, 2, 0, 0, ("tiny", False, False, 4)),          # I below 512
+    (512, 4096, 2048, 256, 6, 1, 0, ("small", False, True, 3)),    # 12 rows per expert
+    (2048, 4096, 2048, 256, 6, 1, 0, ("mid", False, False, 5)),    # two-pass gather, no atomics
+    (4096, 640, 512, 32, 4, 0, 0, ("large", False, False, 5)),     # H % 256 != 0: 96-row weight tiles
+    (8191, 4096, 2048, 256, 6, 0, 0, ("huge", False, False, 5)),   # token-major tiles
+])
+def test_forward_plan(lib, T, H, I, E, k, flags, out, want):
+    """The host-side plan of a forward: tile regime by rows per expert, one or two GEMM launches, the
+    atomic combine, and the kernel count (no device work)."""
+    d = moe.make_desc(T, H, I, E, k, 16, 0.0, flags, out)
+    p = moe.forward_plan(d)
+    assert (p["regime"], p["fused_gemms"], p["fast_combine"], p["launches"]) == want
+    bad = moe.make_desc(T, H, I, E, k, 24)
+    arr = (ctypes.c_int * 4)()
+    assert lib.moe_mxfp4_forward_plan(ctypes.byref(bad), ctypes.byref(arr)) == 2
+    assert lib.moe_mxfp4_forward_plan(ctypes.byref(d), None) == 1
+
+
 def test_entry_points_reject_bad_arguments_without_launching(lib):
     n0 = moe.launch_count()
     null = None

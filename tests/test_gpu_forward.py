@@ -387,6 +387,44 @@ def test_forward_reports_bad_rows_and_clears_the_word_on_the_next_call(gpu_lib, 
     assert moe.read_device_error(word) == 0
 
 
+@pytest.mark.parametrize("T,H,I,E,k,limit", [(8, 512, 512, 64, 6, 0.0), (16, 1024, 512, 48, 4, 0.0),
+                                             (3, 4096, 2048, 256, 6, 10.0), (1, 512, 1024, 8, 1, 0.0),
+                                             (170, 768, 512, 512, 6, 0.0)])
+def test_fused_decode_gemms_match_two_launches_and_oracle(gpu_lib, gpu_layers, T, H, I, E, k, limit):
+    """At most 2 rows per expert, W13 and W2 run as one persistent launch in which an expert's W2
+    tiles wait for its W13 tiles through counters in the workspace. Its output equals the two-launch
+    path (which the forward takes when events are recorded between kernels) bit for bit, and the
+    oracle within tolerance; the same with the atomic combine and with bf16 output."""
+    moe = gpu_lib
+    L = synth.make_layer(T=T, H=H, E=E, k=k, I=I, seed=T * 13 + E)
+    x, logits = gpu_layers.inputs(L)
+    packed = gpu_layers.packed(L)
+    ids, w, _ = moe.route(logits, k)
+    perm = moe.permute(ids, E, 16)
+    d = moe.make_desc(T, H, I, E, k, 16, limit)
+    ws = torch.empty(moe.workspace_bytes(d), dtype=torch.uint8, device="cuda")
+    fused = moe.forward(d, x, packed, w, perm, ws).clone()
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+    for e in evs:
+        e.record()
+    two = torch.empty_like(fused)
+    moe.forward_timed(d, x, packed, w, perm, ws, two, evs)
+    torch.cuda.synchronize()
+    assert moe.read_device_error(ws[:4].view(torch.int32)) == 0
+    assert torch.equal(fused, two)
+    ids_r, w_r, _ = oracle.route(L["logits"], k)
+    _compare(f"fused decode {T}x{H}x{I} E{E} k{k} L{limit}", fused.cpu().numpy(),
+             oracle.forward(L, ids_r, w_r, swiglu_limit=limit))
+    df = moe.make_desc(T, H, I, E, k, 16, limit, moe.FLAG_FAST_COMBINE)
+    fast = moe.forward(df, x, packed, w, perm, ws)
+    db = moe.make_desc(T, H, I, E, k, 16, limit, 0, moe.OUT_BF16)
+    yb = moe.forward(db, x, packed, w, perm, ws)
+    torch.cuda.synchronize()
+    assert moe.read_device_error(ws[:4].view(torch.int32)) == 0
+    assert (fast - fused).abs().max().item() <= 1e-5 * fused.abs().max().item()
+    assert torch.equal(yb, fused.to(torch.bfloat16))
+
+
 def test_forward_deterministic(gpu_lib, gpu_layers):
     L = synth.make_config("decode_t512_h4096_e256")
     a = _run_layer(gpu_lib, gpu_layers, L)["y"].clone()
