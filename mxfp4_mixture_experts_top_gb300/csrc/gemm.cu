@@ -1059,6 +1059,9 @@ cudaError_t launch_forward(const ForwardArgs &a, cudaStream_t s)
     g.K = a.H;
     g.MB = a.I / 64;
     const Regime rg = a.regime;
+    // 17 to 64 rows per expert: token-major tiles of 64 token rows x 2 stacked terms where the 256-row
+    // weight blocks divide H (gemm_rows.cu), else the 64-row weight-major tiles
+    const bool rows64 = rg == Regime::Mid && a.H % 256 == 0;
     if (fused) {
         GemmParams g2 = g;
         g2.y = fast ? static_cast<float *>(a.y) : nullptr;
@@ -1075,7 +1078,8 @@ cudaError_t launch_forward(const ForwardArgs &a, cudaStream_t s)
         if (err != cudaSuccess) return err;
     }
     err = fused               ? cudaSuccess
-        : rg == Regime::Huge  ? launch_gemm_rows(g, 0, a.num_sms, s, pdl)
+        : rg == Regime::Huge  ? launch_gemm_rows(g, 0, false, a.num_sms, s, pdl)
+        : rows64              ? launch_gemm_rows(g, 0, true, a.num_sms, s, pdl)
         : rg == Regime::Tiny  ? launch_gemm<W13Tiny>(g, a.num_sms, s, pdl)
         : rg == Regime::Small ? launch_gemm<W13Small>(g, a.num_sms, s, pdl)
         : rg == Regime::Mid   ? launch_gemm<W13Mid>(g, a.num_sms, s, pdl)
@@ -1096,7 +1100,8 @@ cudaError_t launch_forward(const ForwardArgs &a, cudaStream_t s)
     g.K = a.I;
     g.MB = a.H / TILE_ROWS;
     err = fused               ? cudaSuccess
-        : rg == Regime::Huge  ? launch_gemm_rows(g, 1, a.num_sms, s, pdl)
+        : rg == Regime::Huge  ? launch_gemm_rows(g, 1, false, a.num_sms, s, pdl)
+        : rows64              ? launch_gemm_rows(g, 1, true, a.num_sms, s, pdl)
         : rg == Regime::Tiny  ? (a.E <= W2Tiny::EMAX ? (fast ? launch_gemm<W2Tiny, true>(g, a.num_sms, s, pdl)
                                                           : launch_gemm<W2Tiny>(g, a.num_sms, s, pdl))
                                                      : (fast ? launch_gemm<W2TinyWideE, true>(g, a.num_sms, s, pdl)

@@ -77,6 +77,8 @@ cudaError_t launch_gemm_decode(const GemmParams &g13, const GemmParams &g2, uint
 
 // Token-major tiles for large batches (gemm_rows.cu): 128 token rows x 256 weight rows per tile.
 // MODE 0: W13, MODE 1: W2. p.MB must be even.
-cudaError_t launch_gemm_rows(const GemmParams &p, int mode, int grid, cudaStream_t s, bool pdl);
+// Token-major tiles: 128 token rows per tile (stacked = false) or 64 token rows with their two terms
+// stacked as the MMA's A rows (stacked = true); 256 weight rows either way (H % 256 == 0).
+cudaError_t launch_gemm_rows(const GemmParams &p, int mode, bool stacked, int grid, cudaStream_t s, bool pdl);
 
 }  // namespace moe

@@ -55,10 +55,13 @@ namespace moe {
 namespace {
 
 // MODE 0: W13, MODE 1: W2. NW / NX: weight / activation ring stages; NSF: TMEM scale-factor cells.
-template <int MODE_, int NW_, int NX_, int NSF_, int EMAX_>
+// STACK: 64 token rows per tile, their two terms stacked as the MMA's 128 A rows (see above).
+template <int MODE_, int NW_, int NX_, int NSF_, int EMAX_, bool STACK_ = false>
 struct RCfg {
     static constexpr int MODE = MODE_, NW = NW_, NX = NX_, NSF = NSF_, EMAX = EMAX_;
-    static constexpr int TM = 128;                   // token rows per tile
+    static constexpr bool STACK = STACK_;
+    static constexpr int TM = STACK ? 64 : 128;      // token rows per tile
+    static constexpr int MM = 128;                   // MMA M (A rows)
     static constexpr int TN = 256;                   // weight rows per tile
     static constexpr int NT = 2;                     // activation terms (x: NT_X; h: the Huge h terms)
     static constexpr int CELL_COLS = 16;             // one slab: A cells of term 0 and 1 (4 each), B (8)
@@ -74,11 +77,13 @@ static_assert(NTH_HUGE == 2 && NT_X == 2, "the token-major tiles take two terms 
 
 using W13Rows = RCfg<0, 3, 3, 4, 1024>;
 using W2Rows = RCfg<1, 3, 3, 4, 1024>;
+using W13Rows64 = RCfg<0, 4, 3, 4, 1024, true>;
+using W2Rows64 = RCfg<1, 4, 3, 4, 1024, true>;
 
 template <class C>
 struct RSmem {
     static constexpr int XTERM = C::TM * 128;                  // one term's rows of one slab
-    static constexpr int XSTAGE = C::NT * XTERM;               // 32 KB
+    static constexpr int XSTAGE = C::NT * XTERM;               // 32 KB (16 KB stacked: the A operand)
     static constexpr int WSTAGE = 2 * SLAB_SMEM_BYTES;         // two expanded weight slabs, 32 KB
     static constexpr int XSSTAGE = C::NT * C::TM * 4;          // scale words [term][row], 1 KB
     static constexpr int WSSTAGE = 2 * SLAB_SF_BYTES;          // 1 KB
@@ -86,7 +91,10 @@ struct RSmem {
     static constexpr int W_OFF = X_OFF + C::NX * XSTAGE;
     static constexpr int XS_OFF = W_OFF + C::NW * WSTAGE;
     static constexpr int WS_OFF = XS_OFF + C::NX * XSSTAGE;
-    static constexpr int BAR_OFF = WS_OFF + C::NW * WSSTAGE;
+    // stacked tiles: per epilogue warp 32 columns x 32 lanes of fp32 partial sums for its partner
+    static constexpr int EX_OFF = WS_OFF + C::NW * WSSTAGE;
+    static constexpr int EX_BYTES = C::STACK ? 8 * 32 * 32 * 4 : 0;
+    static constexpr int BAR_OFF = EX_OFF + EX_BYTES;
     static constexpr int NBARS = C::NW + C::NX + C::NSF + C::ND + 3;
     static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;
     static constexpr int PREFIX_OFF = MISC_OFF + 16;
@@ -291,13 +299,20 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_rows_kernel(const __gr
             const uint32_t *xs = reinterpret_cast<const uint32_t *>(xsring + xi * S::XSSTAGE);
             const uint4 w0 = *reinterpret_cast<const uint4 *>(wsring + wi * S::WSSTAGE + lane * 16);
             const uint4 w1 = *reinterpret_cast<const uint4 *>(wsring + wi * S::WSSTAGE + SLAB_SF_BYTES + lane * 16);
-            uint32_t va[8], vb[8];
-#pragma unroll
-            for (int c = 0; c < 8; ++c) va[c] = xs[(c >> 2) * TM + lane + 32 * (c & 3)];
+            uint32_t vb[8];
             vb[0] = w0.x; vb[1] = w0.y; vb[2] = w0.z; vb[3] = w0.w;
             vb[4] = w1.x; vb[5] = w1.y; vb[6] = w1.z; vb[7] = w1.w;
             const uint32_t cell = tmem + quarter + (uint32_t)(C::SF_BASE + sc * C::CELL_COLS);
-            ptx::tmem_st_32x32b_x8(cell, va);
+            if constexpr (C::STACK) {
+                // A row 32c + lane is word 32c + lane of the stage ([term][64 rows]): columns 0-1 term 0,
+                // 2-3 term 1
+                ptx::tmem_st_32x32b_x4(cell, xs[lane], xs[32 + lane], xs[64 + lane], xs[96 + lane]);
+            } else {
+                uint32_t va[8];
+#pragma unroll
+                for (int c = 0; c < 8; ++c) va[c] = xs[(c >> 2) * TM + lane + 32 * (c & 3)];
+                ptx::tmem_st_32x32b_x8(cell, va);
+            }
             ptx::tmem_st_32x32b_x8(cell + 8u, vb);
             ptx::tmem_wait_st();
             ptx::tc_fence_before();
@@ -330,12 +345,20 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_rows_kernel(const __gr
                 const uint64_t wd = wdesc0 + (uint64_t)((uint32_t)(wi * S::WSTAGE) >> 4);
 #pragma unroll
                 for (int kb = 0; kb < 4; ++kb) {
-#pragma unroll
-                    for (int t = 0; t < NT; ++t) {
-                        const uint64_t xd = xdesc0 + (uint64_t)((uint32_t)(xi * S::XSTAGE + t * S::XTERM) >> 4);
+                    if constexpr (C::STACK) {
+                        // both terms in one MMA: A rows 0-63 term 0, 64-127 term 1 of the same tokens
+                        const uint64_t xd = xdesc0 + (uint64_t)((uint32_t)(xi * S::XSTAGE) >> 4);
                         ptx::mma_mx_ss(tmem, xd + (uint64_t)(kb * 2), wd + (uint64_t)(kb * 2),
-                                       ptx::idesc_mx(0u, 5u, TM, C::TN, (uint32_t)kb), cell + (uint32_t)(4 * t),
-                                       cell + 8u, (ka > 0 || kb > 0 || t > 0) ? 1u : 0u);
+                                       ptx::idesc_mx(0u, 5u, C::MM, C::TN, (uint32_t)kb), cell, cell + 8u,
+                                       (ka > 0 || kb > 0) ? 1u : 0u);
+                    } else {
+#pragma unroll
+                        for (int t = 0; t < NT; ++t) {
+                            const uint64_t xd = xdesc0 + (uint64_t)((uint32_t)(xi * S::XSTAGE + t * S::XTERM) >> 4);
+                            ptx::mma_mx_ss(tmem, xd + (uint64_t)(kb * 2), wd + (uint64_t)(kb * 2),
+                                           ptx::idesc_mx(0u, 5u, C::MM, C::TN, (uint32_t)kb), cell + (uint32_t)(4 * t),
+                                           cell + 8u, (ka > 0 || kb > 0 || t > 0) ? 1u : 0u);
+                        }
                     }
                 }
                 ptx::mma_commit(&done[s % C::ND]);
@@ -356,13 +379,78 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_rows_kernel(const __gr
         __syncwarp();
         __all_sync(0xFFFFFFFFu, ptx::mbar_wait(mma_done, 0, &never, LIM));
     } else if (warp < 4 || warp >= 12) {
-        // ===================== epilogue: lane quarter warp % 4 (token rows 32q .. 32q+31), columns
-        // 128g .. 128g+127 in two chunks of 64 (g = 0 for warps 0-3, 1 for warps 12-15)
+        // ===================== epilogue: lane quarter q = warp % 4, columns 128g .. 128g+127 (g = 0 for
+        // warps 0-3, 1 for warps 12-15) in two chunks of 64. Token-row tiles: lane quarter q is token rows
+        // 32q .. 32q+31 and the warp finishes both chunks. Stacked tiles: quarters 0-1 hold term 0 of token
+        // rows 0-63 and quarters 2-3 term 1 of the same rows, so warps q and q ^ 2 hold the two halves of
+        // the same sums: each sends the partner its partial sums of one chunk through shared memory, in two
+        // rounds of 32 columns, and finishes the other (chunk q >> 1), term 0 + term 1 in both.
         const int q = warp & 3, g = warp >= 12 ? 1 : 0;
         const uint32_t t_lane = (uint32_t)(q * 32) << 16;
-        const int trow = q * 32 + lane;                      // token row in the tile
+        const int trow = C::STACK ? (q & 1) * 32 + lane : q * 32 + lane;   // token row in the tile
+        float *ex_send = reinterpret_cast<float *>(smem + S::EX_OFF) + (g * 4 + q) * 32 * 32;
+        const float *ex_recv = reinterpret_cast<const float *>(smem + S::EX_OFF) + (g * 4 + (q ^ 2)) * 32 * 32;
+        const uint32_t pair_bar = 1u + (uint32_t)(2 * g + (q & 1));        // named barrier of warps q, q ^ 2
         uint32_t dph = 0;
         bool ok = true;
+
+        // W13: columns c0 .. c0+63 are features 128*nb + c0/2 + 0..31 (column groups c0/32 and c0/32 + 1),
+        // one W2 K-block: SiLU(gate)*up, its block maximum and its NT terms; the terms' scale bytes are
+        // returned in sb
+        auto w13_chunk = [&](const Tile &tl, int64_t row, int c0, const uint32_t (&a0)[32], const uint32_t (&a1)[32],
+                             uint32_t (&sb)[NT]) {
+            const float L = p.swiglu_limit;
+            float h[32];
+            float mx = 0.f;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                float gt = __uint_as_float(a0[i]), up = __uint_as_float(a0[16 + i]);
+                float gt2 = __uint_as_float(a1[i]), up2 = __uint_as_float(a1[16 + i]);
+                if (L > 0.f) {
+                    gt = fminf(gt, L);
+                    up = fminf(fmaxf(up, -L), L);
+                    gt2 = fminf(gt2, L);
+                    up2 = fminf(fmaxf(up2, -L), L);
+                }
+                h[i] = silu_f(gt) * up;
+                h[16 + i] = silu_f(gt2) * up2;
+                mx = fmaxf(mx, fmaxf(fabsf(h[i]), fabsf(h[16 + i])));
+            }
+            const int e1 = mxfp8_block_exp(mx);
+            const int blk = c0 >> 6;                   // K-block of the slab (0..3)
+#pragma unroll
+            for (int t = 0; t < NT; ++t) {
+                uint32_t w[8];
+                sb[t] = 0;
+#pragma unroll
+                for (int z = 0; z < 8; ++z) {
+                    const uint32_t lo = mxfp8_term_pair(h[4 * z], h[4 * z + 1], e1, t, sb[t]);
+                    const uint32_t hi = mxfp8_term_pair(h[4 * z + 2], h[4 * z + 3], e1, t, sb[t]);
+                    w[z] = lo | (hi << 16);
+                }
+                ptx::st_global_v8(p.hq + (((int64_t)tl.mb * NT + t) * p.rows_cap + row) * 128 + blk * 32, w);
+            }
+        };
+        // W2: 256 contiguous bytes of the pair's staging row, in 32-byte stores (the combine reads them
+        // back once, after the whole launch)
+        auto w2_chunk = [&](const Tile &tl, int pair, int c0, const uint32_t (&a0)[32], const uint32_t (&a1)[32]) {
+            float *dst = p.staging + (int64_t)pair * p.H + (int64_t)tl.mb * C::TN + c0;
+#pragma unroll
+            for (int z = 0; z < 4; ++z) {
+                uint32_t v[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) v[u] = a0[8 * z + u];
+                ptx::st_global_v8_stream(dst + 8 * z, v);
+            }
+#pragma unroll
+            for (int z = 0; z < 4; ++z) {
+                uint32_t v[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) v[u] = a1[8 * z + u];
+                ptx::st_global_v8_stream(dst + 32 + 8 * z, v);
+            }
+        };
+
         for (int j = 0; j < my_tiles; ++j) {
             const Tile tl = tile_of(j);
             ok = ok && __all_sync(0xFFFFFFFFu, ptx::mbar_wait(d_full, dph, s_abort, LIM));
@@ -377,84 +465,88 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_rows_kernel(const __gr
                     pair = -1;
                 }
             }
-            uint32_t sbytes[NT] = {0u, 0u};                 // W13: this warp's two scale bytes per term
-            for (int ch = 0; ch < 2; ++ch) {
-                const int c0 = 128 * g + 64 * ch;            // first column of the chunk
+            if constexpr (C::STACK) {
+                const int ch = q >> 1, c0 = 128 * g + 64 * ch, cs = 128 * g + 64 * (ch ^ 1);
                 uint32_t a0[32], a1[32];
-                __syncwarp();                                // the loads below are warp-collective
-                if (ok) {
-                    ptx::tmem_ld_32x32b_x32(tmem + t_lane + (uint32_t)c0, a0);
-                    ptx::tmem_ld_32x32b_x32(tmem + t_lane + (uint32_t)(c0 + 32), a1);
-                    ptx::tmem_wait_ld();
-                } else {
+                // round r: the partner's columns cs + 32r go into this warp's slot (column-major,
+                // lane-consecutive words), this warp's own columns c0 + 32r come from TMEM, and the
+                // partner's term is added from its slot
+                auto exchange_round = [&](int r, uint32_t (&own)[32]) {
+                    __syncwarp();                            // the loads below are warp-collective
+                    if (ok) {
+                        uint32_t snd[32];
+                        ptx::tmem_ld_32x32b_x32(tmem + t_lane + (uint32_t)(cs + 32 * r), snd);
+                        ptx::tmem_wait_ld();
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) a0[i] = a1[i] = 0u;
-                }
-                if (ch == 1) {                                // the accumulator has been read
-                    ptx::tc_fence_before();
-                    __syncwarp();
-                    if (ok && lane == 0) ptx::mbar_arrive(d_empty);
-                }
-                if (!ok || !row_ok) continue;               // (re-converges at the __syncwarp above)
-                if (MODE == 0) {
-                    // features 128*nb + c0/2 + 0..31 (column groups c0/32 and c0/32 + 1): one W2 K-block
-                    const float L = p.swiglu_limit;
-                    float h[32];
-                    float mx = 0.f;
+                        for (int i = 0; i < 32; ++i) ex_send[i * 32 + lane] = __uint_as_float(snd[i]);
+                        ptx::tmem_ld_32x32b_x32(tmem + t_lane + (uint32_t)(c0 + 32 * r), own);
+                        ptx::tmem_wait_ld();
+                    } else {
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        float gt = __uint_as_float(a0[i]), up = __uint_as_float(a0[16 + i]);
-                        float gt2 = __uint_as_float(a1[i]), up2 = __uint_as_float(a1[16 + i]);
-                        if (L > 0.f) {
-                            gt = fminf(gt, L);
-                            up = fminf(fmaxf(up, -L), L);
-                            gt2 = fminf(gt2, L);
-                            up2 = fminf(fmaxf(up2, -L), L);
-                        }
-                        h[i] = silu_f(gt) * up;
-                        h[16 + i] = silu_f(gt2) * up2;
-                        mx = fmaxf(mx, fmaxf(fabsf(h[i]), fabsf(h[16 + i])));
+                        for (int i = 0; i < 32; ++i) own[i] = 0u;
                     }
-                    const int e1 = mxfp8_block_exp(mx);
-                    const int blk = c0 >> 6;                   // K-block of the slab (0..3)
+                    if (r == 1) {                            // the accumulator has been read
+                        ptx::tc_fence_before();
+                        __syncwarp();
+                        if (ok && lane == 0) ptx::mbar_arrive(d_empty);
+                    }
+                    ptx::bar_sync_n(pair_bar, 64);          // the partner's partial sums are in its slot
+                    if (ok) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            own[i] = __float_as_uint(__uint_as_float(own[i]) + ex_recv[i * 32 + lane]);
+                    }
+                    ptx::bar_sync_n(pair_bar, 64);          // both slots read: they may be refilled
+                };
+                exchange_round(0, a0);
+                exchange_round(1, a1);
+                if (ok && row_ok) {
+                    if (MODE == 0) {
+                        uint32_t sb[NT];
+                        w13_chunk(tl, row, c0, a0, a1, sb);
+#pragma unroll
+                        for (int t = 0; t < NT; ++t)         // byte 2g + ch of the row's scale word per term
+                            p.hs[(((int64_t)tl.mb * NT + t) * p.rows_sf + row) * 4 + 2 * g + ch] = (uint8_t)sb[t];
+                    } else if (pair >= 0) {
+                        w2_chunk(tl, pair, c0, a0, a1);
+                    }
+                }
+            } else {
+                uint32_t sbytes[NT] = {0u, 0u};             // W13: this warp's two scale bytes per term
+                for (int ch = 0; ch < 2; ++ch) {
+                    const int c0 = 128 * g + 64 * ch;        // first column of the chunk
+                    uint32_t a0[32], a1[32];
+                    __syncwarp();                            // the loads below are warp-collective
+                    if (ok) {
+                        ptx::tmem_ld_32x32b_x32(tmem + t_lane + (uint32_t)c0, a0);
+                        ptx::tmem_ld_32x32b_x32(tmem + t_lane + (uint32_t)(c0 + 32), a1);
+                        ptx::tmem_wait_ld();
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) a0[i] = a1[i] = 0u;
+                    }
+                    if (ch == 1) {                            // the accumulator has been read
+                        ptx::tc_fence_before();
+                        __syncwarp();
+                        if (ok && lane == 0) ptx::mbar_arrive(d_empty);
+                    }
+                    if (!ok || !row_ok) continue;           // (re-converges at the __syncwarp above)
+                    if (MODE == 0) {
+                        uint32_t sb[NT];
+                        w13_chunk(tl, row, c0, a0, a1, sb);
+#pragma unroll
+                        for (int t = 0; t < NT; ++t) sbytes[t] |= sb[t] << (8 * ch);
+                    } else if (pair >= 0) {
+                        w2_chunk(tl, pair, c0, a0, a1);
+                    }
+                }
+                if (MODE == 0 && ok && row_ok) {
+                    // K-blocks 2g and 2g + 1 of slab nb: bytes 2g, 2g + 1 of the row's scale word per term
 #pragma unroll
                     for (int t = 0; t < NT; ++t) {
-                        uint32_t w[8], sb = 0;
-#pragma unroll
-                        for (int z = 0; z < 8; ++z) {
-                            const uint32_t lo = mxfp8_term_pair(h[4 * z], h[4 * z + 1], e1, t, sb);
-                            const uint32_t hi = mxfp8_term_pair(h[4 * z + 2], h[4 * z + 3], e1, t, sb);
-                            w[z] = lo | (hi << 16);
-                        }
-                        ptx::st_global_v8(p.hq + (((int64_t)tl.mb * NT + t) * p.rows_cap + row) * 128 + blk * 32, w);
-                        sbytes[t] |= sb << (8 * ch);
+                        uint16_t *ds = reinterpret_cast<uint16_t *>(p.hs + (((int64_t)tl.mb * NT + t) * p.rows_sf + row) * 4) + g;
+                        *ds = (uint16_t)sbytes[t];
                     }
-                } else if (pair >= 0) {
-                    // 256 contiguous bytes of the pair's staging row per chunk, in 32-byte stores (the
-                    // combine reads them back once, after the whole launch)
-                    float *dst = p.staging + (int64_t)pair * p.H + (int64_t)tl.mb * C::TN + c0;
-#pragma unroll
-                    for (int z = 0; z < 4; ++z) {
-                        uint32_t v[8];
-#pragma unroll
-                        for (int u = 0; u < 8; ++u) v[u] = a0[8 * z + u];
-                        ptx::st_global_v8_stream(dst + 8 * z, v);
-                    }
-#pragma unroll
-                    for (int z = 0; z < 4; ++z) {
-                        uint32_t v[8];
-#pragma unroll
-                        for (int u = 0; u < 8; ++u) v[u] = a1[8 * z + u];
-                        ptx::st_global_v8_stream(dst + 32 + 8 * z, v);
-                    }
-                }
-            }
-            if (MODE == 0 && ok && row_ok) {
-                // K-blocks 2g and 2g + 1 of slab nb: bytes 2g, 2g + 1 of the row's scale word per term
-#pragma unroll
-                for (int t = 0; t < NT; ++t) {
-                    uint16_t *ds = reinterpret_cast<uint16_t *>(p.hs + (((int64_t)tl.mb * NT + t) * p.rows_sf + row) * 4) + g;
-                    *ds = (uint16_t)sbytes[t];
                 }
             }
             dph ^= 1u;
@@ -485,8 +577,9 @@ cudaError_t launch_rows(const GemmParams &p, int grid, cudaStream_t s, bool pdl)
 
 }  // namespace
 
-cudaError_t launch_gemm_rows(const GemmParams &p, int mode, int grid, cudaStream_t s, bool pdl)
+cudaError_t launch_gemm_rows(const GemmParams &p, int mode, bool stacked, int grid, cudaStream_t s, bool pdl)
 {
+    if (stacked) return mode == 0 ? launch_rows<W13Rows64>(p, grid, s, pdl) : launch_rows<W2Rows64>(p, grid, s, pdl);
     return mode == 0 ? launch_rows<W13Rows>(p, grid, s, pdl) : launch_rows<W2Rows>(p, grid, s, pdl);
 }
 

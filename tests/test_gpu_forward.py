@@ -286,6 +286,31 @@ def test_forward_fuzz_shapes(gpu_lib, gpu_layers, T, H, I, E, k):
     _compare(f"fuzz {T}x{H}x{I} E{E} k{k}", r["y"].cpu().numpy(), oracle.forward(L, ids_r, w_r))
 
 
+@pytest.mark.parametrize("block_m", [16, 64])
+@pytest.mark.parametrize("T,H,I,E,k,limit,zipf", [
+    (1200, 512, 256, 64, 2, 0.0, False),      # 37.5 rows per expert
+    (500, 256, 384, 16, 2, 10.0, False),      # 62.5 rows per expert (some above 64: two token blocks), clamp,
+                                              # three 256-row W13 blocks
+    (40, 256, 256, 1, 1, 0.0, False),         # one expert, k = 1
+    (2000, 256, 128, 1024, 16, 0.0, False),   # 1,024 experts, 31 rows each
+    (1500, 512, 256, 128, 4, 0.0, True),      # skewed routing: hot experts hold several token blocks
+])
+def test_forward_stacked_token_tiles(gpu_lib, gpu_layers, T, H, I, E, k, limit, zipf, block_m):
+    """17 to 64 rows per expert with H a multiple of 256 selects the token-major tiles of 64 token rows
+    whose two activation terms are stacked as the MMA's 128 A rows (paired epilogue warps add the
+    halves): every output against the oracle, with partial token blocks, rows of the next expert inside
+    a block, the clamp, one expert and more than 512 experts."""
+    moe = gpu_lib
+    assert 16 < T * k / E <= 64 or zipf
+    L = synth.make_layer(T=T, H=H, E=E, k=k, I=I, zipf_bias=zipf, seed=T + 7 * H)
+    r = _run_layer(moe, gpu_layers, L, block_m=block_m, swiglu_limit=limit)
+    assert moe.forward_plan(r["desc"])["regime"] == "mid"
+    ids_r, w_r, _ = oracle.route(L["logits"], k)
+    assert np.array_equal(r["ids"].cpu().numpy(), ids_r)
+    _compare(f"stacked {T}x{H}x{I} E{E} k{k} L{limit} bm{block_m}{' zipf' if zipf else ''}", r["y"].cpu().numpy(),
+             oracle.forward(L, ids_r, w_r, swiglu_limit=limit))
+
+
 @pytest.mark.parametrize("block_m", [16, 128])
 @pytest.mark.parametrize("T,H,I,E,k,limit", [(1200, 512, 256, 16, 4, 0.0),   # 300 rows per expert: 3 token blocks
                                              (1000, 256, 384, 5, 3, 10.0),   # 600 rows per expert, clamp, I/128 odd
