@@ -64,6 +64,29 @@ __device__ __forceinline__ Tile decode_tile(int t, const int *tile_start, int E,
     return r;
 }
 
+// decode_tile with the expert's row count and first padded row read from the permutation offsets in
+// global memory (for kernels that keep only the tile prefix in shared memory)
+template <int NMAX>
+__device__ __forceinline__ Tile decode_tile_g(int t, const int *tile_start, int E, int MB, const int32_t *offsets,
+                                              const int32_t *padded)
+{
+    int lo = 0, hi = E - 1;                 // largest e with tile_start[e] <= t
+    while (lo < hi) {
+        int mid = (lo + hi + 1) >> 1;
+        if (tile_start[mid] <= t) lo = mid; else hi = mid - 1;
+    }
+    Tile r;
+    r.e = lo;
+    int local = t - tile_start[lo];
+    int nb = local / MB;
+    r.mb = local - nb * MB;
+    int rem = (__ldg(offsets + lo + 1) - __ldg(offsets + lo)) - nb * NMAX;
+    int n = rem < NMAX ? rem : NMAX;
+    r.n = (n + 15) & ~15;
+    r.row0 = __ldg(padded + lo) + nb * NMAX;
+    return r;
+}
+
 // SiLU(g) = g / (1 + e^-g) with the fast exp and divide (about 1e-6 relative error, far below the 8
 // bits h keeps in its two terms). For g < -88, e^-g is +inf and the quotient is -0.
 __device__ __forceinline__ float silu_f(float g) { return __fdividef(g, 1.0f + __expf(-g)); }

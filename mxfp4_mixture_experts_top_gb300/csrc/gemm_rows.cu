@@ -77,8 +77,8 @@ static_assert(NTH_HUGE == 2 && NT_X == 2, "the token-major tiles take two terms 
 
 using W13Rows = RCfg<0, 3, 3, 4, 1024>;
 using W2Rows = RCfg<1, 3, 3, 4, 1024>;
-using W13Rows64 = RCfg<0, 4, 3, 4, 1024, true>;
-using W2Rows64 = RCfg<1, 4, 3, 4, 1024, true>;
+using W13Rows64 = RCfg<0, 4, 4, 4, 1024, true>;
+using W2Rows64 = RCfg<1, 4, 4, 4, 1024, true>;
 
 template <class C>
 struct RSmem {
@@ -91,14 +91,15 @@ struct RSmem {
     static constexpr int W_OFF = X_OFF + C::NX * XSTAGE;
     static constexpr int XS_OFF = W_OFF + C::NW * WSTAGE;
     static constexpr int WS_OFF = XS_OFF + C::NX * XSSTAGE;
-    // stacked tiles: per epilogue warp 32 columns x 32 lanes of fp32 partial sums for its partner
+    // stacked tiles: per epilogue warp 16 columns x 32 lanes of fp32 partial sums for its partner
     static constexpr int EX_OFF = WS_OFF + C::NW * WSSTAGE;
-    static constexpr int EX_BYTES = C::STACK ? 8 * 32 * 32 * 4 : 0;
+    static constexpr int EX_BYTES = C::STACK ? 8 * 16 * 32 * 4 : 0;
     static constexpr int BAR_OFF = EX_OFF + EX_BYTES;
     static constexpr int NBARS = C::NW + C::NX + C::NSF + C::ND + 3;
     static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;
     static constexpr int PREFIX_OFF = MISC_OFF + 16;
-    static constexpr size_t bytes(int E) { return 1024 + PREFIX_OFF + sizeof(int) * (size_t)(3 * E + 1 + 32); }
+    // the tile prefix [E + 1] and the scan scratch [32] (an expert's rows are read from global memory)
+    static constexpr size_t bytes(int E) { return 1024 + PREFIX_OFF + sizeof(int) * (size_t)(E + 1 + 32); }
     static_assert(XSTAGE % 1024 == 0 && WSTAGE % 1024 == 0, "stages keep the 1024-byte swizzle alignment");
     static_assert(bytes(C::EMAX) <= 232448, "shared memory per CTA");
 };
@@ -122,7 +123,6 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_rows_kernel(const __gr
     volatile int *s_abort = reinterpret_cast<volatile int *>(smem + S::MISC_OFF + 4);
     int *tile_start = reinterpret_cast<int *>(smem + S::PREFIX_OFF);
     int *scan_tmp = tile_start + p.E + 1;
-    int *s_pad0 = scan_tmp + 32, *s_cnt = s_pad0 + p.E;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int E = p.E, NBT = p.MB / 2;     // 256-row weight blocks per expert
@@ -135,10 +135,6 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_rows_kernel(const __gr
         for (int q = 0; q < 2; ++q) {
             const int e = tid * 2 + q;
             const int cnt = e < E ? (__ldg(p.offsets + e + 1) - __ldg(p.offsets + e)) : 0;
-            if (e < E) {
-                s_cnt[e] = cnt;
-                s_pad0[e] = __ldg(p.padded + e);
-            }
             v[q] = (cnt + TM - 1) / TM * NBT;
             s += v[q];
         }
@@ -208,7 +204,9 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_rows_kernel(const __gr
     auto wait_done = [&](int q) -> bool {
         return q < 0 || ptx::mbar_wait(&done[q % C::ND], (uint32_t)((q / C::ND) & 1), s_abort, LIM);
     };
-    auto tile_of = [&](int j) { return decode_tile<TM>((int)blockIdx.x + j * (int)gridDim.x, tile_start, E, NBT, s_cnt, s_pad0); };
+    auto tile_of = [&](int j) {
+        return decode_tile_g<TM>((int)blockIdx.x + j * (int)gridDim.x, tile_start, E, NBT, p.offsets, p.padded);
+    };
 
     if (warp == 10) {
         // ===================== weight producer: per slab the two 128-row weight tiles' E2M1 slabs (one
@@ -383,13 +381,13 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_rows_kernel(const __gr
         // warps 0-3, 1 for warps 12-15) in two chunks of 64. Token-row tiles: lane quarter q is token rows
         // 32q .. 32q+31 and the warp finishes both chunks. Stacked tiles: quarters 0-1 hold term 0 of token
         // rows 0-63 and quarters 2-3 term 1 of the same rows, so warps q and q ^ 2 hold the two halves of
-        // the same sums: each sends the partner its partial sums of one chunk through shared memory, in two
-        // rounds of 32 columns, and finishes the other (chunk q >> 1), term 0 + term 1 in both.
+        // the same sums: each sends the partner its partial sums of one chunk through shared memory, in four
+        // rounds of 16 columns, and finishes the other (chunk q >> 1), term 0 + term 1 in both.
         const int q = warp & 3, g = warp >= 12 ? 1 : 0;
         const uint32_t t_lane = (uint32_t)(q * 32) << 16;
         const int trow = C::STACK ? (q & 1) * 32 + lane : q * 32 + lane;   // token row in the tile
-        float *ex_send = reinterpret_cast<float *>(smem + S::EX_OFF) + (g * 4 + q) * 32 * 32;
-        const float *ex_recv = reinterpret_cast<const float *>(smem + S::EX_OFF) + (g * 4 + (q ^ 2)) * 32 * 32;
+        float *ex_send = reinterpret_cast<float *>(smem + S::EX_OFF) + (g * 4 + q) * 16 * 32;
+        const float *ex_recv = reinterpret_cast<const float *>(smem + S::EX_OFF) + (g * 4 + (q ^ 2)) * 16 * 32;
         const uint32_t pair_bar = 1u + (uint32_t)(2 * g + (q & 1));        // named barrier of warps q, q ^ 2
         uint32_t dph = 0;
         bool ok = true;
@@ -468,24 +466,24 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_rows_kernel(const __gr
             if constexpr (C::STACK) {
                 const int ch = q >> 1, c0 = 128 * g + 64 * ch, cs = 128 * g + 64 * (ch ^ 1);
                 uint32_t a0[32], a1[32];
-                // round r: the partner's columns cs + 32r go into this warp's slot (column-major,
-                // lane-consecutive words), this warp's own columns c0 + 32r come from TMEM, and the
+                // round r: the partner's columns cs + 16r go into this warp's slot (column-major,
+                // lane-consecutive words), this warp's own columns c0 + 16r come from TMEM, and the
                 // partner's term is added from its slot
-                auto exchange_round = [&](int r, uint32_t (&own)[32]) {
+                auto exchange_round = [&](int r, uint32_t (&own)[16]) {
                     __syncwarp();                            // the loads below are warp-collective
                     if (ok) {
-                        uint32_t snd[32];
-                        ptx::tmem_ld_32x32b_x32(tmem + t_lane + (uint32_t)(cs + 32 * r), snd);
+                        uint32_t snd[16];
+                        ptx::tmem_ld_32x32b_x16(tmem + t_lane + (uint32_t)(cs + 16 * r), snd);
                         ptx::tmem_wait_ld();
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) ex_send[i * 32 + lane] = __uint_as_float(snd[i]);
-                        ptx::tmem_ld_32x32b_x32(tmem + t_lane + (uint32_t)(c0 + 32 * r), own);
+                        for (int i = 0; i < 16; ++i) ex_send[i * 32 + lane] = __uint_as_float(snd[i]);
+                        ptx::tmem_ld_32x32b_x16(tmem + t_lane + (uint32_t)(c0 + 16 * r), own);
                         ptx::tmem_wait_ld();
                     } else {
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) own[i] = 0u;
+                        for (int i = 0; i < 16; ++i) own[i] = 0u;
                     }
-                    if (r == 1) {                            // the accumulator has been read
+                    if (r == 3) {                            // the accumulator has been read
                         ptx::tc_fence_before();
                         __syncwarp();
                         if (ok && lane == 0) ptx::mbar_arrive(d_empty);
@@ -493,13 +491,15 @@ __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_rows_kernel(const __gr
                     ptx::bar_sync_n(pair_bar, 64);          // the partner's partial sums are in its slot
                     if (ok) {
 #pragma unroll
-                        for (int i = 0; i < 32; ++i)
+                        for (int i = 0; i < 16; ++i)
                             own[i] = __float_as_uint(__uint_as_float(own[i]) + ex_recv[i * 32 + lane]);
                     }
                     ptx::bar_sync_n(pair_bar, 64);          // both slots read: they may be refilled
                 };
-                exchange_round(0, a0);
-                exchange_round(1, a1);
+                exchange_round(0, *reinterpret_cast<uint32_t (*)[16]>(a0));
+                exchange_round(1, *reinterpret_cast<uint32_t (*)[16]>(a0 + 16));
+                exchange_round(2, *reinterpret_cast<uint32_t (*)[16]>(a1));
+                exchange_round(3, *reinterpret_cast<uint32_t (*)[16]>(a1 + 16));
                 if (ok && row_ok) {
                     if (MODE == 0) {
                         uint32_t sb[NT];
