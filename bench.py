@@ -99,12 +99,21 @@ KERNEL_NAMES = {"w13": "moe_gemm_kernel<W13*> (grouped W13 GEMM + SiLU*up + h te
                 "gemms": "moe_gemm_decode_kernel (W13 GEMM + SiLU*up + h terms, then W2: one persistent launch)"}
 ROWS_KERNEL_NAMES = {"w13": "moe_gemm_rows_kernel<W13Rows> (token-major grouped W13 GEMM + SiLU*up + h terms)",
                      "w2": "moe_gemm_rows_kernel<W2Rows> (token-major grouped W2 GEMM)"}
+ROWS64_KERNEL_NAMES = {"w13": "moe_gemm_rows_kernel<W13Rows64> (token-major, 64 token rows x 2 stacked terms; grouped "
+                              "W13 GEMM + SiLU*up + h terms)",
+                       "w2": "moe_gemm_rows_kernel<W2Rows64> (token-major, 64 token rows x 2 stacked terms; grouped "
+                             "W2 GEMM)"}
 
 
-def kernel_names(plan):
+def kernel_names(plan, H):
     """Names of the GEMM kernels the library launches for a layer, from its forward plan: token-major
-    tiles in the "huge" regime, weight-major tiles otherwise (one fused launch where the plan says so)."""
-    return ROWS_KERNEL_NAMES if plan["regime"] == "huge" else KERNEL_NAMES
+    tiles in the "huge" regime, stacked token-major tiles in the "mid" regime when H is a multiple of 256,
+    weight-major tiles otherwise (one fused launch where the plan says so)."""
+    if plan["regime"] == "huge":
+        return ROWS_KERNEL_NAMES
+    if plan["regime"] == "mid" and H % 256 == 0:
+        return ROWS64_KERNEL_NAMES
+    return KERNEL_NAMES
 
 
 def kernel_roofline(name, key, alg, ms, peaks, names=KERNEL_NAMES):
@@ -490,10 +499,10 @@ def measure_config(moe, name, L, steps, warmup, flush_buf, peaks):
         "forward_plan": plan,
     }
     if plan["fused_gemms"]:
-        out["gemms_roofline"] = kernel_roofline(name, "gemms", a, pk["gemms"], peaks, kernel_names(plan))
+        out["gemms_roofline"] = kernel_roofline(name, "gemms", a, pk["gemms"], peaks, kernel_names(plan, L["H"]))
     else:
-        out["w13_roofline"] = kernel_roofline(name, "w13", a, pk["w13"], peaks, kernel_names(plan))
-        out["w2_roofline"] = kernel_roofline(name, "w2", a, pk["w2"], peaks, kernel_names(plan))
+        out["w13_roofline"] = kernel_roofline(name, "w13", a, pk["w13"], peaks, kernel_names(plan, L["H"]))
+        out["w2_roofline"] = kernel_roofline(name, "w2", a, pk["w2"], peaks, kernel_names(plan, L["H"]))
     return out, lay, a
 
 
@@ -552,13 +561,13 @@ def run_ours(args, world, rank, local):
     nt_x, nt_h = term_counts(moe, layer.desc)
     alg = algorithmic(L, ids, nt_x, nt_h)
     if plan["fused_gemms"]:
-        roofline = kernel_roofline(args.workload, "gemms", alg, per_kernel["gemms"], peaks, kernel_names(plan))
+        roofline = kernel_roofline(args.workload, "gemms", alg, per_kernel["gemms"], peaks, kernel_names(plan, L["H"]))
         other = None
     else:
         dominant = "w13" if per_kernel["w13"] >= per_kernel["w2"] else "w2"
-        roofline = kernel_roofline(args.workload, dominant, alg, per_kernel[dominant], peaks, kernel_names(plan))
+        roofline = kernel_roofline(args.workload, dominant, alg, per_kernel[dominant], peaks, kernel_names(plan, L["H"]))
         other = kernel_roofline(args.workload, "w2" if dominant == "w13" else "w13", alg,
-                                per_kernel["w2" if dominant == "w13" else "w13"], peaks, kernel_names(plan))
+                                per_kernel["w2" if dominant == "w13" else "w13"], peaks, kernel_names(plan, L["H"]))
     layer_gbs = alg["layer_bytes"] / (ms_per_step / 1e3) / 1e9
     layer_tflops = alg["flops"] / (ms_per_step / 1e3) / 1e12
 

@@ -289,9 +289,11 @@ moe_status_t moe_mxfp4_workspace_layout(const moe_layer_desc *desc, size_t out[7
  * What moe_mxfp4_forward launches for desc (no device work; only the shape,
  * flags and out_dtype of desc matter). out[0]: the GEMM tile regime, by
  * average rows per expert T*k/E: 0 up to 2 (weight tiles of 16 token rows),
- * 1 up to 16 (32 rows), 2 up to 64 (64 rows), 3 above 64 with H not a
- * multiple of 256 (96 rows), 4 above 64 with H a multiple of 256 (token-major
- * tiles of 128 rows x 256 weight rows). out[1]: 1 when W13 and W2 run as one
+ * 1 up to 16 (32 rows), 2 up to 64 (64 token rows: token-major tiles whose
+ * two activation terms are stacked as the MMA's 128 rows against 256 weight
+ * rows when H is a multiple of 256, else weight-major tiles), 3 above 64 with
+ * H not a multiple of 256 (96 rows), 4 above 64 with H a multiple of 256
+ * (token-major tiles of 128 rows x 256 weight rows). out[1]: 1 when W13 and W2 run as one
  * persistent launch (regime 0 with E <= 512, H and I multiples of 256 and at
  * least 512): each expert's W2 tiles start once its W13 tiles have stored
  * their h rows, tracked by per-expert counters in the workspace. out[2]: 1

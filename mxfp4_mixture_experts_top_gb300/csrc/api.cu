@@ -409,6 +409,14 @@ moe_status_t moe_mxfp4_forward_timed(const moe_layer_desc *d, const uint16_t *d_
     if (!get_map(&a.tmap_xs1, 2, a.xs, (uint64_t)a.rows_sf, NT_X, s13, n13, 1, &st)) return st;
     if (!get_map(&a.tmap_hs, 2, a.hs, (uint64_t)a.rows_sf, NT_H, s2, n2, sps, &st)) return st;
     if (!get_map(&a.tmap_hs1, 2, a.hs, (uint64_t)a.rows_sf, NT_H, s2, n2, 1, &st)) return st;
+    // at most 8 tokens: no expert holds more than 8 rows, and the fused decode GEMMs take 8-row tiles
+    a.rows8 = d->T <= 8 && a.regime == Regime::Tiny;
+    if (a.rows8) {
+        if (!get_map(&a.tmap_xq8, 1, a.xq, (uint64_t)d->H, (uint64_t)R, NT_X, 8, sps, &st)) return st;
+        if (!get_map(&a.tmap_hq8, 1, a.hq, (uint64_t)d->I, (uint64_t)R, NT_H, 8, sps, &st)) return st;
+        if (!get_map(&a.tmap_xs8, 2, a.xs, (uint64_t)a.rows_sf, NT_X, s13, 8, sps, &st)) return st;
+        if (!get_map(&a.tmap_hs8, 2, a.hs, (uint64_t)a.rows_sf, NT_H, s2, 8, sps, &st)) return st;
+    }
     // the first kernel of the forward clears the device error word (a memset here would break the
     // programmatic-dependent-launch chain between the permutation and the gather)
     return from_cuda(launch_forward(a, s));

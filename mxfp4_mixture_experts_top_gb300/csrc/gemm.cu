@@ -1074,7 +1074,13 @@ cudaError_t launch_forward(const ForwardArgs &a, cudaStream_t s)
         g2.wsf = a.packed + packed_w13_bytes(a.E, a.H, a.I) + (size_t)a.E * a.H * (a.I / 2);
         g2.K = a.I;
         g2.MB = a.H / TILE_ROWS;
-        err = launch_gemm_decode(g, g2, a.done13, fast, a.num_sms, s, pdl);
+        if (a.rows8) {                 // at most 8 tokens: 8-row tiles (no expert holds more rows)
+            g.tm_b = a.tmap_xq8;
+            g.tm_bs = a.tmap_xs8;
+            g2.tm_b = a.tmap_hq8;
+            g2.tm_bs = a.tmap_hs8;
+        }
+        err = launch_gemm_decode(g, g2, a.done13, fast, a.rows8, a.num_sms, s, pdl);
         if (err != cudaSuccess) return err;
     }
     err = fused               ? cudaSuccess

@@ -91,12 +91,12 @@ __device__ __forceinline__ Tile decode_tile_g(int t, const int *tile_start, int 
 // bits h keeps in its two terms). For g < -88, e^-g is +inf and the quotient is -0.
 __device__ __forceinline__ float silu_f(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
 
-// The decode GEMMs (16-row tiles, at most 2 rows per expert) as one persistent launch (gemm_decode.cu):
+// The decode GEMMs (16-row tiles, 8-row with rows8, at most 2 rows per expert) as one persistent launch (gemm_decode.cu):
 // W13 tiles, then W2 tiles, each W2 tile of an expert after that expert's W13 tiles (counters done13[E],
 // zeroed by the caller before). decode_fused_supported: the shapes it takes.
 bool decode_fused_supported(int H, int I, int E);
-cudaError_t launch_gemm_decode(const GemmParams &g13, const GemmParams &g2, uint32_t *done13, bool fast, int grid,
-                               cudaStream_t s, bool pdl);
+cudaError_t launch_gemm_decode(const GemmParams &g13, const GemmParams &g2, uint32_t *done13, bool fast, bool rows8,
+                               int grid, cudaStream_t s, bool pdl);
 
 // Token-major tiles for large batches (gemm_rows.cu): 128 token rows x 256 weight rows per tile.
 // MODE 0: W13, MODE 1: W2. p.MB must be even.

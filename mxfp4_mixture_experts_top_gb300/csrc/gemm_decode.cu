@@ -43,10 +43,13 @@ namespace moe {
 
 namespace {
 
+// NMAX token rows per tile: 16, or 8 when no expert can hold more (at most 8 tokens), which halves
+// the activation stages and leaves room for a sixth weight stage.
+template <int NMAX_>
 struct DCfg {
-    static constexpr int NMAX = 16, NT = 2, NP = NT * NMAX;   // token rows per tile, terms, MMA N
-    static constexpr int SPS = 2;                              // slabs per stage
-    static constexpr int NA = 5, NB = 4, NSF = 6, MW = 2, ND = 8, EMAX = 512;
+    static constexpr int NMAX = NMAX_, NT = 2, NP = NT * NMAX;   // token rows per tile, terms, MMA N
+    static constexpr int SPS = 2;                                 // slabs per stage
+    static constexpr int NA = NMAX == 8 ? 6 : 5, NB = 4, NSF = 6, MW = 2, ND = 8, EMAX = 512;
     static constexpr int SF_COLS = 8;                          // one slab's cell: A (4 columns), B (1), pad
     static constexpr int CELL_COLS = SPS * SF_COLS;
     static constexpr int D_COLS = NP;                          // one accumulator set
@@ -56,8 +59,8 @@ struct DCfg {
     static_assert(NA <= ND && NB <= ND && NSF <= ND, "done ring");
 };
 
+template <class C>
 struct DSmem {
-    using C = DCfg;
     static constexpr int ASTAGE = C::SPS * SLAB_SMEM_BYTES;   // expanded E2M1 slabs
     static constexpr int BSLAB = C::NP * 128;                 // [term][row][128 K bytes]
     static constexpr int BSTAGE = C::SPS * BSLAB;
@@ -77,7 +80,8 @@ struct DSmem {
     static constexpr size_t bytes(int E) { return 1024 + PREFIX_OFF + sizeof(int) * (size_t)(4 * E + 2 + 32); }
     static_assert(BSLAB % 1024 == 0 && ASTAGE % 1024 == 0, "stages keep the 1024-byte swizzle alignment");
 };
-static_assert(DSmem::bytes(DCfg::EMAX) <= 232448, "shared memory per CTA");
+static_assert(DSmem<DCfg<16>>::bytes(DCfg<16>::EMAX) <= 232448, "shared memory per CTA");
+static_assert(DSmem<DCfg<8>>::bytes(DCfg<8>::EMAX) <= 232448, "shared memory per CTA");
 
 struct DecodeParams {
     GemmParams g13, g2;    // W13 (x terms in, h terms out) and W2 (h terms in, staging or y out)
@@ -94,11 +98,10 @@ struct DTile {
 
 namespace {
 
-template <bool FAST>
-__global__ void __launch_bounds__(DCfg::THREADS, 1) moe_gemm_decode_kernel(const __grid_constant__ DecodeParams dp)
+template <class C, bool FAST>
+__global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_decode_kernel(const __grid_constant__ DecodeParams dp)
 {
-    using C = DCfg;
-    using S = DSmem;
+    using S = DSmem<C>;
     constexpr int NMAX = C::NMAX, NT = C::NT, NP = C::NP, SPS = C::SPS;
     const GemmParams &p13 = dp.g13;
     const GemmParams &p2 = dp.g2;
@@ -328,7 +331,8 @@ __global__ void __launch_bounds__(DCfg::THREADS, 1) moe_gemm_decode_kernel(const
                 for (int pos = 0; pos < SPS; ++pos) {
                     const uint4 aw = *reinterpret_cast<const uint4 *>(sfring + ai * S::SFSTAGE + pos * SLAB_SF_BYTES + lane * 16);
                     const uint32_t *bs = reinterpret_cast<const uint32_t *>(bsring + bi * S::BSSTAGE + pos * S::BSSLAB);
-                    const uint32_t v8[8] = {aw.x, aw.y, aw.z, aw.w, bs[lane], 0u, 0u, 0u};   // B row j = lane (NP = 32)
+                    const uint32_t bw = lane < NP ? bs[lane] : 0u;                          // B row j = lane
+                    const uint32_t v8[8] = {aw.x, aw.y, aw.z, aw.w, bw, 0u, 0u, 0u};
                     ptx::tmem_st_32x32b_x8(tmem + quarter + (uint32_t)(C::SF_BASE + sc * C::CELL_COLS + pos * C::SF_COLS), v8);
                 }
                 ptx::tmem_wait_st();
@@ -398,8 +402,8 @@ __global__ void __launch_bounds__(DCfg::THREADS, 1) moe_gemm_decode_kernel(const
         __syncwarp();
         if (q == 0) __all_sync(0xFFFFFFFFu, ptx::mbar_wait(mma_done, 0, &never, LIM));
     } else if (warp < 4) {
-        // ===================== epilogue: TMEM -> registers -> global, one 16-column chunk per tile (a tile
-        // holds at most 16 token rows). W13 tiles pair warps at named barriers (1 and 2) and meet all four
+        // ===================== epilogue: TMEM -> registers -> global, one chunk of NMAX columns per term and
+        // tile. W13 tiles pair warps at named barriers (1 and 2) and meet all four
         // epilogue warps at barrier 3 before publishing the tile, so no warp leaves the loop early: after
         // a failed wait a warp skips the work but still meets the others at every barrier.
         const uint32_t t_lane = (uint32_t)(warp * 32) << 16;
@@ -411,36 +415,41 @@ __global__ void __launch_bounds__(DCfg::THREADS, 1) moe_gemm_decode_kernel(const
             const Tile &tl = d.t;
             ok = ok && __all_sync(0xFFFFFFFFu, ptx::mbar_wait(&d_full[di], dph, s_abort, LIM));
             ptx::tc_fence_after();
-            uint32_t raw[16];
+            constexpr int HALF = NMAX / 2;
+            uint32_t raw[NMAX];
 #pragma unroll
-            for (int q = 0; q < 16; ++q) raw[q] = 0u;
+            for (int q = 0; q < NMAX; ++q) raw[q] = 0u;
             if (ok) {
-                // both MMA warps wrote every tile: sum their sets' term columns in (warp, term) order
-                uint32_t part[C::MW * NT][16];
+                // both MMA warps wrote every tile: sum their sets' term columns (term t, token q at column
+                // t * NMAX + q of the set) in (warp, term) order
+                uint32_t part[C::MW][C::D_COLS];
 #pragma unroll
-                for (int u = 0; u < C::MW * NT; ++u)
-                    ptx::tmem_ld_32x32b_x16(tmem + t_lane + (uint32_t)(((u / NT) * 2 + di) * C::D_COLS + (u % NT) * NMAX),
-                                            part[u]);
+                for (int w = 0; w < C::MW; ++w)
+#pragma unroll
+                    for (int c = 0; c < C::D_COLS; c += 16)
+                        ptx::tmem_ld_32x32b_x16(tmem + t_lane + (uint32_t)((w * 2 + di) * C::D_COLS + c),
+                                                *reinterpret_cast<uint32_t (*)[16]>(&part[w][c]));
                 ptx::tmem_wait_ld();
 #pragma unroll
                 for (int u = 0; u < C::MW * NT; ++u)
 #pragma unroll
-                    for (int q = 0; q < 16; ++q) raw[q] = __float_as_uint(__uint_as_float(raw[q]) + __uint_as_float(part[u][q]));
+                    for (int q = 0; q < NMAX; ++q)
+                        raw[q] = __float_as_uint(__uint_as_float(raw[q]) + __uint_as_float(part[u / NT][(u % NT) * NMAX + q]));
             }
             if (!d.w2) {
                 const GemmParams &g = p13;
                 // lane i < 16: gate of feature f; lane i + 16: up of the same f. Lane i ends with h[f] for
-                // tokens 0 .. 7 of the tile, lane i + 16 for tokens 8 .. 15.
+                // tokens 0 .. HALF-1 of the tile, lane i + 16 for tokens HALF .. NMAX-1.
                 const bool is_gate = lane < 16;
                 const int f = tl.mb * 64 + warp * 16 + (lane & 15);
                 const float L = g.swiglu_limit;
-                float h[8], am[8];
+                float h[HALF], am[HALF];
 #pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    const float send = __uint_as_float(is_gate ? raw[8 + q] : raw[q]);
+                for (int q = 0; q < HALF; ++q) {
+                    const float send = __uint_as_float(is_gate ? raw[HALF + q] : raw[q]);
                     const float recv = __shfl_xor_sync(0xFFFFFFFFu, send, 16);
                     float gt = is_gate ? __uint_as_float(raw[q]) : recv;
-                    float up = is_gate ? recv : __uint_as_float(raw[8 + q]);
+                    float up = is_gate ? recv : __uint_as_float(raw[HALF + q]);
                     if (L > 0.f) {
                         gt = fminf(gt, L);
                         up = fminf(fmaxf(up, -L), L);
@@ -451,23 +460,23 @@ __global__ void __launch_bounds__(DCfg::THREADS, 1) moe_gemm_decode_kernel(const
                 // W2 scale blocks are 32 consecutive features: 16 in this half-warp, 16 in the partner warp
                 // (warps 0+1 and 2+3), which trade maxima through shared memory
 #pragma unroll
-                for (int q = 0; q < 8; ++q)
+                for (int q = 0; q < HALF; ++q)
 #pragma unroll
                     for (int o = 1; o < 16; o <<= 1) am[q] = fmaxf(am[q], __shfl_xor_sync(0xFFFFFFFFu, am[q], o));
                 float *pm = pairmax + (chunk & 1) * 64;
                 if ((lane & 15) == 0)
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) pm[warp * 16 + (lane >> 4) * 8 + q] = am[q];
+                    for (int q = 0; q < HALF; ++q) pm[warp * 16 + (lane >> 4) * HALF + q] = am[q];
                 ptx::bar_sync_n(1 + (warp >> 1), 64);
                 if (ok) {
                     const int blk = f >> 5;                      // W2 K-block of this feature
                     const bool writes_scale = (lane & 15) == 0 && (warp & 1) == 0;
 #pragma unroll
-                    for (int q = 0; q < 8; q += 2) {           // two token rows per conversion
-                        const float *pmq = pm + (warp ^ 1) * 16 + (lane >> 4) * 8 + q;
+                    for (int q = 0; q < HALF; q += 2) {        // two token rows per conversion
+                        const float *pmq = pm + (warp ^ 1) * 16 + (lane >> 4) * HALF + q;
                         const int e0 = mxfp8_block_exp(fmaxf(am[q], pmq[0]));
                         const int e1 = mxfp8_block_exp(fmaxf(am[q + 1], pmq[1]));
-                        const int64_t row = (int64_t)tl.row0 + (lane >> 4) * 8 + q;
+                        const int64_t row = (int64_t)tl.row0 + (lane >> 4) * HALF + q;
                         float r0 = h[q], r1 = h[q + 1];
 #pragma unroll
                         for (int term = 0; term < NT; ++term) {
@@ -493,12 +502,12 @@ __global__ void __launch_bounds__(DCfg::THREADS, 1) moe_gemm_decode_kernel(const
             } else if (ok) {
                 const GemmParams &g = p2;
                 const int c = tl.mb * TILE_ROWS + warp * 32 + lane;
-                const int my_pair = (lane < 16) ? __ldg(g.row_to_pair + tl.row0 + lane) : -1;
+                const int my_pair = (lane < NMAX) ? __ldg(g.row_to_pair + tl.row0 + lane) : -1;
                 if constexpr (FAST) {
-                    // fast combine: w * o added into the token's row of y; lane q < 16 holds row q's weight
+                    // fast combine: w * o added into the token's row of y; lane q < NMAX holds row q's weight
                     const float my_w = (my_pair >= 0 && my_pair < g.P) ? __ldg(g.topk_w + my_pair) : 0.f;
 #pragma unroll
-                    for (int q = 0; q < 16; ++q) {
+                    for (int q = 0; q < NMAX; ++q) {
                         const int pr = __shfl_sync(0xFFFFFFFFu, my_pair, q);
                         const float wq = __shfl_sync(0xFFFFFFFFu, my_w, q);
                         if (pr >= 0 && pr < g.P)
@@ -508,7 +517,7 @@ __global__ void __launch_bounds__(DCfg::THREADS, 1) moe_gemm_decode_kernel(const
                     }
                 } else {
 #pragma unroll
-                    for (int q = 0; q < 16; ++q) {
+                    for (int q = 0; q < NMAX; ++q) {
                         const int pr = __shfl_sync(0xFFFFFFFFu, my_pair, q);
                         if (pr >= 0 && pr < g.P)
                             g.staging[(int64_t)pr * g.H + c] = __uint_as_float(raw[q]);
@@ -531,36 +540,37 @@ __global__ void __launch_bounds__(DCfg::THREADS, 1) moe_gemm_decode_kernel(const
     if (warp == 8) ptx::tmem_dealloc(tmem, TMEM_COLS);
 }
 
-template <bool FAST>
+template <class C, bool FAST>
 cudaError_t launch_decode(const DecodeParams &p, int grid, cudaStream_t s, bool pdl)
 {
     static unsigned long long attr_set = 0;   // bit d: attribute set on device d
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 64 || !((attr_set >> dev) & 1ull)) {
-        cudaError_t e = cudaFuncSetAttribute(moe_gemm_decode_kernel<FAST>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)DSmem::bytes(DCfg::EMAX));
+        cudaError_t e = cudaFuncSetAttribute(moe_gemm_decode_kernel<C, FAST>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)DSmem<C>::bytes(C::EMAX));
         if (e != cudaSuccess) return e;
         if (dev < 64) __atomic_fetch_or(&attr_set, 1ull << dev, __ATOMIC_RELAXED);
     }
-    return launch_ex(moe_gemm_decode_kernel<FAST>, dim3(grid), dim3(DCfg::THREADS), DSmem::bytes(p.g13.E), s, pdl, p);
+    return launch_ex(moe_gemm_decode_kernel<C, FAST>, dim3(grid), dim3(C::THREADS), DSmem<C>::bytes(p.g13.E), s, pdl, p);
 }
 
 }  // namespace
 
 bool decode_fused_supported(int H, int I, int E)
 {
-    return E <= DCfg::EMAX && H % 256 == 0 && I % 256 == 0 && H >= 512 && I >= 512;
+    return E <= DCfg<16>::EMAX && H % 256 == 0 && I % 256 == 0 && H >= 512 && I >= 512;
 }
 
-cudaError_t launch_gemm_decode(const GemmParams &g13, const GemmParams &g2, uint32_t *done13, bool fast, int grid,
-                               cudaStream_t s, bool pdl)
+cudaError_t launch_gemm_decode(const GemmParams &g13, const GemmParams &g2, uint32_t *done13, bool fast, bool rows8,
+                               int grid, cudaStream_t s, bool pdl)
 {
     DecodeParams p;
     p.g13 = g13;
     p.g2 = g2;
     p.done13 = done13;
-    return fast ? launch_decode<true>(p, grid, s, pdl) : launch_decode<false>(p, grid, s, pdl);
+    if (rows8) return fast ? launch_decode<DCfg<8>, true>(p, grid, s, pdl) : launch_decode<DCfg<8>, false>(p, grid, s, pdl);
+    return fast ? launch_decode<DCfg<16>, true>(p, grid, s, pdl) : launch_decode<DCfg<16>, false>(p, grid, s, pdl);
 }
 
 }  // namespace moe

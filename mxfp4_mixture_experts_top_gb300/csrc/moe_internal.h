@@ -104,6 +104,8 @@ struct ForwardArgs {
     CUtensorMap tmap_w13, tmap_w13_1, tmap_w2, tmap_w2_1;   // weight nibbles: stage / single-slab boxes
     CUtensorMap tmap_xq, tmap_xq1, tmap_hq, tmap_hq1;      // activation terms: stage / one-slab boxes
     CUtensorMap tmap_xs, tmap_xs1, tmap_hs, tmap_hs1;      // their scale words
+    bool rows8;            // T <= 8: the maps below (8-row boxes of a whole stage) are set
+    CUtensorMap tmap_xq8, tmap_xs8, tmap_hq8, tmap_hs8;
     Regime regime;
     int num_sms;
     void *const *events;   // optional: 5 cudaEvent_t recorded between kernels
