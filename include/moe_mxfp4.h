@@ -167,8 +167,9 @@ moe_status_t moe_permute(const int32_t *d_topk_ids, int T, int E, int k, int blo
 
 /*
  * moe_route followed by moe_permute on the ids it writes, in one launch (one
- * thread block) for T <= 128 and in two launches above: same arguments, same
- * outputs, same bit-exactness. The fused form saves a decode step one kernel
+ * thread block) for T <= 128 and as the two calls above (two launches, four
+ * when the permutation runs chunked): same arguments, same outputs, same
+ * bit-exactness. The fused form saves a decode step one kernel
  * boundary (the first of the two steps of the fused decode path).
  * T == 0 writes counts, offsets and padded offsets (all zero) like moe_permute.
  */
