@@ -130,7 +130,7 @@ int64_t moe_permute_rows_capacity(int T, int E, int k, int block_m);
 
 /*
  * Device workspace bytes moe_permute needs for these sizes: always 0. The
- * permutation keeps its histograms and scans in shared memory, and above 4,096
+ * permutation keeps its histograms and scans in shared memory, and above 2,048
  * pairs its per-chunk counts in d_pair_to_row until it overwrites them, so the
  * caller passes no workspace; the function exists so that callers written
  * against a workspace-taking permutation can size one without special cases.
@@ -155,7 +155,7 @@ size_t moe_permute_workspace_size(int T, int E, int k, int block_m);
  *                    MOE_ERR_DEVICE if an id is outside [0, E) (that pair is
  *                    skipped and its pair_to_row entry is -1).
  * All integer outputs are bit-exact with the oracle. Runs as one thread block
- * up to 4,096 pairs. Above, three launches on chunks of consecutive pairs
+ * up to 2,048 pairs. Above, three launches on chunks of consecutive pairs
  * (chunk histograms, a per-expert scan over the chunks, the scatter); between
  * the first and the last of them d_pair_to_row holds the chunks' counts, so
  * its contents are defined only once the call's work has completed.

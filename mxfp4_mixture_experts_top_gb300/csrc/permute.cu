@@ -1,5 +1,5 @@
 // Per-expert histogram, prefix offsets, block-padded offsets and the stable
-// token permutation: one thread block for small batches, many above 4096
+// token permutation: one thread block for small batches, many above 2048
 // (token, slot) pairs.
 //
 // Method: "DeepSeek V4 Flash 单卡 MI300X" (txtmix.com) §三 — the expert
@@ -201,7 +201,7 @@ constexpr int PC_THREADS = 256;
 constexpr int PC_WARPS = PC_THREADS / 32;
 constexpr int PC_TARGET_CHUNKS = 256;            // chunks are at least P / 256 pairs
 // Above this many pairs the permutation runs chunked on many blocks.
-constexpr int64_t PERMUTE_MULTI_MIN_PAIRS = 4096;
+constexpr int64_t PERMUTE_MULTI_MIN_PAIRS = 2048;
 
 struct ChunkPlan {
     int64_t C;     // pairs per chunk (the last chunk: P - (nc - 1) * C)
@@ -215,7 +215,7 @@ static ChunkPlan chunk_plan(int64_t P, int E)
     c = (c + PC_THREADS - 1) / PC_THREADS * PC_THREADS;
     ChunkPlan pl;
     pl.C = c;
-    pl.nc = (int)(P / c);          // 1 .. 256: P > 4096 and C <= max(1024, P / 256 + 256) < P; C >= P / 256
+    pl.nc = (int)(P / c);          // 1 .. 256: P > 2048 and C <= max(1024, P / 256 + 256) < P; C >= P / 256
     return pl;
 }
 

@@ -286,7 +286,43 @@ def test_forward_fuzz_shapes(gpu_lib, gpu_layers, T, H, I, E, k):
     _compare(f"fuzz {T}x{H}x{I} E{E} k{k}", r["y"].cpu().numpy(), oracle.forward(L, ids_r, w_r))
 
 
-@pytest.mark.parametrize("block_m", [16, 64])
+@pytest.mark.parametrize("T,H,I,E,k,flags", [
+    (8, 512, 512, 64, 6, 0),           # decode, 8-row fused GEMMs: gather, GEMMs, combine
+    (8, 512, 512, 64, 6, 1),           # the same with the atomic combine: no combine kernel
+    (40, 256, 128, 1024, 6, 0),        # more than 512 experts: decode tiles in two GEMM launches
+    (300, 256, 128, 64, 6, 0),         # 28 rows per expert: two-pass gather, stacked token tiles
+    (700, 256, 256, 8, 2, 0),          # 175 rows per expert: token-major tiles
+])
+def test_forward_launches_what_its_plan_says(gpu_lib, gpu_layers, T, H, I, E, k, flags):
+    """The kernels the GPU ran for one forward, counted by the CUDA profiler, are the number
+    moe_mxfp4_forward_plan reports, and every one of them is this library's."""
+    moe = gpu_lib
+    L = synth.make_layer(T=T, H=H, E=E, k=k, I=I, seed=T + E)
+    x, logits = gpu_layers.inputs(L)
+    packed = gpu_layers.packed(L)
+    ids, w, _ = moe.route(logits, k)
+    perm = moe.permute(ids, E, 16)
+    d = moe.make_desc(T, H, I, E, k, 16, 0.0, flags)
+    ws = torch.empty(moe.workspace_bytes(d), dtype=torch.uint8, device="cuda")
+    moe.forward(d, x, packed, w, perm, ws)            # warm-up: attributes, tensor maps
+    torch.cuda.synchronize()
+    from torch.profiler import ProfilerActivity, profile
+    with profile(activities=[ProfilerActivity.CUDA]):     # the process's first session may start late
+        moe.forward(d, x, packed, w, perm, ws)
+        torch.cuda.synchronize()
+    with profile(activities=[ProfilerActivity.CUDA]) as prof:
+        moe.forward(d, x, packed, w, perm, ws)
+        torch.cuda.synchronize()
+    kernels = [e.name for e in prof.events() if e.device_type.name == "CUDA" and "memcpy" not in e.name.lower()
+               and "memset" not in e.name.lower()]
+    if not kernels:
+        pytest.skip("the CUDA profiler recorded no kernels on this host")
+    plan = moe.forward_plan(d)
+    assert all("moe" in n for n in kernels), kernels
+    assert len(kernels) == plan["launches"], (kernels, plan)
+
+
+@pytest.mark.parametrize("block_m", [16, 64, 128])
 @pytest.mark.parametrize("T,H,I,E,k,limit,zipf", [
     (1200, 512, 256, 64, 2, 0.0, False),      # 37.5 rows per expert
     (500, 256, 384, 16, 2, 10.0, False),      # 62.5 rows per expert (some above 64: two token blocks), clamp,

@@ -146,7 +146,7 @@ def test_route_permute_deterministic(gpu_lib):
 @pytest.mark.parametrize("E,k,block_m", [(256, 6, 16), (32, 6, 128), (1024, 32, 16), (8, 8, 64)])
 def test_fused_route_permute_matches_oracle(gpu_lib, T, E, k, block_m):
     """moe_route_permute (one launch up to T = 128; above, routing, then the one-block permutation up
-    to 4,096 pairs and the chunked one beyond) gives the oracle's ids, weights, bitmatrix and
+    to 2,048 pairs and the chunked one beyond) gives the oracle's ids, weights, bitmatrix and
     permutation, with heavy ties in half of the cases."""
     rng = np.random.default_rng(T * 131 + E + k)
     if T % 2:
@@ -171,7 +171,9 @@ def test_fused_route_permute_matches_oracle(gpu_lib, T, E, k, block_m):
 
 
 @pytest.mark.parametrize("T,E,k,block_m,skew", [
-    (683, 256, 6, 16, 0.0),        # 4098 pairs: just past the one-block limit
+    (342, 256, 6, 16, 0.0),        # 2052 pairs: just past the one-block limit, 8 chunks of 256
+    (300, 1024, 8, 16, 1.0),       # 2400 pairs over 1024 experts: 2 chunks of 1024 (the last takes 352 more)
+    (683, 256, 6, 16, 0.0),        # 4098 pairs
     (1366, 37, 6, 128, 8.0),       # 8196 pairs: a second chunk of 4 pairs; E not a multiple of 8
     (1024, 8, 8, 64, 0.0),         # 8192 pairs: exactly one chunk
     (8191, 256, 6, 16, 30.0),      # one expert takes nearly every token
@@ -179,7 +181,7 @@ def test_fused_route_permute_matches_oracle(gpu_lib, T, E, k, block_m):
     (20000, 5, 5, 32, 0.0),        # every token picks every expert
 ])
 def test_multi_block_permute_guards_and_skew(gpu_lib, T, E, k, block_m, skew):
-    """The many-block permutation (more than 4096 pairs) is bit-exact and writes nothing past
+    """The many-block permutation (more than 2048 pairs) is bit-exact and writes nothing past
     its outputs: every output carries guard words after its logical end."""
     moe = gpu_lib
     rng = np.random.default_rng(T + E)
