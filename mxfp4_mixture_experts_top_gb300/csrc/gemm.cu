@@ -109,7 +109,7 @@ using W2TinyWideE = Cfg<1, 16, NTH_DECODE, 2, 4, 4, 6, 1, 2, 1024>;
 // decode batches: <= 16 rows per expert
 using W13Small = Cfg<0, 32, NT_X, 2, 4, 4, 6, 1, 2, 1024, NTH_DECODE>;
 using W2Small = Cfg<1, 32, NTH_DECODE, 2, 4, 3, 4, 1, 2, 1024>;
-// <= 64 rows per expert
+// <= 64 rows per expert when H is not a multiple of 256 (else the stacked token-major tiles of gemm_rows.cu)
 using W13Mid = Cfg<0, 64, NT_X, 2, 3, 3, 6, 1, 1, 1024, NTH_MID>;
 using W2Mid = Cfg<1, 64, NTH_MID, 2, 3, 3, 6, 1, 1, 1024>;
 // prefill
@@ -939,7 +939,7 @@ Regime pick_regime(int T, int k, int E, int H)
     const double avg = (double)T * k / E;
     if (avg <= 2.0) return Regime::Tiny;
     if (avg <= 16.0) return Regime::Small;
-    if (avg <= 64.0) return Regime::Mid;
+    if (avg <= 64.0) return Regime::Mid;      // stacked 64-row token-major tiles, or weight-major 64-row ones
     if (H % 256 != 0) return Regime::Large;   // weight-major 96-row tiles
     return Regime::Huge;       // token-major tiles (gemm_rows.cu): 256 W2 output rows per tile
 }

@@ -5,14 +5,16 @@
 // expert GEMMs with SiLU(gate)*up fused into the W13 epilogue, then W2; §九 —
 // the optional SwiGLU clamp. Same tiles and arithmetic as the 16-row
 // weight-major tiles of gemm.cu (swap-AB: 128 weight rows x 16 token rows x 2
-// MXFP8 terms, two-slab stages, two MMA warps); see there for the operand and
-// scale-factor layouts.
+// MXFP8 terms, two-slab stages, two MMA warps; with at most 8 tokens, 8 token
+// rows and a sixth weight stage); see there for the operand and scale-factor
+// layouts.
 //
 // What the single launch adds: a CTA walks the W13 tiles of the tile list and
 // then the W2 tiles, all in the same rings. A W2 tile of expert e may start as
 // soon as every W13 tile of e has stored its h rows: each W13 tile's
-// epilogue, after its h stores, makes them visible to the tensor-memory
-// access proxy (fence.proxy.async) and adds one to e's counter (release);
+// epilogue, after its h stores, makes them visible to the async proxy that
+// the TMA copies of h go through (fence.proxy.async) and device-wide, and adds
+// one to e's counter (release);
 // the activation producer of a W2 tile of e waits (acquire, bounded) for the
 // counter to reach e's W13 tile count before its first copy of h. W13 tiles
 // never wait on anything of W2, so no wait is circular, and the tile list is
@@ -93,10 +95,6 @@ struct DTile {
     int w2;      // 0: W13, 1: W2
     Tile t;
 };
-
-}  // namespace
-
-namespace {
 
 template <class C, bool FAST>
 __global__ void __launch_bounds__(C::THREADS, 1) moe_gemm_decode_kernel(const __grid_constant__ DecodeParams dp)

@@ -35,6 +35,15 @@
 //     then 128-row token block, then 256-row weight block. Rows of a block past
 //     the expert's own rows (the next expert's, or the unwritten tail) are
 //     computed and never stored.
+// Stacked tiles (17 to 64 rows per expert, where 128 token rows would leave
+// most of a tile empty; block-scaled MMAs take M = 128 only): a tile is 64
+// token rows, and the A operand's 128 rows are their two terms, term 0 in rows
+// 0-63 and term 1 in rows 64-127 (the order in which the 64-row activation box
+// lands), so one MMA per 32-K block covers both terms and an activation slab
+// still serves 256 weight rows. Lane quarters 0-1 of the accumulator then hold
+// term 0's partial sums and quarters 2-3 term 1's, for the same tokens and
+// columns; warps q and q ^ 2 trade 16-column pieces through shared memory and
+// each finishes one 64-column chunk. Four weight and four activation stages.
 // Warp roles (512 threads): 0-3 and 12-15 epilogue (columns 0-127 and
 // 128-255 of lane quarter warp % 4), 4-7 scale-factor copiers, 8 MMA issuer
 // and TMEM owner, 9 activation producer, 10 weight producer, 11 idle.
