@@ -57,7 +57,8 @@ def per_expert_bytes(H, I):
     return w13, w2
 
 
-NT_X, NT_H = 2, 3   # default MXFP8 terms of the activations: x (bf16) and h = SiLU(gate)*up
+NT_X, NT_H = 2, 2   # MXFP8 terms of the activations, x (bf16) and h = SiLU(gate)*up (the library's; run-time
+                    # figures use the counts read off its workspace layout, term_counts())
 
 
 def algorithmic(L, ids, nt_x=NT_X, nt_h=NT_H):

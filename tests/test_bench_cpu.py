@@ -25,12 +25,47 @@ def test_algorithmic_counts_touched_experts_and_routed_pairs():
     a = bench.algorithmic(L, ids)
     P = T * k
     assert a["touched"] == 45
-    assert a["w13_kernel_bytes"] == 45 * 8_912_896 + 2 * P * (H + H // 32) + 3 * P * (I + I // 32)
-    assert a["w13_kernel_bytes"] == 401_789_952        # the decode figure quoted with the W13 roofline
+    assert a["w13_kernel_bytes"] == 45 * 8_912_896 + 2 * P * (H + H // 32) + 2 * P * (I + I // 32)
+    assert a["w13_kernel_bytes"] == 401_688_576        # the decode figure quoted with the W13 roofline
+    assert a["w2_kernel_bytes"] == 45 * 4_456_448 + 2 * P * (I + I // 32) + 4 * P * H
+    assert a["gemms_kernel_bytes"] == a["w13_kernel_bytes"] + a["w2_kernel_bytes"] == 603_217_920
     assert a["layer_bytes"] == 45 * (8_912_896 + 4_456_448) + T * H * 2 + T * E * 4 + T * H * 4
-    assert a["flops"] == 6.0 * P * H * I
-    # executed: W13 (2I rows) against 2 x terms, W2 (H rows) against 3 h terms
-    assert a["mma_flops"] == 2.0 * P * H * I * (2 * 2 + 3)
+    assert a["flops"] == 6.0 * P * H * I == a["gemms_flops"]
+    # executed: W13 (2I rows) against 2 x terms, W2 (H rows) against 2 h terms
+    assert a["mma_flops"] == 2.0 * P * H * I * (2 * 2 + 2) == a["gemms_mma_flops"]
+    # the library's own term counts (as bench.py reads them off the workspace layout at run time)
+    assert bench.term_counts(moe, moe.make_desc(T, H, I, E, k, 16)) == (bench.NT_X, bench.NT_H)
+
+
+class _Ev:
+    """A stand-in for a recorded CUDA event at a fixed time (ms)."""
+    def __init__(self, t):
+        self.t = t
+
+    def elapsed_time(self, other):
+        return other.t - self.t
+
+
+def test_event_pass_times_the_fused_launch_as_one_interval():
+    """Events 0..6: start, after route+permute, before the gather, after it, after W13, after W2, after
+    the combine. With both GEMMs in one launch no event sits between them: "gemms" is 3 -> 5."""
+    ev = [_Ev(t) for t in (0.0, 0.010, 0.010, 0.018, 0.5, 0.130, 0.138)]   # event 4 never recorded
+    pk, total, _ = bench.summarize([ev], fused=True)
+    assert set(pk) == {"route_permute", "gather", "gemms", "combine"}
+    assert abs(pk["gemms"] - 0.112) < 1e-12 and abs(pk["combine"] - 0.008) < 1e-12
+    ev = [_Ev(t) for t in (0.0, 0.010, 0.010, 0.018, 0.100, 0.140, 0.148)]
+    pk, _, _ = bench.summarize([ev])
+    assert abs(pk["w13"] - 0.082) < 1e-12 and abs(pk["w2"] - 0.040) < 1e-12 and "gemms" not in pk
+
+
+def test_kernel_labels_follow_the_forward_plan():
+    for T, H, want in ((8, 4096, "moe_gemm_decode_kernel"), (512, 4096, "moe_gemm_kernel<W13*>"),
+                       (2048, 4096, "W13Rows64"), (2048, 640, "moe_gemm_kernel<W13*>"),
+                       (8191, 4096, "moe_gemm_rows_kernel<W13Rows>")):
+        plan = moe.forward_plan(moe.make_desc(T, H, 2048, 256, 6, 16))
+        names = bench.kernel_names(plan, H)
+        label = names["gemms"] if plan["fused_gemms"] else names["w13"]
+        assert want in label, (T, H, plan, label)
 
 
 def test_roofline_bound_follows_the_executed_work():
