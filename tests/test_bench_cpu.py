@@ -84,6 +84,8 @@ def test_roofline_bound_follows_the_executed_work():
     assert r["bound"] == "tensor" and r["unit"] == "TFLOP/s" and r["peak"] == 2 * 1900.0
     assert abs(r["achieved"] - 4.0 * T * k * H * I / 1.4e-3 / 1e12) < 1e-9 * r["achieved"]
     assert abs(r["executed_frac"] - 2 * r["frac"]) < 1e-12
+    assert abs(r["frac_of_bf16_peak"] - 2 * r["frac"]) < 1e-12        # useful flops against the bf16 rate
+    assert abs(r["frac_of_mxfp4_peak"] - r["frac"] / 3) < 1e-12       # against 6 x bf16
 
 
 def test_both_arms_report_the_same_config():
