@@ -330,6 +330,8 @@ def test_forward_launches_what_its_plan_says(gpu_lib, gpu_layers, T, H, I, E, k,
     (40, 256, 256, 1, 1, 0.0, False),         # one expert, k = 1
     (2000, 256, 128, 1024, 16, 0.0, False),   # 1,024 experts, 31 rows each
     (1500, 512, 256, 128, 4, 0.0, True),      # skewed routing: hot experts hold several token blocks
+    (600, 768, 256, 64, 4, 0.0, False),       # 37.5 rows per expert, three 256-row W2 blocks (H = 768)
+    (1200, 256, 128, 40, 1, 10.0, False),     # k = 1, clamp
 ])
 def test_forward_stacked_token_tiles(gpu_lib, gpu_layers, T, H, I, E, k, limit, zipf, block_m):
     """17 to 64 rows per expert with H a multiple of 256 selects the token-major tiles of 64 token rows
