@@ -400,6 +400,9 @@ permute_chunk_scatter_kernel(const int32_t *__restrict__ ids, int64_t P, int E, 
 }
 
 static size_t chunk_scatter_smem(int E) { return sizeof(int) * ((size_t)E + 1 + E + E + (size_t)PC_WARPS * E); }
+// launched without raising the dynamic shared memory limit: up to 1,024 experts must fit the default 48 KB
+static_assert(sizeof(int) * (1024 + 1 + 1024 + 1024 + PC_WARPS * 1024) <= 48 * 1024,
+              "chunk scatter shared memory at 1,024 experts exceeds the default limit");
 
 static size_t permute_smem(int E) { return sizeof(int) * ((size_t)PERM_WARPS * E + E + E + 1 + 32); }
 
